@@ -1,0 +1,185 @@
+/*
+ * gemm_pipelined.h -- C ABI of the software-pipelined tiled GEMM library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the matrix product C = A x B, computed by a tiled K-loop
+ * whose global-to-shared tile loads are software-pipelined: a prologue fills
+ * the first buffers, the steady state loads tile k+1 .. k+S-1 while the MMA
+ * consumes tile k, and an epilogue drains the buffers
+ * ("CUDA Kernel Study: Pipelining", Background, Case 1 "Ping-Pong Double
+ * Buffering" and Case 2 "cp.async Multi-Stage Pipeline";
+ * "pipeline-gpu-kernel", Step 3 "restructure the K loop").  The arithmetic is
+ * the plain definition of the product ("Part 4 -- Pipelining and Occupancy",
+ * section 4.3): pipelining reorders loads, not arithmetic.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Dimensions: C is M x N, the sum runs over K.  M, N, K >= 0.
+ *  - Layouts (elements, no padding; leading dimension = the contiguous extent):
+ *      A      row-major M x K (K contiguous);
+ *      B      GP_A_ROW_B_COL: column-major K x N, i.e. stored N x K with K
+ *             contiguous (both operands K-major);
+ *             GP_A_ROW_B_ROW: row-major K x N (N contiguous);
+ *      C      row-major M x N.
+ *  - Pointers are DEVICE pointers owned by the caller; the library neither
+ *    allocates nor frees operand memory and keeps no reference after a call
+ *    returns (it caches tensor-map descriptors keyed by pointer and shape,
+ *    which hold no ownership).  Every base pointer must be 16-byte aligned.
+ *  - Calls are asynchronous on the caller's CUDA stream (a cudaStream_t passed
+ *    as void*; NULL is the legacy default stream).  Nothing synchronises
+ *    unless a function says so.
+ *  - Return value: GP_OK (0) or a negative GP_ERR_* code.  Argument errors are
+ *    detected on the host before anything is launched; the output is then
+ *    untouched.  gemm_strerror() names every code.
+ *  - Thread safety: the per-thread "last call" record read by gemm_stats() is
+ *    thread-local; everything else may be called from several host threads.
+ */
+#ifndef GEMM_PIPELINED_H
+#define GEMM_PIPELINED_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types: inputs -> accumulator -> output. */
+typedef enum {
+    GP_I8_I32 = 0,              /* int8 x int8 -> int32 sums (two's-complement wrap) -> int32 C */
+    GP_F16_F32ACC_F16OUT = 1,   /* fp16 x fp16 -> fp32 sums -> fp16 C (round to nearest even) */
+    GP_BF16_F32ACC_BF16OUT = 2, /* bf16 x bf16 -> fp32 sums -> bf16 C (round to nearest even) */
+    GP_F32 = 3                  /* fp32 x fp32 -> fp32 sums (FFMA, no tensor cores) -> fp32 C */
+} gp_dtype;
+
+typedef enum {
+    GP_A_ROW_B_COL = 0, /* A row-major, B column-major: both K-major */
+    GP_A_ROW_B_ROW = 1  /* A row-major, B row-major */
+} gp_layout;
+
+/* How the K-loop moves tiles from global to shared memory.  The MMA engine is
+ * fixed by the dtype (tcgen05 UMMA with TMEM accumulators for FP16/BF16,
+ * warp-level IMMA for INT8 -- sm_103a has no tcgen05 integer kind -- and FFMA
+ * on the CUDA cores for FP32), so variants differ only in the data path. */
+typedef enum {
+    /* Register-staged double buffer: global loads into registers, compute on
+     * the current shared buffer, then store the registers into the other one
+     * ("CUDA Kernel Study: Pipelining", Case 1; "pipeline-gpu-kernel", Step 3,
+     * LDG-register variant).  stages must be 0 or 2. */
+    GP_PINGPONG = 0,
+    /* Warp-specialised S-stage ring: a TMA producer warp fills S shared-memory
+     * slots guarded by mbarrier full/empty phases while the consumers run the
+     * MMA ("CUDA Kernel Study: Pipelining", Case 2, with TMA and mbarrier in
+     * place of cp.async commit/wait groups).  stages 1..8, 0 = default. */
+    GP_PIPELINED = 1,
+    /* No overlap: load, synchronise, compute, synchronise
+     * ("CUDA Kernel Study: Pipelining", Background).  stages must be 0 or 1. */
+    GP_NOPIPE = 2
+} gp_variant;
+
+/* Error codes. */
+#define GP_OK 0
+#define GP_ERR_ARG (-1)         /* null pointer with non-empty output, negative size, bad enum, stages out of range */
+#define GP_ERR_UNSUPPORTED (-2) /* dtype x layout x variant not built, or an alignment rule broken */
+#define GP_ERR_SMEM (-3)        /* no tile of this variant fits the per-CTA shared-memory budget at this stage count */
+#define GP_ERR_CUDA (-4)        /* a CUDA runtime call or the launch failed (detail in gp_stats.cuda_error) */
+#define GP_ERR_TIMEOUT (-5)     /* a bounded wait inside the kernel gave up; reported by gemm_stats(sync=1) */
+#define GP_ERR_SIZE (-6)        /* a dimension exceeds what the variant can address (see gemm_pipelined) */
+
+/* Tile, stage and resource choice for one problem ("pipeline-gpu-kernel",
+ * Step 1 "shared-memory budget" and Step 2 "compute/load ratio"; "Part 4 --
+ * Pipelining and Occupancy", section 4.2). */
+typedef struct gp_plan {
+    int32_t dtype, layout, variant;
+    int32_t stages;              /* shared-memory ring slots actually used */
+    int32_t bm, bn, bk;          /* CTA output tile BM x BN, K step BK */
+    int32_t threads;             /* threads per CTA */
+    int32_t stage_bytes;         /* one slot: (BM*BK + BN*BK) * sizeof(input) */
+    int32_t ring_bytes;          /* stages * stage_bytes */
+    int32_t smem_bytes;          /* dynamic shared memory per CTA (ring + epilogue staging + barriers) */
+    int32_t tmem_cols;           /* TMEM columns allocated per CTA (tcgen05 kernels), else 0 */
+    int32_t persistent;          /* 1 if CTAs loop over output tiles */
+    int32_t grid;                /* CTAs launched (0 when no device was queried) */
+    int64_t tiles;               /* output tiles ceil(M/BM) * ceil(N/BN) */
+    int64_t k_tiles;             /* ceil(K/BK) */
+    double compute_load_ratio;   /* 2*BM*BN*BK / ((BM*BK + BK*BN) * sizeof(input)), FLOP per byte */
+    const char* kernel;          /* kernel family name, static string */
+} gp_plan;
+
+/* Record of the last gemm_pipelined call made by the calling host thread. */
+typedef struct gp_stats {
+    gp_plan plan;
+    int32_t status;              /* return code of that call */
+    int32_t cuda_error;          /* cudaError_t of the failing CUDA call, else 0 */
+    int32_t regs_per_thread;     /* cudaFuncAttributes.numRegs of the kernel launched */
+    int32_t local_bytes;         /* cudaFuncAttributes.localSizeBytes (register spills) */
+    int32_t blocks_per_sm;       /* cudaOccupancyMaxActiveBlocksPerMultiprocessor at plan.smem_bytes */
+    int32_t sm_count;            /* multiprocessors of the device used */
+    uint32_t device_status;      /* kernel status word (0 = clean); valid after gemm_stats(sync=1) */
+    float last_ms;               /* kernel time from CUDA events if timing was requested, else -1 */
+} gp_stats;
+
+/* Per-call options for gemm_pipelined_ex.  Zero-initialise and set what you need. */
+typedef struct gp_options {
+    int32_t bn;                  /* force the CTA tile width BN (0 = automatic); must be one the variant builds */
+    int32_t time_kernel;         /* 1: record CUDA events around the launch; gemm_stats(sync=1) reports last_ms */
+    uint64_t timeout_ns;         /* limit of every bounded wait inside the kernel (0 = 1 s) */
+    int32_t inject_lost_load;    /* test hook: the TMA producer skips the last tile load of the problem, so a
+                                    consumer wait runs out and the call reports GP_ERR_TIMEOUT (no GPU fault) */
+    int32_t reserved[5];
+} gp_options;
+
+/*
+ * gemm_pipelined -- C = A x B on `stream`.
+ *   A, B      device pointers to the inputs (layouts above); may be NULL when M*N == 0 or K == 0.
+ *   C         device pointer to the output, written completely (every element of M x N); may be NULL
+ *             when M*N == 0 (then no argument but the enums and sizes is looked at).
+ *   M, N, K   sizes.  M == 0 or N == 0: nothing is launched.  K == 0: C is filled with zeros.
+ *   dtype     gp_dtype.  layout: gp_layout.  variant: gp_variant.
+ *   stages    shared-memory buffers in the K-loop ring; 0 picks the variant's default.
+ *   stream    cudaStream_t (as void*).
+ * Built combinations: dtype I8/F16/BF16 with GP_A_ROW_B_COL, dtype F32 with
+ * GP_A_ROW_B_ROW; every variant for each.  Alignment rules (TMA and vector
+ * loads need 16-byte rows): K % 16 == 0 for I8, K % 8 == 0 for F16/BF16,
+ * K % 4 == 0 for F32; N % 4 == 0 for I8 and F32, N % 8 == 0 for F16/BF16.
+ * M, N, K must each be below 2^31 (GP_ERR_SIZE).
+ * Errors: GP_ERR_ARG, GP_ERR_UNSUPPORTED, GP_ERR_SMEM, GP_ERR_SIZE before any
+ * launch; GP_ERR_CUDA if the launch fails.  A kernel that timed out is
+ * reported only by gemm_stats(sync=1).
+ */
+int gemm_pipelined(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
+                   int stages, int variant, void* stream);
+
+/* gemm_pipelined with options (opts may be NULL: same as gemm_pipelined). */
+int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
+                      int stages, int variant, void* stream, const gp_options* opts);
+
+/*
+ * gemm_plan -- the tile / stage / shared-memory choice gemm_pipelined would
+ * make, without touching the GPU (plan->grid is filled only if a device is
+ * present).  bn: as gp_options.bn.  Returns the same argument / budget errors
+ * gemm_pipelined would (alignment and pointer checks excepted).
+ */
+int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn,
+              gp_plan* out);
+
+/*
+ * gemm_stats -- copy the calling thread's last-call record into *out.
+ *   sync != 0: first synchronise the stream of that call, read and clear the
+ *   device status word, and compute last_ms if timing was requested.  If the
+ *   kernel reported a timed-out wait, the record's status becomes
+ *   GP_ERR_TIMEOUT and so does the return value.
+ * Returns GP_OK, GP_ERR_ARG (out == NULL) or the code described above.
+ */
+int gemm_stats(gp_stats* out, int sync);
+
+/* Static, human-readable name of an error code. */
+const char* gemm_strerror(int code);
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+int gemm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_PIPELINED_H */

@@ -1,0 +1,172 @@
+"""ctypes binding of the C ABI in include/gemm_pipelined.h.
+
+Argument marshalling only: every step of the GEMM runs in the CUDA kernels of
+libgemmpipe.so.  If the library is missing the first call raises -- there is
+no fallback of any kind.
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgemmpipe.so")
+
+# gp_dtype
+GP_I8_I32 = 0
+GP_F16_F32ACC_F16OUT = 1
+GP_BF16_F32ACC_BF16OUT = 2
+GP_F32 = 3
+# gp_layout
+GP_A_ROW_B_COL = 0
+GP_A_ROW_B_ROW = 1
+# gp_variant
+GP_PINGPONG = 0
+GP_PIPELINED = 1
+GP_NOPIPE = 2
+# error codes
+GP_OK = 0
+GP_ERR_ARG = -1
+GP_ERR_UNSUPPORTED = -2
+GP_ERR_SMEM = -3
+GP_ERR_CUDA = -4
+GP_ERR_TIMEOUT = -5
+GP_ERR_SIZE = -6
+
+DTYPES = {"i8": GP_I8_I32, "f16": GP_F16_F32ACC_F16OUT, "bf16": GP_BF16_F32ACC_BF16OUT, "f32": GP_F32}
+LAYOUTS = {"row_col": GP_A_ROW_B_COL, "row_row": GP_A_ROW_B_ROW}
+VARIANTS = {"pingpong": GP_PINGPONG, "pipelined": GP_PIPELINED, "nopipe": GP_NOPIPE}
+
+# exported symbols, in header order
+SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_stats", "gemm_strerror", "gemm_abi_version"]
+
+
+class GpPlan(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32), ("variant", ctypes.c_int32),
+        ("stages", ctypes.c_int32), ("bm", ctypes.c_int32), ("bn", ctypes.c_int32), ("bk", ctypes.c_int32),
+        ("threads", ctypes.c_int32), ("stage_bytes", ctypes.c_int32), ("ring_bytes", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32), ("persistent", ctypes.c_int32),
+        ("grid", ctypes.c_int32), ("tiles", ctypes.c_int64), ("k_tiles", ctypes.c_int64),
+        ("compute_load_ratio", ctypes.c_double), ("kernel", ctypes.c_char_p),
+    ]
+
+    def as_dict(self):
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["kernel"] = (self.kernel or b"").decode()
+        return d
+
+
+class GpStats(ctypes.Structure):
+    _fields_ = [
+        ("plan", GpPlan), ("status", ctypes.c_int32), ("cuda_error", ctypes.c_int32),
+        ("regs_per_thread", ctypes.c_int32), ("local_bytes", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
+        ("sm_count", ctypes.c_int32), ("device_status", ctypes.c_uint32), ("last_ms", ctypes.c_float),
+    ]
+
+    def as_dict(self):
+        d = {f: getattr(self, f) for f, _ in self._fields_ if f != "plan"}
+        d["plan"] = self.plan.as_dict()
+        return d
+
+
+class GpOptions(ctypes.Structure):
+    _fields_ = [
+        ("bn", ctypes.c_int32), ("time_kernel", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
+        ("inject_lost_load", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5),
+    ]
+
+
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (where, strerror(code), code))
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libgemmpipe.so is not built (run software_pipelined_tiled_pipeline_gb300.build.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    L.gemm_pipelined.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, vp]
+    L.gemm_pipelined.restype = ci
+    L.gemm_pipelined_ex.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, vp, ctypes.POINTER(GpOptions)]
+    L.gemm_pipelined_ex.restype = ci
+    L.gemm_plan.argtypes = [i64, i64, i64, ci, ci, ci, ci, ci, ctypes.POINTER(GpPlan)]
+    L.gemm_plan.restype = ci
+    L.gemm_stats.argtypes = [ctypes.POINTER(GpStats), ci]
+    L.gemm_stats.restype = ci
+    L.gemm_strerror.argtypes = [ci]
+    L.gemm_strerror.restype = ctypes.c_char_p
+    L.gemm_abi_version.argtypes = []
+    L.gemm_abi_version.restype = ci
+    _lib = L
+    return L
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()   # torch tensor (device memory)
+
+
+def _enum(val, table, name):
+    if isinstance(val, str):
+        if val not in table:
+            raise ValueError("unknown %s %r" % (name, val))
+        return table[val]
+    return int(val)
+
+
+def strerror(code: int) -> str:
+    return lib().gemm_strerror(int(code)).decode()
+
+
+def abi_version() -> int:
+    return lib().gemm_abi_version()
+
+
+def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
+                   time_kernel=False, timeout_ns=0, inject_lost_load=False, check=True) -> int:
+    """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
+    stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0."""
+    s = getattr(stream, "cuda_stream", stream)
+    opts = GpOptions()
+    opts.bn = int(bn)
+    opts.time_kernel = 1 if time_kernel else 0
+    opts.timeout_ns = int(timeout_ns)
+    opts.inject_lost_load = 1 if inject_lost_load else 0
+    rc = lib().gemm_pipelined_ex(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"),
+                                 _enum(layout, LAYOUTS, "layout"), int(stages), _enum(variant, VARIANTS, "variant"),
+                                 s or None, ctypes.byref(opts))
+    if check and rc != GP_OK:
+        raise GemmError(rc, "gemm_pipelined")
+    return rc
+
+
+def gemm_plan(M, N, K, dtype, layout, stages=0, variant="pipelined", bn=0) -> dict:
+    p = GpPlan()
+    rc = lib().gemm_plan(int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"), _enum(layout, LAYOUTS, "layout"),
+                         int(stages), _enum(variant, VARIANTS, "variant"), int(bn), ctypes.byref(p))
+    if rc != GP_OK:
+        raise GemmError(rc, "gemm_plan")
+    return p.as_dict()
+
+
+def gemm_plan_rc(M, N, K, dtype, layout, stages=0, variant="pipelined", bn=0) -> int:
+    p = GpPlan()
+    return lib().gemm_plan(int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"), _enum(layout, LAYOUTS, "layout"),
+                           int(stages), _enum(variant, VARIANTS, "variant"), int(bn), ctypes.byref(p))
+
+
+def gemm_stats(sync=True) -> dict:
+    s = GpStats()
+    lib().gemm_stats(ctypes.byref(s), 1 if sync else 0)
+    return s.as_dict()

@@ -1,0 +1,498 @@
+// api.cu -- the C ABI (include/gemm_pipelined.h): argument checks, tile and
+// stage selection against the shared-memory budget, tensor-map encoding,
+// dispatch to the kernel families, and the per-thread last-call record.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include <cudaTypedefs.h>
+
+#include "gp_internal.h"
+
+namespace gp {
+
+// Kernel status word, one per device (every device that loads the library
+// holds its own copy).  Kernels receive its address; gemm_stats(sync=1)
+// reads and clears it.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s
+constexpr int kMaxDevices = 64;
+
+// ---------------------------------------------------------------------------
+// per-device caches
+// ---------------------------------------------------------------------------
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+cudaError_t device_info(int dev, uint32_t** status, int* sms) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    g_sm_count[dev] = n;
+  }
+  *status = g_status_ptr[dev];
+  *sms = g_sm_count[dev];
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct TmapKey {
+  int dev;
+  const void* base;
+  int type;
+  uint64_t inner, outer, row_bytes;
+  uint32_t box_inner, box_outer;
+  int swizzle;
+  bool operator==(const TmapKey& o) const {
+    return dev == o.dev && base == o.base && type == o.type && inner == o.inner && outer == o.outer &&
+           row_bytes == o.row_bytes && box_inner == o.box_inner && box_outer == o.box_outer && swizzle == o.swizzle;
+  }
+};
+
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  uint64_t stamp;
+  bool used;
+};
+
+constexpr int kTmapCache = 64;
+TmapEntry g_tmaps[kTmapCache];
+uint64_t g_tmap_clock = 0;
+
+// ---------------------------------------------------------------------------
+// per-thread last-call record
+// ---------------------------------------------------------------------------
+struct LastCall {
+  gp_stats stats;
+  int device = -1;
+  cudaStream_t stream = nullptr;
+  const void* kernel = nullptr;
+  bool timed = false;
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  int ev_device = -1;
+  bool valid = false;
+};
+thread_local LastCall t_last;
+
+int family_of(int dtype) {
+  switch (dtype) {
+    case GP_F32: return 0;                                   // FFMA
+    case GP_I8_I32: return 1;                                // IMMA
+    default: return 2;                                       // UMMA
+  }
+}
+
+int in_elem_bytes(int dtype) {
+  switch (dtype) {
+    case GP_I8_I32: return 1;
+    case GP_F32: return 4;
+    default: return 2;
+  }
+}
+
+int out_elem_bytes(int dtype) { return dtype == GP_I8_I32 || dtype == GP_F32 ? 4 : 2; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int default_stages(int family) { return family == 0 ? 3 : 4; }
+
+// Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
+int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
+              int sm_count, gp_plan* p) {
+  if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
+  if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
+  if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
+  if (M < 0 || N < 0 || K < 0) return GP_ERR_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GP_ERR_SIZE;
+  if (bn_req < 0) return GP_ERR_ARG;
+  const int fam = family_of(dtype);
+  if (fam == 0 && layout != GP_A_ROW_B_ROW) return GP_ERR_UNSUPPORTED;
+  if (fam != 0 && layout != GP_A_ROW_B_COL) return GP_ERR_UNSUPPORTED;
+
+  int S;
+  if (variant == GP_NOPIPE) {
+    if (stages != 0 && stages != 1) return GP_ERR_ARG;
+    S = 1;
+  } else if (variant == GP_PINGPONG) {
+    if (stages != 0 && stages != 2) return GP_ERR_ARG;
+    S = 2;
+  } else {
+    if (stages < 0 || stages > kMaxStages) return GP_ERR_ARG;
+    S = stages == 0 ? default_stages(fam) : stages;
+  }
+
+  std::memset(p, 0, sizeof(*p));
+  p->dtype = dtype;
+  p->layout = layout;
+  p->variant = variant;
+  p->stages = S;
+  const bool ring = variant == GP_PIPELINED;
+
+  int cands[3] = {0, 0, 0};
+  int ncand = 0;
+  int extra = 0;
+  if (fam == 0) {
+    p->bm = kFfmaBM;
+    p->bk = kFfmaBK;
+    cands[ncand++] = kFfmaBN;
+    p->threads = ring ? 288 : 256;
+    p->kernel = ring ? "ffma_ring" : (variant == GP_PINGPONG ? "ffma_pingpong" : "ffma_nopipe");
+  } else if (fam == 1) {
+    p->bm = kImmaBM;
+    p->bk = kImmaBK;
+    cands[ncand++] = 128;
+    cands[ncand++] = 64;
+    p->threads = ring ? 288 : 256;
+    p->kernel = ring ? "imma_ring" : (variant == GP_PINGPONG ? "imma_pingpong" : "imma_nopipe");
+  } else {
+    p->bm = kUmmaBM;
+    p->bk = kUmmaBK;
+    cands[ncand++] = 256;
+    cands[ncand++] = 128;
+    cands[ncand++] = 64;
+    extra = kUmmaEpiBytes;
+    p->threads = ring ? 192 : 256;
+    p->kernel = ring ? "umma_ring" : (variant == GP_PINGPONG ? "umma_pingpong" : "umma_nopipe");
+  }
+  auto stage_bytes = [&](int bn) {
+    if (fam == 0) return kFfmaStageBytes;
+    if (fam == 1) return imma_stage_bytes(bn);
+    return umma_stage_bytes(bn);
+  };
+  auto fits = [&](int bn) { return ring_smem_total(S * stage_bytes(bn), extra) <= kSmemPerCtaMax; };
+
+  int bn = 0;
+  if (bn_req) {
+    bool known = false;
+    for (int i = 0; i < ncand; ++i) known |= (cands[i] == bn_req);
+    if (!known) return GP_ERR_UNSUPPORTED;
+    if (!fits(bn_req)) return GP_ERR_SMEM;
+    bn = bn_req;
+  } else {
+    for (int i = 0; i < ncand; ++i) {
+      const int c = cands[i];
+      const bool smaller_covers = (i + 1 < ncand) && (c / 2 >= N);
+      if (fits(c) && !smaller_covers) { bn = c; break; }
+    }
+    if (!bn) {
+      for (int i = 0; i < ncand; ++i)
+        if (fits(cands[i])) { bn = cands[i]; break; }
+    }
+    if (!bn) return GP_ERR_SMEM;
+  }
+  p->bn = bn;
+  p->stage_bytes = stage_bytes(bn);
+  p->ring_bytes = S * p->stage_bytes;
+  p->smem_bytes = ring_smem_total(p->ring_bytes, extra);
+  if (fam == 2) {
+    p->tmem_cols = ring ? 2 * bn : bn;
+    if (ring && p->smem_bytes < kSmemPerCtaMax / 2 + 1024) {
+      // a persistent CTA holds 2*BN TMEM columns for its whole life: keep one CTA per SM
+      p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
+    }
+  }
+  p->persistent = (ring && fam != 0) ? 1 : 0;
+  p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
+  p->k_tiles = ceil_div(K, p->bk);
+  if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
+  if (p->persistent)
+    p->grid = sm_count > 0 ? static_cast<int32_t>(p->tiles < sm_count ? p->tiles : sm_count) : 0;
+  else
+    p->grid = static_cast<int32_t>(p->tiles);
+  const double e = in_elem_bytes(dtype);
+  p->compute_load_ratio = 2.0 * p->bm * p->bn * p->bk / ((static_cast<double>(p->bm) * p->bk + p->bk * p->bn) * e);
+  return GP_OK;
+}
+
+int alignment_ok(const void* A, const void* B, const void* C, int64_t N, int64_t K, int dtype) {
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+                         reinterpret_cast<uintptr_t>(C)) & 15u;
+  if (mis) return 0;
+  switch (dtype) {
+    case GP_I8_I32: return (K % 16 == 0) && (N % 4 == 0);
+    case GP_F32: return (K % 4 == 0) && (N % 4 == 0);
+    default: return (K % 8 == 0) && (N % 8 == 0);
+  }
+}
+
+void record(int status, int cuda_err) {
+  t_last.stats.status = status;
+  t_last.stats.cuda_error = cuda_err;
+  t_last.valid = true;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// helpers used by the kernel translation units
+// ---------------------------------------------------------------------------
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType type, uint64_t inner,
+                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                         CUtensorMapSwizzle swizzle) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  TmapKey key{dev, base, static_cast<int>(type), inner, outer, row_bytes, box_inner, box_outer,
+              static_cast<int>(swizzle)};
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& t : g_tmaps) {
+    if (t.used && t.key == key) {
+      t.stamp = ++g_tmap_clock;
+      *map = t.map;
+      return cudaSuccess;
+    }
+  }
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  const CUresult r = g_encode(&m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TmapEntry* victim = &g_tmaps[0];
+  for (auto& t : g_tmaps) {
+    if (!t.used) { victim = &t; break; }
+    if (t.stamp < victim->stamp) victim = &t;
+  }
+  victim->key = key;
+  victim->map = m;
+  victim->stamp = ++g_tmap_clock;
+  victim->used = true;
+  *map = m;
+  return cudaSuccess;
+}
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (done.count({dev, kernel})) return cudaSuccess;
+  }
+  if (bytes > kSmemPerCtaMax) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCtaMax);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  done.insert({dev, kernel});
+  return cudaSuccess;
+}
+
+namespace {
+__global__ void zero_fill_kernel(uint4* p, int64_t n16) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride)
+    p[i] = make_uint4(0, 0, 0, 0);
+}
+}  // namespace
+
+cudaError_t launch_zero_fill(void* C, int64_t bytes, cudaStream_t stream) {
+  const int64_t n16 = bytes / 16;   // output rows are multiples of 16 bytes under the alignment rules
+  if (n16 <= 0) return cudaSuccess;
+  int64_t blocks = (n16 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  zero_fill_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<uint4*>(C), n16);
+  return cudaGetLastError();
+}
+
+}  // namespace gp
+
+using namespace gp;
+
+extern "C" {
+
+int gemm_abi_version(void) { return 10000; }
+
+const char* gemm_strerror(int code) {
+  switch (code) {
+    case GP_OK: return "ok";
+    case GP_ERR_ARG: return "invalid argument";
+    case GP_ERR_UNSUPPORTED: return "unsupported dtype/layout/variant combination or alignment";
+    case GP_ERR_SMEM: return "no tile fits the shared-memory budget at this stage count";
+    case GP_ERR_CUDA: return "CUDA runtime or launch error";
+    case GP_ERR_TIMEOUT: return "a bounded wait inside the kernel timed out";
+    case GP_ERR_SIZE: return "a dimension is too large for this kernel";
+    default: return "unknown error code";
+  }
+}
+
+int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn,
+              gp_plan* out) {
+  if (!out) return GP_ERR_ARG;
+  int sms = 0;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  } else {
+    cudaGetLastError();   // clear the sticky "no device" error of the probe
+  }
+  return plan_impl(M, N, K, dtype, layout, stages, variant, bn, sms, out);
+}
+
+int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
+                      int stages, int variant, void* stream, const gp_options* opts) {
+  std::memset(&t_last.stats, 0, sizeof(t_last.stats));
+  t_last.stats.last_ms = -1.f;
+  t_last.kernel = nullptr;
+  t_last.timed = false;
+  t_last.stream = static_cast<cudaStream_t>(stream);
+  const int bn_req = opts ? opts->bn : 0;
+
+  // argument checks that need no device
+  gp_plan plan;
+  int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan);
+  if (rc != GP_OK) { record(rc, 0); return rc; }
+  t_last.stats.plan = plan;
+  if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }   // empty output: nothing read or written
+  if (!C || (K > 0 && (!A || !B))) {
+    record(GP_ERR_ARG, 0);
+    return GP_ERR_ARG;
+  }
+  if (!alignment_ok(A, B, C, N, K, dtype)) { record(GP_ERR_UNSUPPORTED, 0); return GP_ERR_UNSUPPORTED; }
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (e == cudaSuccess) e = device_info(dev, &status, &sms);
+  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  t_last.device = dev;
+  t_last.stats.sm_count = sms;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool timed = opts && opts->time_kernel;
+  if (timed) {
+    if (t_last.ev_device != dev) {
+      if (t_last.ev[0]) { cudaEventDestroy(t_last.ev[0]); cudaEventDestroy(t_last.ev[1]); }
+      t_last.ev[0] = t_last.ev[1] = nullptr;
+      if ((e = cudaEventCreate(&t_last.ev[0])) != cudaSuccess || (e = cudaEventCreate(&t_last.ev[1])) != cudaSuccess) {
+        record(GP_ERR_CUDA, e);
+        return GP_ERR_CUDA;
+      }
+      t_last.ev_device = dev;
+    }
+    cudaEventRecord(t_last.ev[0], st);
+  }
+
+  if (K == 0) {
+    e = launch_zero_fill(C, M * N * out_elem_bytes(dtype), st);
+  } else {
+    rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan);
+    if (rc != GP_OK) { record(rc, 0); return rc; }
+    LaunchArgs a;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.M = static_cast<int32_t>(M);
+    a.N = static_cast<int32_t>(N);
+    a.K = static_cast<int32_t>(K);
+    a.dtype = dtype;
+    a.layout = layout;
+    a.variant = variant;
+    a.plan = plan;
+    a.stream = st;
+    a.ctl.status = status;
+    a.ctl.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
+    a.ctl.inject_lost_load = opts ? opts->inject_lost_load : 0;
+    a.sm_count = sms;
+    const void* kernel = nullptr;
+    switch (family_of(dtype)) {
+      case 0: e = launch_ffma(a, &kernel); break;
+      case 1: e = launch_imma(a, &kernel); break;
+      default: e = launch_umma(a, &kernel); break;
+    }
+    t_last.stats.plan = a.plan;
+    t_last.kernel = kernel;
+  }
+  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  if (timed) {
+    cudaEventRecord(t_last.ev[1], st);
+    t_last.timed = true;
+  }
+  record(GP_OK, 0);
+  return GP_OK;
+}
+
+int gemm_pipelined(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
+                   int stages, int variant, void* stream) {
+  return gemm_pipelined_ex(A, B, C, M, N, K, dtype, layout, stages, variant, stream, nullptr);
+}
+
+int gemm_stats(gp_stats* out, int sync) {
+  if (!out) return GP_ERR_ARG;
+  if (!t_last.valid) {
+    std::memset(out, 0, sizeof(*out));
+    out->last_ms = -1.f;
+    return GP_OK;
+  }
+  gp_stats& s = t_last.stats;
+  if (sync && t_last.device >= 0 && s.status == GP_OK) {
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != t_last.device) cudaSetDevice(t_last.device);
+    cudaError_t e = cudaStreamSynchronize(t_last.stream);
+    if (e == cudaSuccess) {
+      uint32_t word = 0;
+      e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word));
+      if (e == cudaSuccess && word != 0) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
+        s.device_status = word;
+        s.status = GP_ERR_TIMEOUT;
+      }
+    }
+    if (e != cudaSuccess) {
+      s.status = GP_ERR_CUDA;
+      s.cuda_error = e;
+    } else if (t_last.timed) {
+      float ms = -1.f;
+      if (cudaEventElapsedTime(&ms, t_last.ev[0], t_last.ev[1]) == cudaSuccess) s.last_ms = ms;
+      t_last.timed = false;
+    }
+    if (prev != t_last.device) cudaSetDevice(prev);
+  }
+  if (t_last.kernel && s.regs_per_thread == 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, t_last.kernel) == cudaSuccess) {
+      s.regs_per_thread = fa.numRegs;
+      s.local_bytes = static_cast<int32_t>(fa.localSizeBytes);
+    }
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, t_last.kernel, s.plan.threads, s.plan.smem_bytes) ==
+        cudaSuccess)
+      s.blocks_per_sm = occ;
+  }
+  *out = s;
+  return s.status;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// gp_internal.h -- declarations shared by the host API and the kernel
+// translation units of the pipelined GEMM library.  Not installed; the public
+// interface is include/gemm_pipelined.h.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_pipelined.h"
+
+namespace gp {
+
+// ---------------------------------------------------------------------------
+// device status word
+// ---------------------------------------------------------------------------
+constexpr uint32_t kDevErrTimeout = 1;  // a bounded wait gave up
+
+// wait-site codes (bits 8.. of the status word) -- which wait gave up
+enum WaitSite : uint32_t {
+  kSiteProducerEmpty = 1,
+  kSiteConsumerFull = 2,
+  kSiteMmaAccEmpty = 3,
+  kSiteEpilogueAccFull = 4,
+  kSitePingPongMma = 5,
+  kSiteDrain = 6,
+};
+
+struct KernelCtl {
+  uint32_t* status;         // device word, 0 = clean
+  uint64_t timeout_ns;      // limit of every bounded wait
+  int32_t inject_lost_load; // test hook: producer skips the final tile load
+};
+
+// ---------------------------------------------------------------------------
+// shared-memory budget
+// ---------------------------------------------------------------------------
+constexpr int kSmemPerCtaMax = 232448;   // 227 KB opt-in dynamic shared memory per CTA on sm_100/sm_103
+constexpr int kSmemAlignSlack = 1024;    // dynamic smem base is re-aligned to 1024 B (128-byte swizzle atoms)
+constexpr int kBarrierRegion = 256;      // mbarriers, TMEM address slot, abort flag
+constexpr int kMaxStages = 8;
+
+// FFMA (FP32) family: CTA tile 128 x 128 x 8, 8 compute warps, 8x8 outputs per thread.
+constexpr int kFfmaBM = 128, kFfmaBN = 128, kFfmaBK = 8;
+constexpr int kFfmaStageBytes = (kFfmaBM * kFfmaBK + kFfmaBK * kFfmaBN) * 4;
+
+// IMMA (INT8) family: CTA tile 128 x BN x 128, BN in {128, 64}; 8 compute warps (2 x 4).
+constexpr int kImmaBM = 128, kImmaBK = 128;
+__host__ __device__ constexpr int imma_stage_bytes(int bn) { return (kImmaBM + bn) * kImmaBK; }
+
+// UMMA (FP16/BF16, tcgen05) family: CTA tile 128 x BN x 64, BN in {256, 128, 64}.
+constexpr int kUmmaBM = 128, kUmmaBK = 64;
+constexpr int kUmmaEpiWarps = 4;
+constexpr int kUmmaEpiRows = 32;         // rows per epilogue warp (one TMEM lane quarter)
+constexpr int kUmmaEpiCols = 64;         // 16-bit columns per staged chunk (128 bytes)
+constexpr int kUmmaEpiBufBytes = kUmmaEpiRows * kUmmaEpiCols * 2;
+constexpr int kUmmaEpiBytes = kUmmaEpiWarps * 2 * kUmmaEpiBufBytes;   // double-buffered per warp
+__host__ __device__ constexpr int umma_stage_bytes(int bn) { return (kUmmaBM + bn) * kUmmaBK * 2; }
+
+__host__ __device__ constexpr int ring_smem_total(int ring_bytes, int extra) {
+  return kSmemAlignSlack + ring_bytes + extra + kBarrierRegion;
+}
+
+// ---------------------------------------------------------------------------
+// launch interface between the API and the kernel translation units
+// ---------------------------------------------------------------------------
+struct LaunchArgs {
+  const void* A;
+  const void* B;
+  void* C;
+  int32_t M, N, K;
+  int32_t dtype, layout, variant;
+  gp_plan plan;
+  cudaStream_t stream;
+  KernelCtl ctl;
+  int32_t sm_count;
+};
+
+// Each family launcher fills *kernel with the function launched (for
+// cudaFuncGetAttributes) and returns a cudaError_t.
+cudaError_t launch_ffma(LaunchArgs& a, const void** kernel);
+cudaError_t launch_imma(LaunchArgs& a, const void** kernel);
+cudaError_t launch_umma(LaunchArgs& a, const void** kernel);
+cudaError_t launch_zero_fill(void* C, int64_t bytes, cudaStream_t stream);
+
+// Tensor-map encoding (driver entry point obtained once through the runtime).
+// inner/outer: extents in elements; row_bytes: stride of the outer dimension.
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType type, uint64_t inner,
+                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                         CUtensorMapSwizzle swizzle);
+
+// Opt a kernel into more than 48 KB of dynamic shared memory (cached per device).
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+}  // namespace gp

@@ -1,0 +1,273 @@
+// k_ffma.cu -- FP32 SGEMM on the CUDA cores (FFMA, no tensor cores), in the
+// configuration of "CUDA Kernel Study: Pipelining", Kernel Parameters: CTA
+// tile 128 x 128 x 8, 16 x 16 = 256 compute threads, 8 x 8 outputs per thread
+// accumulated in registers as outer products ("Part 4 -- Pipelining and
+// Occupancy", section 4.3, register tiling).  A is row-major M x K, B
+// row-major K x N, C row-major M x N.
+//
+// Three data paths for the K-loop, sharing the shared-memory layout (A tile
+// [128][8], B tile [8][128], as a TMA box copy lays them out) and the compute:
+//  * ffma_ring_kernel    -- a TMA producer warp fills an S-slot ring guarded by
+//                           mbarrier full/empty phases; 8 compute warps
+//                           consume it (Case 2 with TMA + mbarrier).
+//  * ffma_staged_kernel<PINGPONG=true>  -- register-staged double buffer (Case 1).
+//  * ffma_staged_kernel<PINGPONG=false> -- no overlap (Background).
+#include "gp_device.cuh"
+
+namespace gp {
+namespace {
+
+constexpr int BM = kFfmaBM, BN = kFfmaBN, BK = kFfmaBK;
+constexpr int A_FLOATS = BM * BK;          // 1024
+constexpr int STAGE = kFfmaStageBytes;     // 8192
+constexpr int kComputeThreads = 256;
+constexpr int kComputeWarps = 8;
+
+struct FfmaBarriers {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  int32_t consumed;
+  CtaCtl ctl;
+};
+static_assert(sizeof(FfmaBarriers) <= kBarrierRegion, "barrier region too small");
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int& mb, int& nb) {
+  constexpr int GM = 8;
+  const int per_group = GM * n_blocks;
+  const int group = tile / per_group;
+  const int first_m = group * GM;
+  const int gm = min(GM, m_blocks - first_m);
+  const int in_group = tile - group * per_group;
+  mb = first_m + in_group % gm;
+  nb = in_group / gm;
+}
+
+// Thread (tx, ty) of the 16 x 16 compute grid owns rows ty + 16*i (i < 8) and
+// columns tx*4 + {0..3} and 64 + tx*4 + {0..3}.  Rows 16 apart put the two
+// rows a warp reads from A (ty = 0, 1) 32 bytes apart, in different banks.
+struct Acc {
+  float c[8][8];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[i][j] = 0.f;
+  }
+};
+
+__device__ __forceinline__ void ffma_kblock(const float* __restrict__ As, const float* __restrict__ Bs, int tx,
+                                            int ty, Acc& acc) {
+#pragma unroll
+  for (int kh = 0; kh < BK; kh += 4) {
+    float a[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = *reinterpret_cast<const float4*>(As + (ty + 16 * i) * BK + kh);
+      a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 b0 = *reinterpret_cast<const float4*>(Bs + (kh + q) * BN + tx * 4);
+      const float4 b1 = *reinterpret_cast<const float4*>(Bs + (kh + q) * BN + 64 + tx * 4);
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc.c[i][j] = fmaf(a[i][q], b[j], acc.c[i][j]);
+    }
+  }
+}
+
+__device__ __forceinline__ void ffma_store(float* C, int M, int N, int m0, int n0, int tx, int ty, const Acc& acc) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = m0 + ty + 16 * i;
+    if (r >= M) continue;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = n0 + h * 64 + tx * 4;
+      if (col < N)   // N % 4 == 0: the float4 is entirely inside
+        *reinterpret_cast<float4*>(C + static_cast<size_t>(r) * N + col) =
+            make_float4(acc.c[i][4 * h], acc.c[i][4 * h + 1], acc.c[i][4 * h + 2], acc.c[i][4 * h + 3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA ring: 8 compute warps + 1 producer warp, one tile per CTA
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
+    ffma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     float* __restrict__ C, int M, int N, int K, int stages, KernelCtl ctl) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = align1024(smem_raw);
+  FfmaBarriers* bar = reinterpret_cast<FfmaBarriers*>(ring + stages * STAGE);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
+  int mb, nb;
+  tile_coords(blockIdx.x, m_blocks, n_blocks, mb, nb);
+  const int kt = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&bar->full[s], 1);
+      mbar_init(&bar->empty[s], kComputeWarps);
+    }
+    bar->ctl.abort = 0;
+    bar->consumed = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  CtaCtl* cta = &bar->ctl;
+  int issued = 0;
+
+  if (warp == kComputeWarps) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int s = 0;
+      uint32_t ph = 0;
+      const bool last_tile = blockIdx.x == gridDim.x - 1;
+      for (int kb = 0; kb < kt; ++kb) {
+        if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) break;
+        if (!(ctl.inject_lost_load && last_tile && kb == kt - 1)) {
+          uint8_t* slot = ring + s * STAGE;
+          mbar_arrive_expect_tx(&bar->full[s], STAGE);
+          tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, mb * BM);
+          tma_load_2d(smem_u32(slot + A_FLOATS * 4), &tmB, &bar->full[s], nb * BN, kb * BK);
+          ++issued;
+        }
+        if (++s == stages) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else {
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    Acc acc;
+    acc.zero();
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int consumed = 0;
+    for (int kb = 0; kb < kt; ++kb) {
+      const bool w = mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      const float* As = reinterpret_cast<const float*>(ring + s * STAGE);
+      ffma_kblock(As, As + A_FLOATS, tx, ty, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->empty[s]);
+      ++consumed;
+      if (++s == stages) { s = 0; ph ^= 1u; }
+    }
+    if (ok) ffma_store(C, M, N, mb * BM, nb * BN, tx, ty, acc);
+    if (threadIdx.x == 0) bar->consumed = consumed;
+  }
+
+  __syncthreads();
+  if (cta->abort && warp == kComputeWarps && lane == 0) {
+    CtaCtl never_abort{0};
+    for (int i = bar->consumed; i < issued; ++i)
+      mbar_wait(&bar->full[i % stages], static_cast<uint32_t>((i / stages) & 1), ctl, &never_abort, kSiteDrain);
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// register-staged ping-pong / no-overlap (256 threads)
+// ---------------------------------------------------------------------------
+struct RegStage {
+  float4 a, b;
+  // A: thread t loads row t/2, k-quad t%2; B: row t/32, column quad t%32
+  __device__ __forceinline__ void load(const float* A, const float* B, int M, int N, int K, int m0, int n0, int kb) {
+    const int t = threadIdx.x;
+    const int k0 = kb * BK;
+    const int gm = m0 + (t >> 1), gk = k0 + (t & 1) * 4;
+    a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (gm < M && gk < K) a = __ldg(reinterpret_cast<const float4*>(A + static_cast<size_t>(gm) * K + gk));
+    const int bk = k0 + (t >> 5), bn = n0 + (t & 31) * 4;
+    b = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bk < K && bn < N) b = __ldg(reinterpret_cast<const float4*>(B + static_cast<size_t>(bk) * N + bn));
+  }
+  __device__ __forceinline__ void store(uint8_t* slot) const {
+    const int t = threadIdx.x;
+    float* As = reinterpret_cast<float*>(slot);
+    float* Bs = As + A_FLOATS;
+    *reinterpret_cast<float4*>(As + (t >> 1) * BK + (t & 1) * 4) = a;
+    *reinterpret_cast<float4*>(Bs + (t >> 5) * BN + (t & 31) * 4) = b;
+  }
+};
+
+template <bool PINGPONG>
+__global__ void __launch_bounds__(kComputeThreads, 1)
+    ffma_staged_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C, int M, int N,
+                       int K) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = align1024(smem_raw);
+  const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
+  int mb, nb;
+  tile_coords(blockIdx.x, m_blocks, n_blocks, mb, nb);
+  const int m0 = mb * BM, n0 = nb * BN;
+  const int kt = (K + BK - 1) / BK;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+
+  Acc acc;
+  acc.zero();
+  RegStage rs;
+  if (PINGPONG) {
+    rs.load(A, B, M, N, K, m0, n0, 0);
+    rs.store(ring);
+    __syncthreads();
+    for (int kb = 0; kb < kt; ++kb) {
+      const int cur = kb & 1;
+      if (kb + 1 < kt) rs.load(A, B, M, N, K, m0, n0, kb + 1);   // in flight during the compute
+      const float* As = reinterpret_cast<const float*>(ring + cur * STAGE);
+      ffma_kblock(As, As + A_FLOATS, tx, ty, acc);
+      if (kb + 1 < kt) rs.store(ring + (cur ^ 1) * STAGE);   // last read in iteration kb-1
+      __syncthreads();
+    }
+  } else {
+    for (int kb = 0; kb < kt; ++kb) {
+      rs.load(A, B, M, N, K, m0, n0, kb);
+      rs.store(ring);
+      __syncthreads();
+      const float* As = reinterpret_cast<const float*>(ring);
+      ffma_kblock(As, As + A_FLOATS, tx, ty, acc);
+      __syncthreads();
+    }
+  }
+  ffma_store(C, M, N, m0, n0, tx, ty, acc);
+}
+
+}  // namespace
+
+cudaError_t launch_ffma(LaunchArgs& a, const void** kernel) {
+  gp_plan& p = a.plan;
+  cudaError_t e;
+  if (a.variant == GP_PIPELINED) {
+    CUtensorMap tmA, tmB;
+    const uint64_t M = a.M, N = a.N, K = a.K;
+    if ((e = make_tmap_2d(&tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, K, M, K * 4, BK, BM,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+      return e;
+    if ((e = make_tmap_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, K, N * 4, BN, BK,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+      return e;
+    *kernel = reinterpret_cast<const void*>(ffma_ring_kernel);
+    if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
+    ffma_ring_kernel<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(tmA, tmB, static_cast<float*>(a.C), a.M, a.N,
+                                                                     a.K, p.stages, a.ctl);
+  } else {
+    auto k = (a.variant == GP_PINGPONG) ? ffma_staged_kernel<true> : ffma_staged_kernel<false>;
+    *kernel = reinterpret_cast<const void*>(k);
+    if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
+    k<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(static_cast<const float*>(a.A), static_cast<const float*>(a.B),
+                                                      static_cast<float*>(a.C), a.M, a.N, a.K);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gp

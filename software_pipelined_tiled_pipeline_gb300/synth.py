@@ -20,6 +20,9 @@ Distributions (the shapes of the pages' synthetic square GEMM workloads):
   u2 = (d >> 11) * 2^-53, z = sqrt(-2 ln u1) cos(2 pi u2), scaled by 1/sqrt(K),
   rounded to float32 and then to bfloat16 (both round-to-nearest-even).
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -49,10 +52,20 @@ def draws(seed: int, tensor_id: int, start: int, count: int) -> np.ndarray:
 
 
 def _fill(n, fn, dtype, seed, tensor_id):
+    """Generate in chunks of draws (several threads: numpy releases the GIL)."""
     out = np.empty(n, dtype=dtype)
-    for s in range(0, n, _CHUNK):
+    starts = list(range(0, n, _CHUNK))
+
+    def work(s):
         c = min(_CHUNK, n - s)
         out[s:s + c] = fn(seed, tensor_id, s, c)
+
+    if len(starts) <= 1:
+        for s in starts:
+            work(s)
+    else:
+        with ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 1, 16)) as ex:
+            list(ex.map(work, starts))
     return out
 
 

@@ -1,0 +1,167 @@
+"""Host-side checks of the C ABI (no GPU): the library loads and exports every
+symbol the header declares, argument errors are reported before anything is
+launched, and the tile / stage / shared-memory choice follows the budget
+rules ("pipeline-gpu-kernel", Step 1 and Step 2)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from software_pipelined_tiled_pipeline_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def gp():
+    gbuild.build()
+    import software_pipelined_tiled_pipeline_gb300 as mod
+    mod.lib()
+    return mod
+
+
+def header_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\([^;{]*\)\s*;", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_function(gp):
+    names = header_functions()
+    assert "gemm_pipelined" in names and "gemm_stats" in names
+    L = ctypes.CDLL(gbuild.LIB)
+    for n in names:
+        assert hasattr(L, n), "symbol %s declared in include/ but not exported" % n
+    from software_pipelined_tiled_pipeline_gb300 import _binding
+    assert sorted(_binding.SYMBOLS) == sorted(names)
+
+
+def test_version_and_strerror(gp):
+    assert gp.abi_version() == 10000
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert gp.strerror(code) and "unknown" not in gp.strerror(code)
+    assert "unknown" in gp.strerror(-99)
+
+
+def test_struct_sizes_match_c_layout():
+    from software_pipelined_tiled_pipeline_gb300 import _binding as b
+    assert ctypes.sizeof(b.GpPlan) == 88
+    assert ctypes.sizeof(b.GpStats) == 120
+    assert ctypes.sizeof(b.GpOptions) == 40
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(dtype=7), -1), (dict(layout=5), -1), (dict(variant=9), -1),
+    (dict(M=-1), -1), (dict(K=-3), -1), (dict(M=1 << 31), -6),
+    (dict(stages=9), -1), (dict(stages=-1), -1),
+    (dict(variant=0, stages=3), -1), (dict(variant=2, stages=2), -1),
+    (dict(dtype=3, layout=0), -2), (dict(dtype=0, layout=1), -2),
+    (dict(bn=96), -2), (dict(bn=256, stages=8), -3), (dict(bn=-1), -1),
+])
+def test_plan_argument_errors(gp, args, code):
+    a = dict(M=256, N=256, K=256, dtype=1, layout=0, stages=4, variant=1, bn=0)
+    a.update(args)
+    rc = gp.gemm_plan_rc(a["M"], a["N"], a["K"], a["dtype"], a["layout"], a["stages"], a["variant"], a["bn"])
+    assert rc == code
+
+
+def test_call_argument_errors_need_no_device(gp):
+    L = gp.lib()
+    f = L.gemm_pipelined
+    ok_ptr = 0x10000
+    # null output with a non-empty result
+    assert f(ok_ptr, ok_ptr, None, 64, 64, 64, 1, 0, 4, 1, None) == gp.GP_ERR_ARG
+    assert f(None, ok_ptr, ok_ptr, 64, 64, 64, 1, 0, 4, 1, None) == gp.GP_ERR_ARG
+    # misaligned base pointer
+    assert f(ok_ptr + 8, ok_ptr, ok_ptr, 64, 64, 64, 1, 0, 4, 1, None) == gp.GP_ERR_UNSUPPORTED
+    # K not a multiple of 16 bytes of row for INT8 / FP16, N rule for C rows
+    assert f(ok_ptr, ok_ptr, ok_ptr, 64, 64, 40, 0, 0, 4, 1, None) == gp.GP_ERR_UNSUPPORTED
+    assert f(ok_ptr, ok_ptr, ok_ptr, 64, 64, 36, 1, 0, 4, 1, None) == gp.GP_ERR_UNSUPPORTED
+    assert f(ok_ptr, ok_ptr, ok_ptr, 64, 60, 64, 1, 0, 4, 1, None) == gp.GP_ERR_UNSUPPORTED
+    assert f(ok_ptr, ok_ptr, ok_ptr, 64, 62, 64, 3, 1, 2, 1, None) == gp.GP_ERR_UNSUPPORTED
+    # empty output: nothing to do, no device touched
+    assert f(None, None, None, 0, 64, 64, 1, 0, 4, 1, None) == gp.GP_OK
+    assert f(None, None, None, 64, 0, 64, 0, 0, 4, 1, None) == gp.GP_OK
+    st = gp.gemm_stats(sync=False)
+    assert st["status"] == 0
+
+
+@pytest.mark.parametrize("S,bn", [(1, 256), (2, 256), (3, 256), (4, 256), (5, 128), (6, 128), (7, 64), (8, 64)])
+def test_umma_tile_shrinks_with_stages(gp, S, bn):
+    p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined")
+    assert p["bm"] == 128 and p["bk"] == 64 and p["bn"] == bn and p["stages"] == S
+    assert p["stage_bytes"] == (128 + bn) * 64 * 2
+    assert p["ring_bytes"] == S * p["stage_bytes"]
+    assert p["smem_bytes"] <= 232448
+    assert p["tmem_cols"] == 2 * bn and p["persistent"] == 1
+    assert p["tiles"] == (4096 // 128) * (4096 // bn) and p["k_tiles"] == 64
+
+
+@pytest.mark.parametrize("S,bn", [(1, 128), (4, 128), (6, 128), (7, 128), (8, 64)])
+def test_imma_tile_shrinks_with_stages(gp, S, bn):
+    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined")
+    assert p["bn"] == bn and p["bk"] == 128 and p["stage_bytes"] == (128 + bn) * 128
+    assert p["k_tiles"] == 32 and p["smem_bytes"] <= 232448
+
+
+def test_small_n_picks_narrow_tile(gp):
+    assert gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 4, "pipelined")["bn"] == 128
+    assert gp.gemm_plan(8192, 64, 8192, "bf16", "row_col", 4, "pipelined")["bn"] == 64
+    assert gp.gemm_plan(256, 100 + 4, 256, "i8", "row_col", 4, "pipelined")["bn"] == 128
+
+
+def test_default_stages_and_variant_stage_rules(gp):
+    assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pipelined")["stages"] == 4
+    assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pingpong")["stages"] == 2
+    assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "nopipe")["stages"] == 1
+    assert gp.gemm_plan(512, 512, 512, "f32", "row_row", 0, "pipelined")["stages"] == 3
+
+
+def test_compute_load_ratio_is_the_pages_formula(gp):
+    for dtype, layout, esize in (("f16", "row_col", 2), ("i8", "row_col", 1), ("f32", "row_row", 4)):
+        p = gp.gemm_plan(4096, 4096, 4096, dtype, layout, 2, "pipelined")
+        bm, bn, bk = p["bm"], p["bn"], p["bk"]
+        assert p["compute_load_ratio"] == pytest.approx(2 * bm * bn * bk / ((bm * bk + bk * bn) * esize))
+    # FP16 128x256x64: 2*128*256*64 / ((128*64 + 64*256) * 2) = 85.33 FLOP/byte, far above the 20:1 line
+    p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 4, "pipelined")
+    assert p["compute_load_ratio"] == pytest.approx(85.333, rel=1e-4)
+
+
+def test_ffma_tile_matches_pages_kernel_table(gp):
+    g = json.load(open(os.path.join(GOLDEN, "p1_kernel_table.json")))
+    t = g["tile"]
+    M = g["problem"]["M"]
+    nop = gp.gemm_plan(M, M, M, "f32", "row_row", 1, "nopipe")
+    pp = gp.gemm_plan(M, M, M, "f32", "row_row", 2, "pingpong")
+    ring2 = gp.gemm_plan(M, M, M, "f32", "row_row", 2, "pipelined")
+    assert (nop["bm"], nop["bn"], nop["bk"], nop["threads"]) == (t["bm"], t["bn"], t["bk"], t["threads"])
+    assert nop["k_tiles"] == g["k_tiles"]
+    kb = g["static_smem_per_block_kb"]
+    assert round(nop["ring_bytes"] / 1000, 2) == kb["baseline"]
+    assert round(pp["ring_bytes"] / 1000, 2) == kb["ping_pong"]
+    assert round(ring2["ring_bytes"] / 1000, 2) == kb["cp_async_2stage"]
+
+
+def test_throughput_formula_matches_pages_benchmark():
+    from software_pipelined_tiled_pipeline_gb300.workloads import Workload
+    g = json.load(open(os.path.join(GOLDEN, "p1_kernel_table.json")))
+    M = g["problem"]["M"]
+    w = Workload("p1", "f32", "row_row", M, M, M)
+    for row in g["benchmark"]:
+        gflops = w.ops / (row["avg_ms"] * 1e-3) / 1e9
+        # the printed time has 3 decimals: +-0.0005 ms
+        slack = w.ops / ((row["avg_ms"] - 0.0005) * 1e-3) / 1e9 - gflops
+        assert abs(gflops - row["gflops"]) <= slack + 0.05
+
+
+def test_double_buffer_rule_matches_pages_example():
+    g = json.load(open(os.path.join(GOLDEN, "p2_smem_budget.json")))
+    # single buffer 2 KB + 2 KB -> doubled 8 KB
+    assert 2 * g["single_buffer_kb"] == g["double_buffer_kb"]

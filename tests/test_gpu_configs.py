@@ -1,0 +1,70 @@
+"""GPU parity at the full sizes of the measured workloads, in the launch
+configurations the benchmark times.  INT8 4096^3 and the small configs are
+compared with the oracle element by element; the large float configs on
+sampled rows and points the oracle computes one by one, plus the
+stage/variant invariance (identical bits across ring depths)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import check_full, check_sampled, operands, run
+from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype in (torch.float16, torch.bfloat16) else t
+
+
+@pytest.mark.parametrize("name", ["i8_256", "f32_1024"])
+def test_small_configs_full_compare(name):
+    w = WORKLOADS[name]
+    A, B = operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    for variant in w.variants:
+        stages = w.stages if variant == "pipelined" else (0,)
+        for S in stages:
+            C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant=variant, stages=S)
+            check_full(w.dtype, w.layout, A, B, C, w.K)
+
+
+def test_i8_4096_bit_exact_every_stage_and_variant():
+    w = WORKLOADS["i8_4096"]
+    A, B = operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    ref, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4)
+    check_full(w.dtype, w.layout, A, B, ref, w.K)           # every element against the oracle
+    for S in w.stages:
+        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
+        assert torch.equal(C, ref)
+    for variant in ("pingpong", "nopipe"):
+        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant=variant)
+        assert torch.equal(C, ref)
+
+
+def test_f16_4096_sampled_and_stage_invariant():
+    w = WORKLOADS["f16_4096"]
+    A, B = operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    ref, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4)
+    rows = list(range(0, 4096, 67)) + [4095]
+    check_sampled(w.dtype, w.layout, A, B, ref, w.K, rows=rows, npts=4000, seed=1)
+    for S in w.stages:
+        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
+        assert torch.equal(_bits(C), _bits(ref))
+    for variant in ("pingpong", "nopipe"):
+        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant=variant)
+        assert torch.equal(_bits(C), _bits(ref))
+
+
+@pytest.mark.parametrize("name", ["bf16_8192_k256", "bf16_8192_k1024", "bf16_8192_k4096", "bf16_8192_k16384",
+                                  "bf16_skinny"])
+def test_bf16_sweep_configs(name):
+    w = WORKLOADS[name]
+    A, B = operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    ref = None
+    for S in w.stages:
+        C, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
+        if ref is None:
+            rows = [0, 1, 127, 128, 4095, 8191] if w.K > 4096 else list(range(0, w.M, 257)) + [w.M - 1]
+            check_sampled(w.dtype, w.layout, A, B, C, w.K, rows=rows, npts=2000, seed=S)
+            ref = C
+        assert torch.equal(_bits(C), _bits(ref)), "stage %d differs" % S

@@ -1,0 +1,180 @@
+"""GPU parity: the CUDA kernels, called through the C ABI, against the CPU
+oracle, element by element (bit-exact for INT8; max|C - C_ref| <=
+1e-2 * sqrt(K/256) * max|C_ref| for FP16/BF16/FP32).
+
+Sizes span several CTA tiles and ragged tails in M, N and K; every variant
+(no overlap, register ping-pong, TMA ring) and every ring depth 1..8 is run.
+Targeted cases follow the pitfalls of "pipeline-gpu-kernel" (Common pitfalls:
+a dropped epilogue loses the last K slab; an off-by-one buffer index swaps
+slabs; the loop-count edge cases num_tiles in {1, S-1, S, S+1, 2S+1}; K not a
+multiple of BK) and its invariant (Step 5 item 4): pipelining only reorders
+loads, so all variants and depths give identical outputs for a fixed MMA
+order."""
+import numpy as np
+import pytest
+import torch
+
+import software_pipelined_tiled_pipeline_gb300 as gp
+from gpu_helpers import check_full, check_sampled, host_float, operands, run, to_dev
+
+pytestmark = pytest.mark.gpu
+
+LAYOUT = {"i8": "row_col", "f16": "row_col", "bf16": "row_col", "f32": "row_row"}
+BK = {"i8": 128, "f16": 64, "bf16": 64, "f32": 8}
+SMALL = {
+    "i8": [(256, 256, 256), (300, 196, 400), (129, 68, 16), (520, 260, 1040)],
+    "f16": [(256, 256, 256), (300, 264, 200), (130, 72, 8), (520, 392, 776)],
+    "bf16": [(256, 256, 256), (300, 264, 200), (130, 72, 8), (520, 392, 776)],
+    "f32": [(256, 256, 128), (300, 260, 100), (129, 132, 4), (384, 512, 264)],
+}
+VARIANTS = ["nopipe", "pingpong", "pipelined"]
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16", "f32"])
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("idx", range(4))
+def test_small_shapes(dtype, variant, idx):
+    M, N, K = SMALL[dtype][idx]
+    lay = LAYOUT[dtype]
+    A, B = operands(dtype, lay, M, N, K, seed=100 + idx)
+    C, st = run(dtype, lay, A, B, M, N, K, variant=variant)
+    check_full(dtype, lay, A, B, C, K)
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16", "f32"])
+@pytest.mark.parametrize("stages", range(1, 9))
+def test_ring_every_depth(dtype, stages):
+    M, N, K = SMALL[dtype][3]
+    lay = LAYOUT[dtype]
+    A, B = operands(dtype, lay, M, N, K, seed=7)
+    C, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=stages)
+    assert st["plan"]["stages"] == stages
+    check_full(dtype, lay, A, B, C, K)
+
+
+@pytest.mark.parametrize("dtype,bn", [("f16", 256), ("f16", 128), ("f16", 64), ("bf16", 256), ("bf16", 64),
+                                      ("i8", 128), ("i8", 64)])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_every_tile_width(dtype, bn, variant):
+    M, N, K = 264, 520, 392 if dtype != "i8" else 384
+    lay = LAYOUT[dtype]
+    A, B = operands(dtype, lay, M, N, K, seed=11)
+    C, st = run(dtype, lay, A, B, M, N, K, variant=variant, bn=bn)
+    assert st["plan"]["bn"] == bn
+    check_full(dtype, lay, A, B, C, K)
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16", "f32"])
+@pytest.mark.parametrize("S", [2, 3, 4])
+@pytest.mark.parametrize("nt_of", ["1", "S-1", "S", "S+1", "2S+1"])
+def test_k_tile_counts_around_depth(dtype, S, nt_of):
+    nt = {"1": 1, "S-1": S - 1, "S": S, "S+1": S + 1, "2S+1": 2 * S + 1}[nt_of]
+    if nt < 1:
+        pytest.skip("no K tiles")
+    lay = LAYOUT[dtype]
+    M, N, K = 192, 136, nt * BK[dtype]
+    A, B = operands(dtype, lay, M, N, K, seed=nt)
+    C, _ = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S)
+    check_full(dtype, lay, A, B, C, K)
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16", "f32"])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_only_last_k_slab_nonzero(dtype, variant):
+    # a dropped drain/epilogue would silently lose exactly this slab
+    lay = LAYOUT[dtype]
+    M, N = 200, 136
+    K = 5 * BK[dtype] + (16 if dtype == "i8" else 8)   # ragged last slab
+    A, B = operands(dtype, lay, M, N, K, seed=3)
+    last = (K // BK[dtype]) * BK[dtype]
+    A = A.copy()
+    B = B.copy()
+    A[:, :last] = 0
+    if lay == "row_col":
+        B[:, :last] = 0
+    else:
+        B[:last, :] = 0
+    C, _ = run(dtype, lay, A, B, M, N, K, variant=variant, stages=3 if variant == "pipelined" else 0)
+    check_full(dtype, lay, A, B, C, K)
+    assert np.any(host_float(C) != 0)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_i8_slab_order_is_kept(variant):
+    # K slab t of A holds the constant t+1 and B a fixed random slab: any
+    # swapped or repeated slab changes C.
+    M, N, nt = 128, 128, 9
+    K = nt * 128
+    A = np.zeros((M, K), np.int8)
+    for t in range(nt):
+        A[:, t * 128:(t + 1) * 128] = t + 1
+    rng = np.random.default_rng(5)
+    B = rng.integers(-128, 128, (N, K)).astype(np.int8)
+    C, _ = run("i8", "row_col", A, B, M, N, K, variant=variant, stages=4 if variant == "pipelined" else 0)
+    check_full("i8", "row_col", A, B, C, K)
+
+
+@pytest.mark.parametrize("dtype", ["i8", "f16", "bf16", "f32"])
+def test_k_zero_gives_zeros(dtype):
+    lay = LAYOUT[dtype]
+    M, N = 72, 64
+    A = np.zeros((M, 0), np.int8 if dtype == "i8" else np.float32)
+    tC = torch.full((M, N), 7, dtype=torch.float32 if dtype != "i8" else torch.int32, device="cuda")
+    if dtype in ("f16", "bf16"):
+        tC = tC.to(torch.float16 if dtype == "f16" else torch.bfloat16)
+    dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    gp.gemm_pipelined(dummy, dummy, tC, M, N, 0, dtype, lay, 0, "pipelined", torch.cuda.current_stream())
+    assert gp.gemm_stats(sync=True)["status"] == 0
+    assert bool((tC.float() == 0).all())
+    del A
+
+
+def test_empty_output_is_not_touched():
+    tC = torch.full((4, 8), 3.0, dtype=torch.float16, device="cuda")
+    gp.gemm_pipelined(None, None, tC, 0, 8, 64, "f16", "row_col", 0, "pipelined", 0)
+    torch.cuda.synchronize()
+    assert bool((tC == 3.0).all())
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32", "i8"])
+def test_all_variants_and_depths_bitwise_identical(dtype):
+    # pipelining only reorders loads: with the same MMA sequence the outputs agree bit for bit
+    lay = LAYOUT[dtype]
+    M, N, K = 264, 392, 520 if dtype != "i8" else 512
+    A, B = operands(dtype, lay, M, N, K, seed=21)
+    ref, _ = run(dtype, lay, A, B, M, N, K, variant="nopipe")
+    check_full(dtype, lay, A, B, ref, K)
+    outs = [run(dtype, lay, A, B, M, N, K, variant="pingpong")[0]]
+    for S in range(1, 9):
+        outs.append(run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S)[0])
+    for o in outs:
+        assert torch.equal(o.view(torch.int16) if o.dtype in (torch.float16, torch.bfloat16) else o,
+                           ref.view(torch.int16) if ref.dtype in (torch.float16, torch.bfloat16) else ref)
+
+
+def test_repeat_calls_reuse_cached_descriptors():
+    A, B = operands("f16", "row_col", 512, 512, 512, seed=2)
+    c1, _ = run("f16", "row_col", A, B, 512, 512, 512)
+    c2, _ = run("f16", "row_col", A, B, 512, 512, 512)
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "i8", "f32"])
+def test_lost_load_reports_timeout_and_context_survives(dtype):
+    # test hook: the producer skips the final tile load, a consumer's bounded
+    # wait runs out, the kernel exits cleanly and the host sees GP_ERR_TIMEOUT
+    lay = LAYOUT[dtype]
+    M, N, K = 256, 256, 4 * BK[dtype]
+    A, B = operands(dtype, lay, M, N, K, seed=1)
+    tA, tB = to_dev(A, dtype), to_dev(B, dtype)
+    out = {"i8": torch.int32, "f16": torch.float16, "f32": torch.float32}[dtype]
+    tC = torch.empty((M, N), dtype=out, device="cuda")
+    gp.gemm_pipelined(tA, tB, tC, M, N, K, dtype, lay, 2, "pipelined", torch.cuda.current_stream(),
+                      timeout_ns=20_000_000, inject_lost_load=True)
+    st = gp.gemm_stats(sync=True)
+    assert st["status"] == gp.GP_ERR_TIMEOUT
+    assert st["device_status"] & 0xFF == 1
+    # the context is still usable and the status word was cleared
+    C, st2 = run(dtype, lay, A, B, M, N, K)
+    assert st2["device_status"] == 0
+    check_full(dtype, lay, A, B, C, K)
