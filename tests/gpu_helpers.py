@@ -62,7 +62,7 @@ def check_full(dtype, layout, A, B, C, K):
     got = host_float(C)
     assert np.all(np.isfinite(got)), "non-finite output (unwritten element?)"
     err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
-    tol = oracle.tolerance(K, ref)
+    tol = oracle.tolerance(K, ref, dtype)
     assert err <= tol, "max err %g > tol %g" % (err, tol)
     return err
 
@@ -80,7 +80,7 @@ def check_sampled(dtype, layout, A, B, C, K, rows=None, npts=0, seed=0):
             ref = oracle.gemm_ref(A, B, dtype, layout, rows=rows)
             got = host_float(C)[rows]
             err = float(np.max(np.abs(got - ref)))
-            tol = oracle.tolerance(K, ref)
+            tol = oracle.tolerance(K, ref, dtype)
             assert err <= tol, "max err %g > tol %g on sampled rows" % (err, tol)
     if npts:
         r = rng.integers(0, M, npts)
@@ -92,7 +92,7 @@ def check_sampled(dtype, layout, A, B, C, K, rows=None, npts=0, seed=0):
             ref = oracle.points_ref(A, B, dtype, r, c, layout)
             got = host_float(C)[r, c]
             err = float(np.max(np.abs(got - ref)))
-            tol = oracle.tolerance(K, ref)
+            tol = oracle.tolerance(K, ref, dtype)
             assert err <= tol, "max err %g > tol %g on sampled points" % (err, tol)
 
 

@@ -84,7 +84,7 @@ def test_only_last_k_slab_nonzero(dtype, variant):
     # a dropped drain/epilogue would silently lose exactly this slab
     lay = LAYOUT[dtype]
     M, N = 200, 136
-    K = 5 * BK[dtype] + (16 if dtype == "i8" else 8)   # ragged last slab
+    K = 5 * BK[dtype] + {"i8": 16, "f16": 8, "bf16": 8, "f32": 4}[dtype]   # ragged last slab
     A, B = operands(dtype, lay, M, N, K, seed=3)
     last = (K // BK[dtype]) * BK[dtype]
     A = A.copy()

@@ -341,3 +341,18 @@ def test_tolerance_formula():
     c = np.array([[-3.0, 2.0], [1.0, 0.5]])
     assert oracle.tolerance(256, c) == pytest.approx(0.03)
     assert oracle.tolerance(1024, c) == pytest.approx(0.06)
+    assert oracle.tolerance(1024, c, "bf16") == pytest.approx(0.06)
+    # below K ~ 39 the stated bound is under one bfloat16 rounding: floored at 2^-8
+    assert oracle.tolerance(8, c, "bf16") == pytest.approx(3 * 2.0 ** -8)
+    assert oracle.tolerance(8, c, "f16") == pytest.approx(1e-2 * (8 / 256) ** 0.5 * 3)
+
+
+def test_tolerance_admits_correct_rounding_of_exact_result():
+    # a correctly rounded bfloat16 output of the exact sum must always pass
+    rng = np.random.default_rng(14)
+    for K in (1, 2, 8, 40, 256):
+        A = _as_type(rng.uniform(-1, 1, (16, K)), "bf16")
+        B = _as_type(rng.uniform(-1, 1, (16, K)), "bf16")
+        ref = oracle.gemm_ref(A, B, "bf16", "row_col")
+        rounded = oracle.decode_bf16(oracle.round_bf16(ref))
+        assert np.max(np.abs(rounded - ref)) <= oracle.tolerance(K, ref, "bf16")
