@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""Benchmark of the software-pipelined tiled GEMM library on GB300.
+
+One step = one GEMM over the workload (all steps of the K-loop hot path:
+tile decomposition, prologue, steady-state ring, drain, output epilogue).
+Default workload: FP16 GEMM M=N=K=4096, A row-major, B column-major, FP32
+accumulate, FP16 out, TMA-ring tcgen05 kernel at 4 stages.  Prints ONE JSON
+line (rank 0).  The INT8 4096^3 result, the stage sweep and the FP32
+ping-pong-vs-async comparison ride along as sub-objects.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--stages S] [--no-sweep] [--sweep-bf16]
+
+--impl reference times the CPU oracle (the reference arm of this build) on a
+bounded row sample of the same workload on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "INT8 TOPS and FP16 TFLOPS at 4096^3 (fraction of GB300 dense peak) vs stages"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1920.0, "bf16_tflops_sustained": 1700.0}
+ROTATE = 4            # operand/output buffer sets cycled between steps (working set > L2)
+L2_BYTES = 129e6
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="f16_4096")
+    ap.add_argument("--stages", type=int, default=4)
+    ap.add_argument("--variant", default="pipelined")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-bf16", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["_source"] = "measured (MEASURED_PEAKS.json)"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["_source"] = "fallback (profiling recipe)"
+    return d
+
+
+# ---------------------------------------------------------------------------
+# clocks: nvidia-smi sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="gp_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+            os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        import datetime
+        def ts(p):
+            try:
+                return datetime.datetime.strptime(p, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        inside = [r for r in rows if ts(r[0]) is not None and t0 <= ts(r[0]) <= t1]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in inside if num(r[2]) is not None]
+        mx = [num(r[3]) for r in inside if num(r[3]) is not None]
+        pw = [num(r[4]) for r in inside if num(r[4]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(inside),
+                "window": window}
+
+
+# ---------------------------------------------------------------------------
+# device-side timing helpers
+# ---------------------------------------------------------------------------
+def to_device(torch, x, dtype, dev):
+    import numpy as np
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+
+OUT_TORCH = {"i8": "int32", "f16": "float16", "bf16": "bfloat16", "f32": "float32"}
+
+
+def device_sets(torch, w, A, B, dev, sets):
+    tA = to_device(torch, A, w.dtype, dev)
+    tB = to_device(torch, B, w.dtype, dev)
+    out = []
+    for i in range(sets):
+        a = tA if i == 0 else tA.clone()
+        b = tB if i == 0 else tB.clone()
+        c = torch.empty((w.M, w.N), dtype=getattr(torch, OUT_TORCH[w.dtype]), device=dev)
+        out.append((a, b, c))
+    return out
+
+
+def time_kernel(torch, gp, w, bufs, variant, stages, n, stream, bn=0):
+    """Average device time of n launches (CUDA events around each launch on `stream`)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        a, b, c = bufs[i % len(bufs)]
+        evs[i][0].record(stream)
+        gp.gemm_pipelined(a, b, c, w.M, w.N, w.K, w.dtype, w.layout, stages, variant, stream, bn=bn)
+        evs[i][1].record(stream)
+    stream.synchronize()
+    st = gp.gemm_stats(sync=True)
+    if st["status"] != 0:
+        raise RuntimeError("kernel status %d" % st["status"])
+    ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    return statistics.mean(ms), min(ms), st
+
+
+def sweep(torch, gp, dev, stream, names, steps):
+    from software_pipelined_tiled_pipeline_gb300 import synth
+    from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
+    out = {}
+    for name in names:
+        w = WORKLOADS[name]
+        A, B = synth.operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+        bufs = device_sets(torch, w, A, B, dev, ROTATE if w.M * w.K < (1 << 27) else 2)
+        unit = "TOPS" if w.dtype == "i8" else "TFLOPS"
+        rows = []
+        cases = [("nopipe", 1), ("pingpong", 2)] + [("pipelined", s) for s in w.stages]
+        for variant, S in cases:
+            time_kernel(torch, gp, w, bufs, variant, S, 3, stream)      # warm-up
+            avg, best, st = time_kernel(torch, gp, w, bufs, variant, S, steps, stream)
+            rows.append({"variant": variant, "stages": S, "bn": st["plan"]["bn"], "ms": round(avg, 4),
+                         unit: round(w.ops / (avg * 1e-3) / 1e12, 2),
+                         "regs": st["regs_per_thread"], "smem": st["plan"]["smem_bytes"]})
+        base = next(r for r in rows if r["variant"] == "pingpong")[unit]
+        for r in rows:
+            r["vs_pingpong"] = round(r[unit] / base, 3) if base else None
+        out[name] = {"unit": unit, "rows": rows}
+        del bufs
+        torch.cuda.empty_cache()
+    return out
+
+
+def source_sha(name):
+    path = os.path.join(ROOT, "software_pipelined_tiled_pipeline_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "software_pipelined_tiled_pipeline_gb300", "csrc", "gp_device.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key, src):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(kernel_key)
+    if not d or d.get("source_sha") != source_sha(src):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, A, B, seconds):
+    """Time the oracle on the first R rows of C, R sized to take about `seconds`."""
+    import numpy as np
+    import oracle
+    run = (lambda rows: oracle.gemm_i8(A, B, w.layout, rows=rows)) if w.dtype == "i8" else \
+        (lambda rows: oracle.gemm_ref(A, B, w.dtype, w.layout, rows=rows))
+    r = min(16, w.M)
+    t0 = time.perf_counter()
+    run(np.arange(r))
+    t = time.perf_counter() - t0
+    R = int(min(w.M, max(r, r * seconds / max(t, 1e-6))))
+    t0 = time.perf_counter()
+    run(np.arange(R))
+    t = time.perf_counter() - t0
+    ops = 2.0 * R * w.N * w.K
+    return ops / t / 1e12, R, t, oracle.threads()
+
+
+def run_reference(args, rank):
+    from software_pipelined_tiled_pipeline_gb300 import synth
+    from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    A, B = synth.operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    import numpy as np
+    import oracle
+    unit = "TOPS" if w.dtype == "i8" else "TFLOPS"
+    run = (lambda rows: oracle.gemm_i8(A, B, w.layout, rows=rows)) if w.dtype == "i8" else \
+        (lambda rows: oracle.gemm_ref(A, B, w.dtype, w.layout, rows=rows))
+    # size one step so the whole --warmup + --steps run takes about 60 s
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    r = min(8, w.M)
+    t0 = time.perf_counter()
+    run(np.arange(r))
+    t = time.perf_counter() - t0
+    R = int(min(w.M, max(1, r * budget / max(t, 1e-6))))
+    rows = np.arange(R)
+    for _ in range(args.warmup):
+        run(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(rows)
+    el = time.perf_counter() - t0
+    value = 2.0 * R * w.N * w.K * args.steps / el / 1e12
+    sample = "first %d of %d rows of C per step (%d x %d x %d MACs)" % (R, w.M, R, w.N, w.K)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "M": w.M, "N": w.N, "K": w.K,
+                   "sample_rows": R},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import numpy as np
+    import torch
+    import software_pipelined_tiled_pipeline_gb300 as gp
+    from software_pipelined_tiled_pipeline_gb300 import synth
+    from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    gp.lib()   # fails loudly if the CUDA library is missing
+
+    w = WORKLOADS[args.workload]
+    unit = "TOPS" if w.dtype == "i8" else "TFLOPS"
+    A, B = synth.operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    bufs = device_sets(torch, w, A, B, dev, ROTATE)
+    stream = torch.cuda.Stream(dev)
+    peaks = load_peaks()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    def gemm(i):
+        a, b, c = bufs[i % len(bufs)]
+        gp.gemm_pipelined(a, b, c, w.M, w.N, w.K, w.dtype, w.layout, args.stages, args.variant, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            gemm(i)
+        stream.synchronize()
+        st = gp.gemm_stats(sync=True)
+        if st["status"] != 0:
+            raise RuntimeError("warm-up failed: status %d" % st["status"])
+
+        sampler = ClockSampler(local)
+        sampler.start()
+        # ---- timed region: K steps, barrier + synchronize on both sides ----
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t_start.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            gemm(i)
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.time()
+        barrier()
+        clock_rows = sampler.stop()
+        st = gp.gemm_stats(sync=True)
+        if st["status"] != 0:
+            raise RuntimeError("timed region failed: status %d" % st["status"])
+        total_ms = t_start.elapsed_time(t_end)
+        kern_ms = [a.elapsed_time(b) for a, b in evs]
+
+    if pg is not None:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = w.ops * world * args.steps / (total_ms * 1e-3) / 1e12
+    kavg = statistics.mean(kern_ms)
+    achieved = w.ops / (kavg * 1e-3) / 1e12
+
+    # ---- end to end: pinned host operands in, result out, every step ----
+    hA = to_device(torch, A, w.dtype, "cpu").pin_memory()
+    hB = to_device(torch, B, w.dtype, "cpu").pin_memory()
+    hC = torch.empty((w.M, w.N), dtype=getattr(torch, OUT_TORCH[w.dtype])).pin_memory()
+    e2e_steps = max(1, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        dA, dB, dC = bufs[0]
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            gp.gemm_pipelined(dA, dB, dC, w.M, w.N, w.K, w.dtype, w.layout, args.stages, args.variant, stream)
+            hC.copy_(dC, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = w.ops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+
+    plan = st["plan"]
+    kernel_src = {"umma": "k_umma.cu", "imma": "k_imma.cu", "ffma": "k_ffma.cu"}[plan["kernel"].split("_")[0]]
+    kernel_key = "%s@%s" % (plan["kernel"], w.name)
+    if w.dtype in ("f16", "bf16"):
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
+                    "peak_source": peaks["_source"] + ": dense bf16 burst (FP16 runs at the same tcgen05 rate)",
+                    "kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5)}
+    elif w.dtype == "i8":
+        peak = gp.probe_peak("imma_s8", stream) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TOPS",
+                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
+                    "peak_source": "measured IMMA mma.sync s8 probe (gemm_probe_peak)", "kernel": plan["kernel"],
+                    "kernel_avg_ms": round(kavg, 5)}
+    else:
+        peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
+                    "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz", "kernel": plan["kernel"],
+                    "kernel_avg_ms": round(kavg, 5)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "M": w.M, "N": w.N, "K": w.K,
+                   "layout": w.layout, "variant": args.variant, "stages": plan["stages"], "bm": plan["bm"],
+                   "bn": plan["bn"], "bk": plan["bk"], "grid": plan["grid"], "smem_bytes": plan["smem_bytes"],
+                   "regs_per_thread": st["regs_per_thread"],
+                   "l2": "operands and output rotated over %d buffer sets (%.0f MiB > 129 MB L2)" % (
+                       ROTATE, ROTATE * (A.nbytes + B.nbytes + w.M * w.N * (4 if w.dtype in ("i8", "f32") else 2))
+                       / 2 ** 20),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
+                "d2h_bytes_per_step": int(hC.numel() * hC.element_size()), "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": ClockSampler.summarize(clock_rows, wall0, wall1),
+    }
+
+    extra_steps = max(10, min(args.steps, 50))
+    if not args.no_sweep:
+        names = ["f16_4096", "i8_4096", "f32_1024"]
+        if args.sweep_bf16:
+            names += ["bf16_8192_k256", "bf16_8192_k1024", "bf16_8192_k4096", "bf16_8192_k16384", "bf16_skinny"]
+        del bufs
+        torch.cuda.empty_cache()
+        sw = sweep(torch, gp, dev, stream, names, extra_steps)
+        line["sweep"] = sw
+        i8 = sw.get("i8_4096")
+        if i8:
+            best = max((r for r in i8["rows"] if r["variant"] == "pipelined"), key=lambda r: r["TOPS"])
+            ipeak = gp.probe_peak("imma_s8", stream) / 1e12
+            line["int8"] = {"workload": "i8_4096", "value": best["TOPS"], "unit": "TOPS", "stages": best["stages"],
+                            "peak": round(ipeak, 1), "frac": round(best["TOPS"] / ipeak, 4),
+                            "peak_source": "measured IMMA mma.sync s8 probe (gemm_probe_peak)",
+                            "vs_pingpong": best["vs_pingpong"]}
+        f16 = sw.get("f16_4096")
+        if f16:
+            best = max((r for r in f16["rows"] if r["variant"] == "pipelined"), key=lambda r: r["TFLOPS"])
+            line["fp16_best_stage"] = {"stages": best["stages"], "TFLOPS": best["TFLOPS"],
+                                       "frac": round(best["TFLOPS"] / peaks.get("bf16_tflops", 1920.0), 4)}
+        line["ffma_peak_probe_tflops"] = round(gp.probe_peak("ffma_f32", stream) / 1e12, 2)
+
+    if not args.no_cpu_baseline and world == 1:
+        v, R, t, cores = oracle_sample(w, A, B, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": unit, "cores": cores, "kind": "oracle",
+                                "sample": "first %d of %d rows of C (%d x %d x %d MACs) in %.1f s" % (
+                                    R, w.M, R, w.N, w.K, t)}
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,37 @@
+/*
+ * gemm_probe.h -- measured throughput ceilings for the roofline of the GEMM
+ * library's kernels (part of libgemmpipe.so).
+ *
+ * The pages measure their kernels against the hardware's own limits ("CUDA
+ * Kernel Study: Pipelining", NCU Profiling Comparison: compute and memory
+ * throughput as a fraction of peak).  For the INT8 path (warp-level IMMA; the
+ * GB300's tcgen05 has no integer kind) and the FP32 FFMA path no measured
+ * peak is supplied with the machine, so this probe measures one: independent
+ * chains of the one instruction the kernel's inner loop is built from, on
+ * every SM, with no memory traffic.
+ */
+#ifndef GEMM_PROBE_H
+#define GEMM_PROBE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GP_PROBE_IMMA_S8 0  /* mma.sync.m16n8k32 s8 x s8 -> s32: 2*16*8*32 ops per warp instruction */
+#define GP_PROBE_FFMA_F32 1 /* fmaf on fp32: 2 FLOP per thread instruction */
+
+/*
+ * gemm_probe_peak -- run the probe for `kind` on the current device and
+ * stream (cudaStream_t as void*, NULL = default stream) and store the best
+ * measured rate in *ops_per_s (operations per second: INT8 ops or FP32 FLOP).
+ * Synchronous: returns after the probe kernels have finished (about 0.1 s).
+ * Returns 0, GP_ERR_ARG (-1) for a bad kind or NULL output, or GP_ERR_CUDA (-4).
+ * Allocates nothing.
+ */
+int gemm_probe_peak(int kind, double* ops_per_s, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_PROBE_H */

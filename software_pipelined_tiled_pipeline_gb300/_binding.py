@@ -36,7 +36,8 @@ LAYOUTS = {"row_col": GP_A_ROW_B_COL, "row_row": GP_A_ROW_B_ROW}
 VARIANTS = {"pingpong": GP_PINGPONG, "pipelined": GP_PIPELINED, "nopipe": GP_NOPIPE}
 
 # exported symbols, in header order
-SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_stats", "gemm_strerror", "gemm_abi_version"]
+SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_stats", "gemm_strerror", "gemm_abi_version",
+           "gemm_probe_peak"]
 
 
 class GpPlan(ctypes.Structure):
@@ -105,6 +106,8 @@ def lib():
     L.gemm_strerror.restype = ctypes.c_char_p
     L.gemm_abi_version.argtypes = []
     L.gemm_abi_version.restype = ci
+    L.gemm_probe_peak.argtypes = [ci, ctypes.POINTER(ctypes.c_double), vp]
+    L.gemm_probe_peak.restype = ci
     _lib = L
     return L
 
@@ -170,3 +173,16 @@ def gemm_stats(sync=True) -> dict:
     s = GpStats()
     lib().gemm_stats(ctypes.byref(s), 1 if sync else 0)
     return s.as_dict()
+
+
+PROBES = {"imma_s8": 0, "ffma_f32": 1}
+
+
+def probe_peak(kind, stream=0) -> float:
+    """Measured ops/s of one instruction path (see include/gemm_probe.h)."""
+    out = ctypes.c_double(0.0)
+    s = getattr(stream, "cuda_stream", stream)
+    rc = lib().gemm_probe_peak(_enum(kind, PROBES, "probe"), ctypes.byref(out), s or None)
+    if rc != GP_OK:
+        raise GemmError(rc, "gemm_probe_peak")
+    return out.value

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgemmpipe.so")
 
-SOURCES = ["api.cu", "k_ffma.cu", "k_imma.cu", "k_umma.cu"]
+SOURCES = ["api.cu", "k_ffma.cu", "k_imma.cu", "k_umma.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
@@ -33,7 +33,7 @@ def nvcc() -> str:
 
 def _deps():
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))]
-    deps.append(os.path.join(INCLUDE, "gemm_pipelined.h"))
+    deps += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     deps.append(os.path.abspath(__file__))
     return deps
 
