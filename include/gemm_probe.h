@@ -2,7 +2,7 @@
  * gemm_probe.h -- measured throughput ceilings for the roofline of the GEMM
  * library's kernels (part of libgemmpipe.so).
  *
- * The pages measure their kernels against the hardware's own limits ("CUDA
+ * Pipelined kernels are judged against the hardware's own limits ("CUDA
  * Kernel Study: Pipelining", NCU Profiling Comparison: compute and memory
  * throughput as a fraction of peak).  For the INT8 path (warp-level IMMA; the
  * GB300's tcgen05 has no integer kind) and the FP32 FFMA path no measured

@@ -6,8 +6,8 @@
  * CPU-baseline leg do.  It shares no code, header, table or constant with
  * the CUDA kernels: the only include beyond the C library is <stdint.h>.
  *
- * What it computes is the plain definition of a matrix product, the form the
- * pages print in "Part 4 -- Pipelining and Occupancy", section 4.3 "Register
+ * What it computes is the plain definition of a matrix product, the form
+ * printed in "Part 4 -- Pipelining and Occupancy", section 4.3 "Register
  * reuse": the triple loop over i, j, k whose inner sum is kept in a local
  * variable and stored once per output element.  The software pipeline that the
  * library implements ("CUDA Kernel Study: Pipelining", Case 1 and Case 2;

@@ -11,7 +11,7 @@ and ``mix`` the splitmix64 finaliser.  Draw i feeds the element at flat index
 i of the operand in its storage order (A: M x K row-major; B: N x K for the
 K-major "row_col" layout, K x N for "row_row").
 
-Distributions (the shapes of the pages' synthetic square GEMM workloads):
+Distributions (the value ranges of the synthetic square GEMM workloads):
 
 * ``int8``      -- top 8 bits of the draw, uniform on [-128, 127].
 * ``uniform``   -- u = (draw >> 40) * 2^-24, value 2u - 1 in [-1, 1), exact in

@@ -1,9 +1,9 @@
 """The synthetic GEMM workloads the library is measured and checked on.
 
-Shapes, layouts, element types and value distributions follow the pages'
-square synthetic GEMMs ("CUDA Kernel Study: Pipelining", Kernel Parameters;
-"pipeline-gpu-kernel", Step 2 -- the 4096^3 IGEMM; "Part 4 -- Pipelining and
-Occupancy", section 4.3 -- the 4096^3 FP32 sweep) widened to the stage/ratio
+Shapes, layouts, element types and value distributions follow the square
+synthetic GEMMs in "CUDA Kernel Study: Pipelining" (Kernel Parameters),
+"pipeline-gpu-kernel" (Step 2, the 4096^3 IGEMM) and "Part 4 -- Pipelining and
+Occupancy" (section 4.3, the 4096^3 FP32 sweep), widened to the stage/ratio
 sweep.  Operands come from ``synth`` with the base seed below.
 """
 from dataclasses import dataclass, field

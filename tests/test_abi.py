@@ -124,7 +124,7 @@ def test_default_stages_and_variant_stage_rules(gp):
     assert gp.gemm_plan(512, 512, 512, "f32", "row_row", 0, "pipelined")["stages"] == 3
 
 
-def test_compute_load_ratio_is_the_pages_formula(gp):
+def test_compute_load_ratio_is_the_published_formula(gp):
     for dtype, layout, esize in (("f16", "row_col", 2), ("i8", "row_col", 1), ("f32", "row_row", 4)):
         p = gp.gemm_plan(4096, 4096, 4096, dtype, layout, 2, "pipelined")
         bm, bn, bk = p["bm"], p["bn"], p["bk"]
@@ -134,7 +134,7 @@ def test_compute_load_ratio_is_the_pages_formula(gp):
     assert p["compute_load_ratio"] == pytest.approx(85.333, rel=1e-4)
 
 
-def test_ffma_tile_matches_pages_kernel_table(gp):
+def test_ffma_tile_matches_published_kernel_table(gp):
     g = json.load(open(os.path.join(GOLDEN, "p1_kernel_table.json")))
     t = g["tile"]
     M = g["problem"]["M"]
@@ -149,7 +149,7 @@ def test_ffma_tile_matches_pages_kernel_table(gp):
     assert round(ring2["ring_bytes"] / 1000, 2) == kb["cp_async_2stage"]
 
 
-def test_throughput_formula_matches_pages_benchmark():
+def test_throughput_formula_matches_published_benchmark():
     from software_pipelined_tiled_pipeline_gb300.workloads import Workload
     g = json.load(open(os.path.join(GOLDEN, "p1_kernel_table.json")))
     M = g["problem"]["M"]
@@ -161,7 +161,7 @@ def test_throughput_formula_matches_pages_benchmark():
         assert abs(gflops - row["gflops"]) <= slack + 0.05
 
 
-def test_double_buffer_rule_matches_pages_example():
+def test_double_buffer_rule_matches_published_example():
     g = json.load(open(os.path.join(GOLDEN, "p2_smem_budget.json")))
     # single buffer 2 KB + 2 KB -> doubled 8 KB
     assert 2 * g["single_buffer_kb"] == g["double_buffer_kb"]
