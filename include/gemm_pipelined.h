@@ -103,6 +103,12 @@ typedef struct gp_plan {
     int64_t k_tiles;             /* ceil(K/BK) */
     double compute_load_ratio;   /* 2*BM*BN*BK / ((BM*BK + BK*BN) * sizeof(input)), FLOP per byte */
     const char* kernel;          /* kernel family name, static string */
+    int32_t dp_tiles;            /* persistent kernels: tiles computed whole by one CTA (raster order first) */
+    int32_t sk_tiles;            /* tiles after those whose K-loops are split evenly over all CTAs (stream-K) */
+    int64_t workspace_bytes;     /* FP32 partial-tile workspace the split tiles use (per device and stream) */
+    int32_t cta_pair;            /* 1: two CTAs (a cluster on one TPC) share each BM x BN tile, each holding
+                                    BM/2 rows of A and BN/2 rows of B; stage_bytes and smem_bytes are per CTA */
+    int32_t reserved0;
 } gp_plan;
 
 /* Record of the last gemm_pipelined call made by the calling host thread. */
@@ -125,7 +131,9 @@ typedef struct gp_options {
     uint64_t timeout_ns;         /* limit of every bounded wait inside the kernel (0 = 1 s) */
     int32_t inject_lost_load;    /* test hook: the TMA producer skips the last tile load of the problem, so a
                                     consumer wait runs out and the call reports GP_ERR_TIMEOUT (no GPU fault) */
-    int32_t reserved[5];
+    int32_t no_stream_k;         /* 1: never split K-loops across CTAs (every tile computed whole) */
+    int32_t no_cta_pair;         /* 1: one CTA per output tile even where CTA pairs are available */
+    int32_t reserved[3];
 } gp_options;
 
 /*

@@ -48,6 +48,8 @@ class GpPlan(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32), ("persistent", ctypes.c_int32),
         ("grid", ctypes.c_int32), ("tiles", ctypes.c_int64), ("k_tiles", ctypes.c_int64),
         ("compute_load_ratio", ctypes.c_double), ("kernel", ctypes.c_char_p),
+        ("dp_tiles", ctypes.c_int32), ("sk_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("cta_pair", ctypes.c_int32), ("reserved0", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -72,7 +74,8 @@ class GpStats(ctypes.Structure):
 class GpOptions(ctypes.Structure):
     _fields_ = [
         ("bn", ctypes.c_int32), ("time_kernel", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
-        ("inject_lost_load", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5),
+        ("inject_lost_load", ctypes.c_int32), ("no_stream_k", ctypes.c_int32), ("no_cta_pair", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 
@@ -137,7 +140,8 @@ def abi_version() -> int:
 
 
 def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
-                   time_kernel=False, timeout_ns=0, inject_lost_load=False, check=True) -> int:
+                   time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
+                   check=True) -> int:
     """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
     stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0."""
     s = getattr(stream, "cuda_stream", stream)
@@ -146,6 +150,8 @@ def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined
     opts.time_kernel = 1 if time_kernel else 0
     opts.timeout_ns = int(timeout_ns)
     opts.inject_lost_load = 1 if inject_lost_load else 0
+    opts.no_stream_k = 1 if no_stream_k else 0
+    opts.no_cta_pair = 1 if no_cta_pair else 0
     rc = lib().gemm_pipelined_ex(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"),
                                  _enum(layout, LAYOUTS, "layout"), int(stages), _enum(variant, VARIANTS, "variant"),
                                  s or None, ctypes.byref(opts))

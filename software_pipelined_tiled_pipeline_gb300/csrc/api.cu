@@ -78,6 +78,65 @@ TmapEntry g_tmaps[kTmapCache];
 uint64_t g_tmap_clock = 0;
 
 // ---------------------------------------------------------------------------
+// stream-K workspace: per device and stream, grown on demand, never shrunk.
+// Calls on one stream are ordered, so one workspace per stream is race-free.
+// ---------------------------------------------------------------------------
+struct Workspace {
+  int dev = -1;
+  cudaStream_t stream = nullptr;
+  float* partials = nullptr;
+  size_t bytes = 0;
+  uint32_t* flags = nullptr;
+  size_t nflags = 0;
+  uint32_t epoch = 0;
+};
+constexpr int kMaxWorkspaces = 64;
+Workspace g_ws[kMaxWorkspaces];
+
+cudaError_t get_workspace(int dev, cudaStream_t stream, size_t bytes, size_t nflags, float** partials,
+                          uint32_t** flags, uint32_t* epoch) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace* w = nullptr;
+  for (auto& x : g_ws)
+    if (x.dev == dev && x.stream == stream) { w = &x; break; }
+  if (!w) {
+    for (auto& x : g_ws)
+      if (x.dev < 0) { w = &x; break; }
+    if (!w) return cudaErrorMemoryAllocation;   // more streams than slots
+    w->dev = dev;
+    w->stream = stream;
+  }
+  cudaError_t e;
+  if (w->bytes < bytes) {
+    if (w->partials) {
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+      cudaFree(w->partials);
+      w->partials = nullptr;
+      w->bytes = 0;
+    }
+    if ((e = cudaMalloc(&w->partials, bytes)) != cudaSuccess) return e;
+    w->bytes = bytes;
+  }
+  if (w->nflags < nflags) {
+    if (w->flags) {
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+      cudaFree(w->flags);
+      w->flags = nullptr;
+      w->nflags = 0;
+    }
+    if ((e = cudaMalloc(&w->flags, nflags * sizeof(uint32_t))) != cudaSuccess) return e;
+    if ((e = cudaMemset(w->flags, 0, nflags * sizeof(uint32_t))) != cudaSuccess) return e;
+    w->nflags = nflags;
+    w->epoch = 0;
+  }
+  if (++w->epoch == 0) w->epoch = 1;   // flags hold the epoch of the launch that set them
+  *partials = w->partials;
+  *flags = w->flags;
+  *epoch = w->epoch;
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
 // per-thread last-call record
 // ---------------------------------------------------------------------------
 struct LastCall {
@@ -114,9 +173,31 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int default_stages(int family) { return family == 0 ? 3 : 4; }
 
+// Persistent FP16/BF16 ring: when the output tiles do not fill whole waves of
+// `workers` (CTAs, or CTA pairs), keep all but the last full wave as whole
+// tiles and spread the K steps of the rest evenly over every worker
+// (stream-K).  Not worth it when each worker would get fewer than
+// kMinSkUnits K steps of the split tiles.
+void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allowed) {
+  constexpr int64_t kMinSkUnits = 4;
+  const int64_t T = p->tiles, G = workers;
+  p->dp_tiles = static_cast<int32_t>(T);
+  p->sk_tiles = 0;
+  p->workspace_bytes = 0;
+  p->grid = static_cast<int32_t>(ctas_per_worker * (T < G ? T : G));
+  if (!allowed || G <= 0 || p->k_tiles <= 0 || T % G == 0) return;
+  const int64_t dp = T > G ? (T / G - 1) * G : 0;
+  const int64_t skt = T - dp;
+  if (skt * p->k_tiles < kMinSkUnits * G) return;
+  p->dp_tiles = static_cast<int32_t>(dp);
+  p->sk_tiles = static_cast<int32_t>(skt);
+  p->grid = static_cast<int32_t>(ctas_per_worker * G);
+  p->workspace_bytes = static_cast<int64_t>(p->grid) * 128 * p->bn * 4;   // one 128 x BN FP32 slot per CTA
+}
+
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
-              int sm_count, gp_plan* p) {
+              int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
@@ -179,8 +260,12 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   };
   auto fits = [&](int bn) { return ring_smem_total(S * stage_bytes(bn), extra) <= kSmemPerCtaMax; };
 
+  const bool pair_ok = fam == 2 && ring && !no_pair && (bn_req == 0 || bn_req == 256) && N > 128 &&
+                       ring_smem_total(S * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax;
   int bn = 0;
-  if (bn_req) {
+  if (pair_ok) {
+    bn = 256;   // the pair kernel below replaces the single-CTA fields
+  } else if (bn_req) {
     bool known = false;
     for (int i = 0; i < ncand; ++i) known |= (cands[i] == bn_req);
     if (!known) return GP_ERR_UNSUPPORTED;
@@ -199,7 +284,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     if (!bn) return GP_ERR_SMEM;
   }
   p->bn = bn;
-  p->stage_bytes = stage_bytes(bn);
+  p->stage_bytes = pair_ok ? kUmmaPairStageBytes : stage_bytes(bn);
   p->ring_bytes = S * p->stage_bytes;
   p->smem_bytes = ring_smem_total(p->ring_bytes, extra);
   if (fam == 2) {
@@ -210,15 +295,40 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     }
   }
   p->persistent = (ring && fam != 0) ? 1 : 0;
+  // FP16/BF16 ring on CTA pairs: 256 x 256 tile per pair, 32 KB per CTA per K step
+  if (pair_ok) {
+    p->cta_pair = 1;
+    p->bm = 256;
+    p->bn = 256;
+    p->stage_bytes = kUmmaPairStageBytes;
+    p->ring_bytes = S * p->stage_bytes;
+    p->smem_bytes = ring_smem_total(p->ring_bytes, kUmmaEpiBytes);
+    if (p->smem_bytes < kSmemPerCtaMax / 2 + 1024) p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
+    p->tmem_cols = 512;
+    p->kernel = "umma_pair_ring";
+  }
   p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
   p->k_tiles = ceil_div(K, p->bk);
   if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
-  if (p->persistent)
+  if (p->cta_pair)
+    p->grid = sm_count > 1 ? static_cast<int32_t>(2 * (p->tiles < sm_count / 2 ? p->tiles : sm_count / 2)) : 0;
+  else if (p->persistent)
     p->grid = sm_count > 0 ? static_cast<int32_t>(p->tiles < sm_count ? p->tiles : sm_count) : 0;
   else
     p->grid = static_cast<int32_t>(p->tiles);
+  p->dp_tiles = static_cast<int32_t>(p->tiles);
+  p->sk_tiles = 0;
+  p->workspace_bytes = 0;
+  if (fam == 2 && ring && sm_count > 0) {
+    if (p->cta_pair)
+      apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
+    else
+      apply_stream_k(p, sm_count, 1, !no_stream_k);
+  }
   const double e = in_elem_bytes(dtype);
   p->compute_load_ratio = 2.0 * p->bm * p->bn * p->bk / ((static_cast<double>(p->bm) * p->bk + p->bk * p->bn) * e);
+  if (p->cta_pair)   // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B
+    p->compute_load_ratio = 2.0 * (p->bm / 2) * p->bn * p->bk / ((p->bm / 2 + p->bn / 2) * p->bk * e);
   return GP_OK;
 }
 
@@ -406,8 +516,23 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   if (K == 0) {
     e = launch_zero_fill(C, M * N * out_elem_bytes(dtype), st);
   } else {
-    rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan);
+    const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
+    rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair);
     if (rc != GP_OK) { record(rc, 0); return rc; }
+    if (plan.cta_pair) {
+      // pairs must sit on one TPC each: the resident count may be below SMs / 2
+      int pairs = 0;
+      e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
+      if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (pairs < sms / 2) apply_stream_k(&plan, pairs, 2, !(opts && opts->no_stream_k));
+    }
+    SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, 0};
+    if (plan.sk_tiles > 0) {
+      e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), static_cast<size_t>(plan.grid),
+                        &sk.workspace, &sk.flags, &sk.epoch);
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+    }
     LaunchArgs a;
     a.A = A;
     a.B = B;
@@ -424,6 +549,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.ctl.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     a.ctl.inject_lost_load = opts ? opts->inject_lost_load : 0;
     a.sm_count = sms;
+    a.sk = sk;
     const void* kernel = nullptr;
     switch (family_of(dtype)) {
       case 0: e = launch_ffma(a, &kernel); break;

@@ -23,12 +23,28 @@ enum WaitSite : uint32_t {
   kSiteEpilogueAccFull = 4,
   kSitePingPongMma = 5,
   kSiteDrain = 6,
+  kSitePartialFlag = 7,
 };
 
 struct KernelCtl {
   uint32_t* status;         // device word, 0 = clean
   uint64_t timeout_ns;      // limit of every bounded wait
   int32_t inject_lost_load; // test hook: producer skips the final tile load
+};
+
+// Stream-K split of a persistent launch: the first dp_tiles output tiles (in
+// raster order) are computed whole, CTA b taking tiles b, b+G, ...; the K-loops
+// of the next sk_tiles tiles form sk_tiles*k_tiles units of one K step each,
+// dealt out as G contiguous, equal ranges.  A CTA whose range starts inside a
+// tile writes that partial accumulator to workspace slot b and raises flags[b]
+// to `epoch`; the CTA owning the tile's first K step adds those partials and
+// writes C.
+struct SkParams {
+  int32_t dp_tiles;
+  int32_t sk_tiles;
+  float* workspace;         // G partial tiles, BM x BN FP32 each, row-major
+  uint32_t* flags;          // G words
+  uint32_t epoch;           // flag value of this launch
 };
 
 // ---------------------------------------------------------------------------
@@ -54,6 +70,8 @@ constexpr int kUmmaEpiRows = 32;         // rows per epilogue warp (one TMEM lan
 constexpr int kUmmaEpiCols = 64;         // 16-bit columns per staged chunk (128 bytes)
 constexpr int kUmmaEpiBufBytes = kUmmaEpiRows * kUmmaEpiCols * 2;
 constexpr int kUmmaEpiBytes = kUmmaEpiWarps * 2 * kUmmaEpiBufBytes;   // double-buffered per warp
+// CTA-pair kernel: 256 x 256 output tile per pair, 128 rows of A and of B per CTA.
+constexpr int kUmmaPairStageBytes = 2 * 128 * kUmmaBK * 2;             // per CTA per K step
 __host__ __device__ constexpr int umma_stage_bytes(int bn) { return (kUmmaBM + bn) * kUmmaBK * 2; }
 
 __host__ __device__ constexpr int ring_smem_total(int ring_bytes, int extra) {
@@ -72,6 +90,7 @@ struct LaunchArgs {
   gp_plan plan;
   cudaStream_t stream;
   KernelCtl ctl;
+  SkParams sk;
   int32_t sm_count;
 };
 
@@ -80,6 +99,8 @@ struct LaunchArgs {
 cudaError_t launch_ffma(LaunchArgs& a, const void** kernel);
 cudaError_t launch_imma(LaunchArgs& a, const void** kernel);
 cudaError_t launch_umma(LaunchArgs& a, const void** kernel);
+// CTA pairs of the FP16/BF16 pair kernel that fit on the device at once.
+cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs);
 cudaError_t launch_zero_fill(void* C, int64_t bytes, cudaStream_t stream);
 
 // Tensor-map encoding (driver entry point obtained once through the runtime).

@@ -9,19 +9,21 @@
 //      warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> FP16/BF16 ->
 //              swizzled shared staging -> TMA store.
 //    The accumulator is double-buffered in TMEM so the epilogue of one tile
-//    overlaps the K-loop of the next.  This is the S-stage ring of
+//    overlaps the K-loop of the next.  When the output tiles do not divide
+//    evenly over the CTAs, the K-loops of the last ones are split evenly
+//    across all CTAs (stream-K) with FP32 partials in a workspace.  This is the S-stage ring of
 //    "CUDA Kernel Study: Pipelining", Case 2 (prologue fills S slots, the
 //    steady state refills the slot just consumed, the tail drains), with TMA
 //    completion bytes on an mbarrier in place of cp.async commit/wait groups.
 //
-//  * umma_pingpong_kernel -- the register-staged double buffer of Case 1 /
+//  * umma_staged_kernel<PINGPONG=true> -- the register-staged double buffer of Case 1 /
 //    "pipeline-gpu-kernel" Step 3 (LDG-register variant): global loads of tile
 //    k+1 into registers are in flight while the tensor core consumes tile k
 //    from one shared buffer; the registers are then stored to the other
 //    buffer.  The "compute finished reading" barrier before that store is the
 //    tcgen05.commit of the previous tile's MMAs.
 //
-//  * umma_nopipe_kernel -- load, synchronise, compute, wait (Background).
+//  * umma_staged_kernel<PINGPONG=false> -- load, synchronise, compute, wait (Background).
 //
 // All three use the same tile shape, shared-memory layout (K-major tiles of
 // 128-byte rows with the 128-byte swizzle), MMA sequence and epilogue, so
@@ -123,13 +125,105 @@ __device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint32_t a_addr, ui
 // ---------------------------------------------------------------------------
 // main path: persistent warp-specialised TMA ring
 // ---------------------------------------------------------------------------
-template <int BN, bool BF16>
+
+// The ordered list of work items of one worker (a CTA, or a CTA pair), walked
+// identically by the producer, the MMA issuer and the epilogue: whole tiles
+// first (w, w+W, ... below dp_tiles), then this worker's contiguous range of
+// the stream-K units (one unit = one K step of one of the sk_tiles tiles after
+// them), cut at tile boundaries.  An item is (tile, first K step, one past the
+// last K step).
+struct WorkIter {
+  int dp_tiles, kt, next_dp, step;
+  int64_t u, u_end;
+
+  __device__ __forceinline__ static int64_t range_start(int w, int64_t units, int workers) {
+    return static_cast<int64_t>(w) * units / workers;
+  }
+  __device__ __forceinline__ void init(const SkParams& sk, int kt_, int worker, int workers) {
+    dp_tiles = sk.dp_tiles;
+    kt = kt_;
+    next_dp = worker;
+    step = workers;
+    const int64_t units = static_cast<int64_t>(sk.sk_tiles) * kt;
+    u = range_start(worker, units, workers);
+    u_end = range_start(worker + 1, units, workers);
+  }
+  __device__ __forceinline__ bool next(int& tile, int& k0, int& k1) {
+    if (next_dp < dp_tiles) {
+      tile = next_dp;
+      k0 = 0;
+      k1 = kt;
+      next_dp += step;
+      return true;
+    }
+    if (u >= u_end) return false;
+    const int t = static_cast<int>(u / kt);
+    k0 = static_cast<int>(u - static_cast<int64_t>(t) * kt);
+    const int64_t left = u_end - u;
+    k1 = (left < kt - k0) ? k0 + static_cast<int>(left) : kt;
+    tile = dp_tiles + t;
+    u += k1 - k0;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void epi_bar_sync() {   // the 4 epilogue warps only
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Barrier of the 4 epilogue warps that also ANDs a predicate over their 128 threads.
+__device__ __forceinline__ bool epi_bar_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Shapes of the ring kernel.  PAIR = false: one CTA per 128 x BN tile.
+// PAIR = true (BN = 256): a cluster of two CTAs per 256 x 256 tile; each CTA
+// loads its own 128-row halves of the A and B tiles (32 KB per K step instead
+// of the 48 KB one CTA needs for 128 x 256), one thread of the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256), which reads both CTAs' halves and writes
+// each CTA's 128 accumulator rows into that CTA's TMEM.  The even CTA's
+// full[s] barrier counts the bytes of both CTAs' loads (the odd CTA's TMA
+// signals it through the cluster window); the MMA commit releases slot s in
+// both CTAs at once, so the two producers run in lockstep; epilogue warps of
+// both CTAs hand an accumulator back by arriving on the even CTA's acc_empty.
+template <int BN, bool PAIR>
+struct RingShape {
+  static constexpr int A_ROWS = 128;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
+  static constexpr int A_BYTES = A_ROWS * BK * 2;
+  static constexpr int STAGE = (A_ROWS + B_ROWS) * BK * 2;
+  static constexpr int TILE_M = PAIR ? 2 * A_ROWS : A_ROWS;
+  static constexpr int CTAS = PAIR ? 2 : 1;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;   // double-buffered 128 x BN FP32 accumulator per CTA
+};
+
+template <int BN, bool BF16, bool PAIR>
 __global__ void __launch_bounds__(192, 1)
     umma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl) {
-  constexpr int STAGE = A_BYTES + BN * BK * 2;
-  constexpr uint32_t TMEM_COLS = 2 * BN;
-  constexpr uint32_t IDESC = umma_idesc_f16(BF16, BM, BN);
+                     const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl,
+                     SkParams sk) {
+  using Sh = RingShape<BN, PAIR>;
+  constexpr int STAGE = Sh::STAGE;
+  constexpr uint32_t IDESC = umma_idesc_f16(BF16, Sh::TILE_M, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -139,7 +233,11 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_blocks = (M + BM - 1) / BM;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int m_blocks = (M + Sh::TILE_M - 1) / Sh::TILE_M;
   const int n_blocks = (N + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int kt = (K + BK - 1) / BK;
@@ -151,7 +249,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->acc_full[a], 1);
-      mbar_init(&bar->acc_empty[a], kUmmaEpiWarps);
+      mbar_init(&bar->acc_empty[a], Sh::CTAS * kUmmaEpiWarps);
     }
     mbar_init(&bar->drain, 1);
     bar->ctl.abort = 0;
@@ -164,32 +262,50 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(&bar->tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&bar->tmem_base, Sh::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bar->tmem_base, Sh::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();   // both CTAs' barriers initialised and TMEM allocated before any cross-CTA signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   CtaCtl* cta = &bar->ctl;
   int issued = 0;  // producer only
+  WorkIter it;
+  it.init(sk, kt, worker, workers);
+  int tile, k0, k1;
 
   if (warp == 0) {
-    // ---------------- producer ----------------
+    // ---------------- producer (every CTA) ----------------
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      for (int tile = blockIdx.x; tile < tiles && !cta->abort; tile += gridDim.x) {
+      while (!cta->abort && it.next(tile, k0, k1)) {
         int mb, nb;
         tile_coords(tile, m_blocks, n_blocks, mb, nb);
-        for (int kb = 0; kb < kt; ++kb) {
+        const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
+        const int n_row = nb * BN + rank * Sh::B_ROWS;
+        for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto producer_done;
-          const bool drop = ctl.inject_lost_load && tile == tiles - 1 && kb == kt - 1;
-          if (!drop) {
-            uint8_t* slot = ring + s * STAGE;
+          uint8_t* slot = ring + s * STAGE;
+          if (PAIR) {
+            if (leader) mbar_arrive_expect_tx(&bar->full[s], 2 * STAGE);
+            const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), 0);
+            tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
+            tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
+            ++issued;
+          } else if (!(ctl.inject_lost_load && tile == tiles - 1 && kb == kt - 1)) {
             mbar_arrive_expect_tx(&bar->full[s], STAGE);
-            tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, mb * BM);
-            tma_load_2d(smem_u32(slot + A_BYTES), &tmB, &bar->full[s], kb * BK, nb * BN);
+            tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, m_row);
+            tma_load_2d(smem_u32(slot + Sh::A_BYTES), &tmB, &bar->full[s], kb * BK, n_row);
             ++issued;
           }
           if (++s == stages) { s = 0; ph ^= 1u; }
@@ -198,64 +314,126 @@ __global__ void __launch_bounds__(192, 1)
     producer_done:;
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuer (one thread; the even CTA of a pair) ----------------
+    if (lane == 0 && leader) {
       int s = 0;
       uint32_t ph = 0;
       int consumed = 0;
-      int t = 0;
-      for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
+      for (int t = 0; it.next(tile, k0, k1); ++t) {
         const int a = t & 1;
         if (!mbar_wait(&bar->acc_empty[a], ((t >> 1) & 1) ^ 1u, ctl, cta, kSiteMmaAccEmpty)) break;
         tc_fence_after();
         const uint32_t d = tmem + a * BN;
         bool ok = true;
-        for (int kb = 0; kb < kt; ++kb) {
+        for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(ring + s * STAGE);
-          umma_kblock<BN>(d, a_addr, a_addr + A_BYTES, IDESC, kb == 0);
-          umma_commit(&bar->empty[s]);   // slot s is free once these MMAs have read it
+          const uint64_t da = umma_desc_sw128(a_addr);
+          const uint64_t db = umma_desc_sw128(a_addr + Sh::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // advancing the start address by 32 bytes (>> 4 = 2) steps 16 elements along K
+            const uint32_t acc = (kb == k0 && kk == 0) ? 0u : 1u;
+            if (PAIR)
+              umma_f16_pair(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
+            else
+              umma_f16(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
+          }
+          // slot s is free (in every CTA that loaded into it) once these MMAs have read it
+          if (PAIR) umma_commit_pair(&bar->empty[s], 0x3); else umma_commit(&bar->empty[s]);
           ++consumed;
           if (++s == stages) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(&bar->acc_full[a]);  // accumulator a complete
+        if (PAIR) umma_commit_pair(&bar->acc_full[a], 0x3); else umma_commit(&bar->acc_full[a]);
       }
       bar->consumed_hi = consumed;
       // every MMA issued by this thread has completed once drain fires
-      umma_commit(&bar->drain);
-      KernelCtl c2 = ctl;
+      if (PAIR) umma_commit_pair(&bar->drain, 0x1); else umma_commit(&bar->drain);
       CtaCtl never_abort{0};
-      mbar_wait(&bar->drain, 0, c2, &never_abort, kSiteDrain);
+      mbar_wait(&bar->drain, 0, ctl, &never_abort, kSiteDrain);
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..5 of every CTA) ----------------
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int e = warp - 2;
+    const int row = q * 32 + lane;      // accumulator row of this CTA that this thread holds
     uint8_t* my_stage = epi + e * 2 * kUmmaEpiBufBytes;
+    const int64_t units = static_cast<int64_t>(sk.sk_tiles) * kt;
     int sb = 0;
-    int t = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++t) {
+    for (int t = 0; it.next(tile, k0, k1); ++t) {
       int mb, nb;
       tile_coords(tile, m_blocks, n_blocks, mb, nb);
       const int a = t & 1;
+      // stream-K: partial writer (this worker's range starts inside the tile)
+      // or owner of the first K step of a split tile (adds the partials after it)
+      const bool writer = k0 > 0;
+      int w_first = 0, w_last = -1;
+      if (!writer && k1 < kt) {
+        const int64_t tile_end = static_cast<int64_t>(tile - sk.dp_tiles + 1) * kt;
+        w_first = worker + 1;
+        w_last = worker;
+        while (w_last + 1 < workers && WorkIter::range_start(w_last + 1, units, workers) < tile_end) ++w_last;
+        if (e == 0 && lane == 0) {
+          for (int w = w_first; w <= w_last && !cta->abort; ++w) {
+            const uint32_t* flag = sk.flags + w * Sh::CTAS + rank;
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_u32(flag) != sk.epoch) {
+              __nanosleep(64);
+              if (cta->abort) break;
+              if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                report_error(ctl.status, kDevErrTimeout, kSitePartialFlag);
+                cta->abort = 1;
+                break;
+              }
+            }
+          }
+        }
+      }
       uint32_t ok = 1;
       if (lane == 0) ok = mbar_wait(&bar->acc_full[a], (t >> 1) & 1, ctl, cta, kSiteEpilogueAccFull) ? 1u : 0u;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      // one decision for all four epilogue warps (they meet at named barriers below)
+      if (!epi_bar_and(ok != 0 && !cta->abort)) break;
       tc_fence_after();
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
-      const int y = mb * BM + q * 32;
+      const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
 #pragma unroll 1
       for (int c = 0; c < BN / kUmmaEpiCols; ++c) {
         uint32_t v[64];
         load_acc_chunk(trow + c * kUmmaEpiCols, v);
         if (c == BN / kUmmaEpiCols - 1) {
-          // all of accumulator a is in registers: hand it back to the MMA warp
+          // all of accumulator a is in registers: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bar->acc_empty[a]);
+          if (lane == 0) {
+            if (PAIR)
+              mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), 0));
+            else
+              mbar_arrive(&bar->acc_empty[a]);
+          }
+        }
+        if (writer) {
+          float4* dst = reinterpret_cast<float4*>(
+              sk.workspace + (static_cast<size_t>(blockIdx.x) * Sh::A_ROWS + row) * BN + c * kUmmaEpiCols);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            __stcg(dst + i, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                        __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+          continue;
+        }
+        for (int w = w_first; w <= w_last; ++w) {
+          const float4* src = reinterpret_cast<const float4*>(
+              sk.workspace + (static_cast<size_t>(w * Sh::CTAS + rank) * Sh::A_ROWS + row) * BN + c * kUmmaEpiCols);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 p = __ldcg(src + i);
+            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + p.x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + p.y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + p.z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + p.w);
+          }
         }
         if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
@@ -263,24 +441,39 @@ __global__ void __launch_bounds__(192, 1)
         stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
         sb ^= 1;
       }
+      if (writer) {
+        // publish the partial: every epilogue thread's stores, then the flag
+        __threadfence();
+        epi_bar_sync();
+        if (e == 0 && lane == 0) st_release_u32(sk.flags + blockIdx.x, sk.epoch);
+      }
     }
     if (lane == 0) bulk_wait<0>();
   }
 
   __syncthreads();
   if (cta->abort && warp == 0 && lane == 0) {
-    // loads still in flight land in shared memory: wait for them before exit
     CtaCtl never_abort{0};
-    const int done = bar->consumed_hi;
-    for (int i = done; i < issued; ++i) {
-      const int s = i % stages;
-      mbar_wait(&bar->full[s], static_cast<uint32_t>((i / stages) & 1), ctl, &never_abort, kSiteDrain);
+    if (PAIR) {
+      // this CTA's loads count on the even CTA's barrier: give any still in
+      // flight time to land before the pair tears down
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+    } else {
+      // loads still in flight land in shared memory: wait for them before exit
+      for (int i = bar->consumed_hi; i < issued; ++i)
+        mbar_wait(&bar->full[i % stages], static_cast<uint32_t>((i / stages) & 1), ctl, &never_abort, kSiteDrain);
     }
   }
-  __syncthreads();
+  if (PAIR) {
+    tc_fence_before();
+    cluster_sync();   // the even CTA's MMAs, which touch both CTAs, have completed
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem, Sh::TMEM_COLS); else tmem_dealloc(tmem, Sh::TMEM_COLS);
   }
 }
 
@@ -469,35 +662,88 @@ __global__ void __launch_bounds__(kPPThreads, 1)
   }
 }
 
+template <int BN, bool BF16, bool PAIR>
+cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
+  using Sh = RingShape<BN, PAIR>;
+  const gp_plan& p = a.plan;
+  const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t M = a.M, N = a.N, K = a.K;
+  CUtensorMap tmA, tmB, tmC;
+  cudaError_t e;
+  if ((e = make_tmap_2d(&tmC, a.C, dt, N, M, N * 2, kUmmaEpiCols, kUmmaEpiRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      cudaSuccess)
+    return e;
+  if ((e = make_tmap_2d(&tmA, a.A, dt, K, M, K * 2, BK, Sh::A_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_2d(&tmB, a.B, dt, K, N, K * 2, BK, Sh::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  auto k = umma_ring_kernel<BN, BF16, PAIR>;
+  *kernel = reinterpret_cast<const void*>(k);
+  if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (PAIR) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (p.sk_tiles > 0) {
+    attr[n].id = cudaLaunchAttributeCooperative;   // stream-K workers wait on each other: all must be resident
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl, a.sk);
+}
+
 template <int BN, bool BF16>
 cudaError_t launch_bn(LaunchArgs& a, const void** kernel) {
   const gp_plan& p = a.plan;
   const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const uint64_t M = a.M, N = a.N, K = a.K;
+  if (a.variant == GP_PIPELINED) return launch_ring<BN, BF16, false>(a, kernel);
+  const uint64_t M = a.M, N = a.N;
   CUtensorMap tmC;
-  cudaError_t e = make_tmap_2d(&tmC, a.C, dt, N, M, N * 2, kUmmaEpiCols, kUmmaEpiRows,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+  cudaError_t e = make_tmap_2d(&tmC, a.C, dt, N, M, N * 2, kUmmaEpiCols, kUmmaEpiRows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  if (a.variant == GP_PIPELINED) {
-    CUtensorMap tmA, tmB;
-    if ((e = make_tmap_2d(&tmA, a.A, dt, K, M, K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
-    if ((e = make_tmap_2d(&tmB, a.B, dt, K, N, K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
-    auto k = umma_ring_kernel<BN, BF16>;
-    *kernel = reinterpret_cast<const void*>(k);
-    if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
-    k<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl);
-  } else {
-    auto k = (a.variant == GP_PINGPONG) ? umma_staged_kernel<BN, BF16, true> : umma_staged_kernel<BN, BF16, false>;
-    *kernel = reinterpret_cast<const void*>(k);
-    if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
-    k<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(static_cast<const uint8_t*>(a.A),
-                                                      static_cast<const uint8_t*>(a.B), tmC, a.M, a.N, a.K, a.ctl);
-  }
+  auto k = (a.variant == GP_PINGPONG) ? umma_staged_kernel<BN, BF16, true> : umma_staged_kernel<BN, BF16, false>;
+  *kernel = reinterpret_cast<const void*>(k);
+  if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
+  k<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(static_cast<const uint8_t*>(a.A), static_cast<const uint8_t*>(a.B),
+                                                    tmC, a.M, a.N, a.K, a.ctl);
   return cudaGetLastError();
+}
+
+// Largest number of CTA pairs of the pair kernel that can be resident at once.
+cudaError_t max_pairs(bool bf16, int smem_bytes, int* pairs) {
+  const void* k = bf16 ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true>)
+                       : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true>);
+  cudaError_t e = ensure_smem_attr(k, smem_bytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(pairs, k, &cfg);
 }
 
 template <bool BF16>
 cudaError_t launch_dtype(LaunchArgs& a, const void** kernel) {
+  if (a.plan.cta_pair) return launch_ring<256, BF16, true>(a, kernel);
   switch (a.plan.bn) {
     case 256: return launch_bn<256, BF16>(a, kernel);
     case 128: return launch_bn<128, BF16>(a, kernel);
@@ -510,6 +756,10 @@ cudaError_t launch_dtype(LaunchArgs& a, const void** kernel) {
 
 cudaError_t launch_umma(LaunchArgs& a, const void** kernel) {
   return a.dtype == GP_BF16_F32ACC_BF16OUT ? launch_dtype<true>(a, kernel) : launch_dtype<false>(a, kernel);
+}
+
+cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs) {
+  return max_pairs(dtype == GP_BF16_F32ACC_BF16OUT, smem_bytes, pairs);
 }
 
 }  // namespace gp

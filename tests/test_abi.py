@@ -52,8 +52,8 @@ def test_version_and_strerror(gp):
 
 def test_struct_sizes_match_c_layout():
     from software_pipelined_tiled_pipeline_gb300 import _binding as b
-    assert ctypes.sizeof(b.GpPlan) == 88
-    assert ctypes.sizeof(b.GpStats) == 120
+    assert ctypes.sizeof(b.GpPlan) == 112
+    assert ctypes.sizeof(b.GpStats) == 144
     assert ctypes.sizeof(b.GpOptions) == 40
 
 
@@ -93,15 +93,38 @@ def test_call_argument_errors_need_no_device(gp):
     assert st["status"] == 0
 
 
-@pytest.mark.parametrize("S,bn", [(1, 256), (2, 256), (3, 256), (4, 256), (5, 128), (6, 128), (7, 64), (8, 64)])
-def test_umma_tile_shrinks_with_stages(gp, S, bn):
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 5, 6])
+def test_umma_pairs_up_to_six_stages(gp, S):
+    # CTA pair: 256 x 256 tile per pair, each CTA 128 rows of A and 128 of B = 32 KB per K step
     p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined")
-    assert p["bm"] == 128 and p["bk"] == 64 and p["bn"] == bn and p["stages"] == S
-    assert p["stage_bytes"] == (128 + bn) * 64 * 2
-    assert p["ring_bytes"] == S * p["stage_bytes"]
-    assert p["smem_bytes"] <= 232448
-    assert p["tmem_cols"] == 2 * bn and p["persistent"] == 1
-    assert p["tiles"] == (4096 // 128) * (4096 // bn) and p["k_tiles"] == 64
+    assert p["cta_pair"] == 1 and p["kernel"] == "umma_pair_ring"
+    assert (p["bm"], p["bn"], p["bk"], p["stages"]) == (256, 256, 64, S)
+    assert p["stage_bytes"] == 2 * 128 * 64 * 2 and p["ring_bytes"] == S * p["stage_bytes"]
+    assert 232448 // 2 < p["smem_bytes"] <= 232448
+    assert p["tmem_cols"] == 512 and p["persistent"] == 1
+    assert p["tiles"] == 16 * 16 and p["k_tiles"] == 64
+    # per CTA: 2*128*256*64 / ((128 + 128) * 64 * 2) FLOP per byte loaded
+    assert p["compute_load_ratio"] == pytest.approx(128.0)
+
+
+@pytest.mark.parametrize("S", range(1, 9))
+def test_umma_single_cta_widths_follow_the_budget(gp, S):
+    # one CTA per 128 x BN tile: the widths the 227 KB budget admits at this depth
+    for b in (256, 128, 64):
+        fits = 1024 + S * (128 + b) * 64 * 2 + 32768 + 256 <= 232448
+        rc = gp.gemm_plan_rc(4096, 4096, 4096, "f16", "row_col", S, "pipelined", bn=b)
+        if b == 256 and S <= 6:
+            assert rc == 0 and gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined", bn=b)["cta_pair"] == 1
+            continue
+        assert rc == (0 if fits else -3), (S, b, rc)
+        if fits:
+            q = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined", bn=b)
+            assert q["cta_pair"] == 0 and q["bm"] == 128 and q["bn"] == b
+            assert q["stage_bytes"] == (128 + b) * 64 * 2 and q["tmem_cols"] == 2 * b
+            assert q["tiles"] == 32 * (4096 // b)
+    if S > 6:
+        p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined")
+        assert p["cta_pair"] == 0 and p["bn"] == 64
 
 
 @pytest.mark.parametrize("S,bn", [(1, 128), (4, 128), (6, 128), (7, 128), (8, 64)])
@@ -125,13 +148,15 @@ def test_default_stages_and_variant_stage_rules(gp):
 
 
 def test_compute_load_ratio_is_the_published_formula(gp):
-    for dtype, layout, esize in (("f16", "row_col", 2), ("i8", "row_col", 1), ("f32", "row_row", 4)):
-        p = gp.gemm_plan(4096, 4096, 4096, dtype, layout, 2, "pipelined")
+    for dtype, layout, esize, bn in (("f16", "row_col", 2, 128), ("i8", "row_col", 1, 0), ("f32", "row_row", 4, 0)):
+        p = gp.gemm_plan(4096, 4096, 4096, dtype, layout, 2, "pipelined", bn=bn)
         bm, bn, bk = p["bm"], p["bn"], p["bk"]
         assert p["compute_load_ratio"] == pytest.approx(2 * bm * bn * bk / ((bm * bk + bk * bn) * esize))
-    # FP16 128x256x64: 2*128*256*64 / ((128*64 + 64*256) * 2) = 85.33 FLOP/byte, far above the 20:1 line
-    p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 4, "pipelined")
-    assert p["compute_load_ratio"] == pytest.approx(85.333, rel=1e-4)
+    # FP16 128x256x64 on one CTA: 2*128*256*64 / ((128*64 + 64*256) * 2) = 85.33 FLOP/byte
+    p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 7, "pipelined", bn=64)
+    assert p["compute_load_ratio"] == pytest.approx(2 * 128 * 64 * 64 / ((128 * 64 + 64 * 64) * 2))
+    p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 4, "pipelined", bn=128)
+    assert p["compute_load_ratio"] == pytest.approx(64.0)
 
 
 def test_ffma_tile_matches_published_kernel_table(gp):

@@ -44,15 +44,33 @@ def test_i8_4096_bit_exact_every_stage_and_variant():
 def test_f16_4096_sampled_and_stage_invariant():
     w = WORKLOADS["f16_4096"]
     A, B = operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
-    ref, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4)
     rows = list(range(0, 4096, 67)) + [4095]
-    check_sampled(w.dtype, w.layout, A, B, ref, w.K, rows=rows, npts=4000, seed=1)
+    # the benchmark's launch: TMA ring on CTA pairs, 4 stages
+    C, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4)
+    assert st["plan"]["cta_pair"] == 1
+    check_sampled(w.dtype, w.layout, A, B, C, w.K, rows=rows, npts=4000, seed=1)
+    for S in (2, 3, 6):
+        C2, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
+        assert torch.equal(_bits(C2), _bits(C))
+    # one CTA per tile, whole tiles: every variant and depth runs the same MMA sequence
+    ref, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4, no_stream_k=True,
+                  no_cta_pair=True)
+    assert st["plan"]["sk_tiles"] == 0 and st["plan"]["cta_pair"] == 0
+    check_sampled(w.dtype, w.layout, A, B, ref, w.K, rows=rows, npts=4000, seed=2)
     for S in w.stages:
-        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
-        assert torch.equal(_bits(C), _bits(ref))
+        C2, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S, no_stream_k=True,
+                    no_cta_pair=True)
+        assert torch.equal(_bits(C2), _bits(ref))
     for variant in ("pingpong", "nopipe"):
-        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant=variant)
-        assert torch.equal(_bits(C), _bits(ref))
+        C2, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant=variant)
+        assert torch.equal(_bits(C2), _bits(ref))
+    # stream-K split of the last wave: differs only by the order of FP32 partial sums
+    C3, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4, no_cta_pair=True)
+    assert st["plan"]["sk_tiles"] > 0
+    check_sampled(w.dtype, w.layout, A, B, C3, w.K, rows=rows, npts=4000, seed=3)
+    for other in (C, C3):
+        diff = (other.float() - ref.float()).abs().max().item()
+        assert diff <= 2.0 ** -6 * ref.float().abs().max().item()
 
 
 @pytest.mark.parametrize("name", ["bf16_8192_k256", "bf16_8192_k1024", "bf16_8192_k4096", "bf16_8192_k16384",
@@ -60,11 +78,16 @@ def test_f16_4096_sampled_and_stage_invariant():
 def test_bf16_sweep_configs(name):
     w = WORKLOADS[name]
     A, B = operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    rows = [0, 1, 127, 128, 4095, 8191] if w.K > 4096 else list(range(0, w.M, 257)) + [w.M - 1]
     ref = None
     for S in w.stages:
+        # default launch (stream-K where the tiles do not fill whole waves): sampled oracle check
         C, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
+        check_sampled(w.dtype, w.layout, A, B, C, w.K, npts=1000, seed=S)
+        # one CTA per tile, whole tiles: bit-identical across depths
+        C2, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S, no_stream_k=True,
+                    no_cta_pair=True)
         if ref is None:
-            rows = [0, 1, 127, 128, 4095, 8191] if w.K > 4096 else list(range(0, w.M, 257)) + [w.M - 1]
-            check_sampled(w.dtype, w.layout, A, B, C, w.K, rows=rows, npts=2000, seed=S)
-            ref = C
-        assert torch.equal(_bits(C), _bits(ref)), "stage %d differs" % S
+            check_sampled(w.dtype, w.layout, A, B, C2, w.K, rows=rows, npts=2000, seed=S)
+            ref = C2
+        assert torch.equal(_bits(C2), _bits(ref)), "stage %d differs" % S

@@ -178,3 +178,67 @@ def test_lost_load_reports_timeout_and_context_survives(dtype):
     C, st2 = run(dtype, lay, A, B, M, N, K)
     assert st2["device_status"] == 0
     check_full(dtype, lay, A, B, C, K)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K,S", [(1024, 1024, 4096, 4), (1536, 1280, 1024, 3), (1000, 776, 2056, 4),
+                                     (2560, 4096, 512, 2), (520, 392, 8192, 6)])
+def test_stream_k_split_tiles(dtype, M, N, K, S):
+    # tiles whose K-loops are split across CTAs, partials added by the first-K-step owner
+    lay = "row_col"
+    A, B = operands(dtype, lay, M, N, K, seed=M + N + K)
+    C, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, no_cta_pair=True)
+    p = st["plan"]
+    assert p["sk_tiles"] > 0 and p["grid"] == st["sm_count"]
+    assert p["dp_tiles"] + p["sk_tiles"] == p["tiles"]
+    check_full(dtype, lay, A, B, C, K)
+    C2, st2 = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, no_stream_k=True, no_cta_pair=True)
+    assert st2["plan"]["sk_tiles"] == 0
+    diff = (C.float() - C2.float()).abs().max().item()
+    assert diff <= 2.0 ** -6 * C2.float().abs().max().item()
+
+
+def test_stream_k_repeated_launches_reuse_workspace():
+    # flags carry a per-launch epoch: back-to-back launches on one stream stay correct
+    A, B = operands("f16", "row_col", 1024, 1024, 4096, seed=9)
+    outs = [run("f16", "row_col", A, B, 1024, 1024, 4096, stages=4, no_cta_pair=True)[0] for _ in range(3)]
+    check_full("f16", "row_col", A, B, outs[0], 4096)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_stream_k_lost_load_reports_timeout():
+    M, N, K = 1024, 1024, 4096
+    A, B = operands("f16", "row_col", M, N, K, seed=4)
+    tA, tB = to_dev(A, "f16"), to_dev(B, "f16")
+    tC = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    gp.gemm_pipelined(tA, tB, tC, M, N, K, "f16", "row_col", 4, "pipelined", torch.cuda.current_stream(),
+                      timeout_ns=20_000_000, inject_lost_load=True)
+    st = gp.gemm_stats(sync=True)
+    assert st["plan"]["sk_tiles"] > 0
+    assert st["status"] == gp.GP_ERR_TIMEOUT
+    C, st2 = run("f16", "row_col", A, B, M, N, K)
+    check_full("f16", "row_col", A, B, C, K)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K,S", [(256, 256, 64, 1), (200, 264, 136, 2), (384, 520, 1000, 3), (1000, 776, 2056, 4),
+                                     (128, 256, 512, 5), (2304, 2560, 640, 6), (4096, 2048, 192, 4)])
+def test_cta_pair_kernel(dtype, M, N, K, S):
+    # 256 x 256 tile per CTA pair (each CTA 128 rows of A and of B), ragged in M, N, K
+    lay = "row_col"
+    A, B = operands(dtype, lay, M, N, K, seed=M * 7 + N + K)
+    C, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S)
+    p = st["plan"]
+    assert p["cta_pair"] == 1 and p["kernel"] == "umma_pair_ring" and p["grid"] % 2 == 0
+    check_full(dtype, lay, A, B, C, K)
+    # whole tiles on pairs: the same MMA order as one CTA per tile, bit for bit
+    Cd, std = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, no_stream_k=True)
+    assert std["plan"]["cta_pair"] == 1 and std["plan"]["sk_tiles"] == 0
+    C1, st1 = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, no_stream_k=True, no_cta_pair=True)
+    assert st1["plan"]["cta_pair"] == 0
+    assert torch.equal(Cd.view(torch.int16), C1.view(torch.int16))
+    if p["sk_tiles"] > 0:
+        assert p["grid"] == 2 * (st["sm_count"] // 2) and p["dp_tiles"] + p["sk_tiles"] == p["tiles"]
+        diff = (C.float() - Cd.float()).abs().max().item()
+        assert diff <= 2.0 ** -6 * Cd.float().abs().max().item()
