@@ -4,7 +4,8 @@
 One step = one GEMM over the workload (all steps of the K-loop hot path:
 tile decomposition, prologue, steady-state ring, drain, output epilogue).
 Default workload: FP16 GEMM M=N=K=4096, A row-major, B column-major, FP32
-accumulate, FP16 out, TMA-ring tcgen05 kernel at 4 stages.  Prints ONE JSON
+accumulate, FP16 out, TMA-ring tcgen05 kernel on CTA pairs at the library's
+default depth (6 stages).  Prints ONE JSON
 line (rank 0).  The INT8 4096^3 result, the stage sweep and the FP32
 ping-pong-vs-async comparison ride along as sub-objects.
 
@@ -40,12 +41,14 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="f16_4096")
-    ap.add_argument("--stages", type=int, default=4)
+    ap.add_argument("--stages", type=int, default=0, help="ring depth (0 = the library's default)")
     ap.add_argument("--variant", default="pipelined")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps for the sustained figure (0 = skip)")
     return ap.parse_args()
 
 
@@ -164,13 +167,13 @@ def device_sets(torch, w, A, B, dev, sets):
     return out
 
 
-def time_kernel(torch, gp, w, bufs, variant, stages, n, stream, bn=0):
+def time_kernel(torch, gp, w, bufs, variant, stages, n, stream, **opts):
     """Average device time of n launches (CUDA events around each launch on `stream`)."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for i in range(n):
         a, b, c = bufs[i % len(bufs)]
         evs[i][0].record(stream)
-        gp.gemm_pipelined(a, b, c, w.M, w.N, w.K, w.dtype, w.layout, stages, variant, stream, bn=bn)
+        gp.gemm_pipelined(a, b, c, w.M, w.N, w.K, w.dtype, w.layout, stages, variant, stream, **opts)
         evs[i][1].record(stream)
     stream.synchronize()
     st = gp.gemm_stats(sync=True)
@@ -190,13 +193,17 @@ def sweep(torch, gp, dev, stream, names, steps):
         bufs = device_sets(torch, w, A, B, dev, ROTATE if w.M * w.K < (1 << 27) else 2)
         unit = "TOPS" if w.dtype == "i8" else "TFLOPS"
         rows = []
-        cases = [("nopipe", 1), ("pingpong", 2)] + [("pipelined", s) for s in w.stages]
-        for variant, S in cases:
-            time_kernel(torch, gp, w, bufs, variant, S, 3, stream)      # warm-up
-            avg, best, st = time_kernel(torch, gp, w, bufs, variant, S, steps, stream)
-            rows.append({"variant": variant, "stages": S, "bn": st["plan"]["bn"], "ms": round(avg, 4),
-                         unit: round(w.ops / (avg * 1e-3) / 1e12, 2),
-                         "regs": st["regs_per_thread"], "smem": st["plan"]["smem_bytes"]})
+        cases = [("nopipe", 1, {}), ("pingpong", 2, {})] + [("pipelined", S, {}) for S in w.stages]
+        if w.dtype in ("f16", "bf16"):
+            # the same ring on one CTA per 128-row tile, whole tiles only (no pairs, no stream-K)
+            cases += [("pipelined", S, {"no_cta_pair": True, "no_stream_k": True}) for S in (4, 6)]
+        for variant, S, opts in cases:
+            time_kernel(torch, gp, w, bufs, variant, S, 3, stream, **opts)      # warm-up
+            avg, best, st = time_kernel(torch, gp, w, bufs, variant, S, steps, stream, **opts)
+            p = st["plan"]
+            rows.append({"variant": variant, "stages": S, "bm": p["bm"], "bn": p["bn"], "cta_pair": p["cta_pair"],
+                         "sk_tiles": p["sk_tiles"], "ms": round(avg, 4), unit: round(w.ops / (avg * 1e-3) / 1e12, 2),
+                         "regs": st["regs_per_thread"], "smem": p["smem_bytes"]})
         base = next(r for r in rows if r["variant"] == "pingpong")[unit]
         for r in rows:
             r["vs_pingpong"] = round(r[unit] / base, 3) if base else None
@@ -371,6 +378,36 @@ def main():
     kavg = statistics.mean(kern_ms)
     achieved = w.ops / (kavg * 1e-3) / 1e12
 
+    # ---- sustained: the same step back to back for a few seconds (clocks settle under the power cap) ----
+    sustained = None
+    if args.sustained_s > 0:
+        n_s = max(1, int(args.sustained_s * 1e3 / max(kavg, 1e-3)))
+        s_sampler = ClockSampler(local)
+        s_sampler.start()
+        with torch.cuda.stream(stream):
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            sw0 = time.time()
+            s0.record(stream)
+            for i in range(n_s):
+                gemm(i)
+            s1.record(stream)
+            torch.cuda.synchronize()
+            sw1 = time.time()
+        s_rows = s_sampler.stop()
+        st_s = gp.gemm_stats(sync=True)
+        if st_s["status"] != 0:
+            raise RuntimeError("sustained loop failed: status %d" % st_s["status"])
+        s_ms = s0.elapsed_time(s1)
+        s_value = w.ops * n_s / (s_ms * 1e-3) / 1e12
+        sustained = {"seconds": round(s_ms / 1e3, 2), "launches": n_s, "value": round(s_value, 2), "unit": unit,
+                     "clocks": ClockSampler.summarize(s_rows, sw0, sw1)}
+        if w.dtype in ("f16", "bf16"):
+            sp = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+            sustained.update({"peak": sp, "frac": round(s_value / sp, 4),
+                              "peak_source": peaks["_source"] + ": dense bf16 sustained"})
+
     # ---- end to end: pinned host operands in, result out, every step ----
     hA = to_device(torch, A, w.dtype, "cpu").pin_memory()
     hB = to_device(torch, B, w.dtype, "cpu").pin_memory()
@@ -445,6 +482,7 @@ def main():
         "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
                 "d2h_bytes_per_step": int(hC.numel() * hC.element_size()), "steps": e2e_steps},
         "gpu_launches": args.steps,
+        "sustained": sustained,
         "clocks": ClockSampler.summarize(clock_rows, wall0, wall1),
     }
 

@@ -129,7 +129,7 @@ cudaError_t get_workspace(int dev, cudaStream_t stream, size_t bytes, size_t nfl
     w->nflags = nflags;
     w->epoch = 0;
   }
-  if (++w->epoch == 0) w->epoch = 1;   // flags hold the epoch of the launch that set them
+  if (++w->epoch == 0) w->epoch = 1;   // split-tile counters are tagged with the launch's epoch
   *partials = w->partials;
   *flags = w->flags;
   *epoch = w->epoch;
@@ -171,28 +171,34 @@ int out_elem_bytes(int dtype) { return dtype == GP_I8_I32 || dtype == GP_F32 ? 4
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int default_stages(int family) { return family == 0 ? 3 : 4; }
+// FFMA: 3; IMMA: 4 (more buys nothing once the IMMA pipe is busy); tcgen05: 6
+// (the deepest ring the CTA-pair tile fits in 227 KB).
+int default_stages(int family) { return family == 0 ? 3 : (family == 1 ? 4 : 6); }
 
 // Persistent FP16/BF16 ring: when the output tiles do not fill whole waves of
 // `workers` (CTAs, or CTA pairs), keep all but the last full wave as whole
 // tiles and spread the K steps of the rest evenly over every worker
-// (stream-K).  Not worth it when each worker would get fewer than
-// kMinSkUnits K steps of the split tiles.
+// (stream-K).  A split costs a partial-tile write and read plus a flag wait,
+// a few microseconds; it pays only when whole-tile scheduling would leave the
+// average worker idle for at least kMinIdleSteps K steps at the tail.
 void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allowed) {
-  constexpr int64_t kMinSkUnits = 4;
+  constexpr int64_t kMinIdleSteps = 16;
+  constexpr int64_t kMinStepsPerWorker = 4;
   const int64_t T = p->tiles, G = workers;
   p->dp_tiles = static_cast<int32_t>(T);
   p->sk_tiles = 0;
   p->workspace_bytes = 0;
   p->grid = static_cast<int32_t>(ctas_per_worker * (T < G ? T : G));
   if (!allowed || G <= 0 || p->k_tiles <= 0 || T % G == 0) return;
+  const int64_t idle_tiles = ((T + G - 1) / G) * G - T;        // empty slots of the last wave
+  if (idle_tiles * p->k_tiles < kMinIdleSteps * G) return;
   const int64_t dp = T > G ? (T / G - 1) * G : 0;
   const int64_t skt = T - dp;
-  if (skt * p->k_tiles < kMinSkUnits * G) return;
+  if (skt * p->k_tiles < kMinStepsPerWorker * G) return;
   p->dp_tiles = static_cast<int32_t>(dp);
   p->sk_tiles = static_cast<int32_t>(skt);
   p->grid = static_cast<int32_t>(ctas_per_worker * G);
-  p->workspace_bytes = static_cast<int64_t>(p->grid) * 128 * p->bn * 4;   // one 128 x BN FP32 slot per CTA
+  p->workspace_bytes = static_cast<int64_t>(p->grid) * 2 * 128 * p->bn * 4;   // two 128 x BN FP32 slots per CTA
 }
 
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
@@ -529,8 +535,9 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     }
     SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, 0};
     if (plan.sk_tiles > 0) {
-      e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), static_cast<size_t>(plan.grid),
-                        &sk.workspace, &sk.flags, &sk.epoch);
+      const size_t counter_words = static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair ? 2 : 1) * 2;
+      e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), counter_words, &sk.workspace, &sk.flags,
+                        &sk.epoch);
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
     }
     LaunchArgs a;

@@ -23,7 +23,6 @@ enum WaitSite : uint32_t {
   kSiteEpilogueAccFull = 4,
   kSitePingPongMma = 5,
   kSiteDrain = 6,
-  kSitePartialFlag = 7,
 };
 
 struct KernelCtl {
@@ -32,19 +31,22 @@ struct KernelCtl {
   int32_t inject_lost_load; // test hook: producer skips the final tile load
 };
 
-// Stream-K split of a persistent launch: the first dp_tiles output tiles (in
-// raster order) are computed whole, CTA b taking tiles b, b+G, ...; the K-loops
-// of the next sk_tiles tiles form sk_tiles*k_tiles units of one K step each,
-// dealt out as G contiguous, equal ranges.  A CTA whose range starts inside a
-// tile writes that partial accumulator to workspace slot b and raises flags[b]
-// to `epoch`; the CTA owning the tile's first K step adds those partials and
-// writes C.
+// Stream-K split of a persistent launch over W workers (CTAs, or CTA pairs):
+// the first dp_tiles output tiles (in raster order) are computed whole,
+// worker w taking tiles w, w+W, ...; the K-loops of the next sk_tiles tiles
+// form sk_tiles*k_tiles units of one K step each, dealt out as W contiguous,
+// equal ranges.  Every segment of a tile split that way stores its FP32
+// partial accumulator in the workspace (slot (2w + j) * CTAs-per-worker +
+// rank, j = 0 for a worker's first segment, 1 for its last) and counts itself
+// on the tile's 64-bit counter {epoch, count}; the segment that brings the
+// count to the number of segments sums every partial in K order and writes C.
+// Nothing waits on another CTA, so no co-residency is required.
 struct SkParams {
   int32_t dp_tiles;
   int32_t sk_tiles;
-  float* workspace;         // G partial tiles, BM x BN FP32 each, row-major
-  uint32_t* flags;          // G words
-  uint32_t epoch;           // flag value of this launch
+  float* workspace;         // 2 * grid partial tiles, 128 x BN FP32 each
+  uint32_t* flags;          // sk_tiles * CTAs-per-worker 64-bit counters (as 32-bit word pairs)
+  uint32_t epoch;           // tag of this launch's counts
 };
 
 // ---------------------------------------------------------------------------

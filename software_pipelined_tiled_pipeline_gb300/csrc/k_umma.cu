@@ -11,7 +11,9 @@
 //    The accumulator is double-buffered in TMEM so the epilogue of one tile
 //    overlaps the K-loop of the next.  When the output tiles do not divide
 //    evenly over the CTAs, the K-loops of the last ones are split evenly
-//    across all CTAs (stream-K) with FP32 partials in a workspace.  This is the S-stage ring of
+//    across all CTAs (stream-K): each segment stores an FP32 partial in a
+//    workspace and the segment that completes last sums them and writes C,
+//    so no CTA ever waits on another.  This is the S-stage ring of
 //    "CUDA Kernel Study: Pipelining", Case 2 (prologue fills S slots, the
 //    steady state refills the slot just consumed, the tail drains), with TMA
 //    completion bytes on an mbarrier in place of cp.async commit/wait groups.
@@ -37,6 +39,7 @@ constexpr int BM = kUmmaBM;   // 128
 constexpr int BK = kUmmaBK;   // 64 elements = 128 bytes per row
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int UMMA_K = 16;    // K of one kind::f16 instruction
+constexpr uint64_t kSkPollNs = 20000;   // how long a split tile's first-K-step owner polls for the others
 
 struct UmmaBarriers {
   uint64_t full[kMaxStages];
@@ -48,6 +51,7 @@ struct UmmaBarriers {
   uint32_t tmem_base;
   int32_t consumed_hi;        // k-blocks consumed by the MMA thread (low 31 bits)
   CtaCtl ctl;
+  int32_t sk_last;            // epilogue: this CTA completed the last segment of a split tile
 };
 static_assert(sizeof(UmmaBarriers) <= kBarrierRegion, "barrier region too small");
 
@@ -183,16 +187,6 @@ __device__ __forceinline__ bool epi_bar_and(bool pred) {
       : "r"(pred ? 1u : 0u)
       : "memory");
   return r != 0;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Shapes of the ring kernel.  PAIR = false: one CTA per 128 x BN tile.
@@ -361,44 +355,65 @@ __global__ void __launch_bounds__(192, 1)
     const int row = q * 32 + lane;      // accumulator row of this CTA that this thread holds
     uint8_t* my_stage = epi + e * 2 * kUmmaEpiBufBytes;
     const int64_t units = static_cast<int64_t>(sk.sk_tiles) * kt;
+    const int64_t my_start = WorkIter::range_start(worker, units, workers);
     int sb = 0;
     for (int t = 0; it.next(tile, k0, k1); ++t) {
       int mb, nb;
       tile_coords(tile, m_blocks, n_blocks, mb, nb);
       const int a = t & 1;
-      // stream-K: partial writer (this worker's range starts inside the tile)
-      // or owner of the first K step of a split tile (adds the partials after it)
-      const bool writer = k0 > 0;
-      int w_first = 0, w_last = -1;
-      if (!writer && k1 < kt) {
-        const int64_t tile_end = static_cast<int64_t>(tile - sk.dp_tiles + 1) * kt;
-        w_first = worker + 1;
-        w_last = worker;
+      // A split tile (stream-K): every segment stores its FP32 partial; the
+      // segment that completes last sums all of them in K order and writes C.
+      const bool split = (k0 > 0) || (k1 < kt);
+      int64_t tile_start = 0;
+      int w_first = 0, w_last = -1, segments = 0;
+      unsigned long long* ctr = nullptr;
+      if (split) {
+        tile_start = static_cast<int64_t>(tile - sk.dp_tiles) * kt;
+        const int64_t tile_end = tile_start + kt;
+        w_first = static_cast<int>(tile_start * workers / units);
+        while (w_first + 1 < workers && WorkIter::range_start(w_first + 1, units, workers) <= tile_start) ++w_first;
+        while (w_first > 0 && WorkIter::range_start(w_first, units, workers) > tile_start) --w_first;
+        w_last = w_first;
         while (w_last + 1 < workers && WorkIter::range_start(w_last + 1, units, workers) < tile_end) ++w_last;
-        if (e == 0 && lane == 0) {
-          for (int w = w_first; w <= w_last && !cta->abort; ++w) {
-            const uint32_t* flag = sk.flags + w * Sh::CTAS + rank;
-            const uint64_t t0 = global_timer_ns();
-            while (ld_acquire_u32(flag) != sk.epoch) {
-              __nanosleep(64);
-              if (cta->abort) break;
-              if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                report_error(ctl.status, kDevErrTimeout, kSitePartialFlag);
-                cta->abort = 1;
-                break;
-              }
-            }
-          }
-        }
+        for (int w = w_first; w <= w_last; ++w)   // workers with a non-empty range
+          segments += WorkIter::range_start(w, units, workers) < WorkIter::range_start(w + 1, units, workers);
+        ctr = reinterpret_cast<unsigned long long*>(sk.flags) + (tile - sk.dp_tiles) * Sh::CTAS + rank;
       }
       uint32_t ok = 1;
       if (lane == 0) ok = mbar_wait(&bar->acc_full[a], (t >> 1) & 1, ctl, cta, kSiteEpilogueAccFull) ? 1u : 0u;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       // one decision for all four epilogue warps (they meet at named barriers below)
+      // Fast path of a split tile: the owner of its first K step (normally the
+      // segment that completes last) sees every other segment counted within
+      // kSkPollNs, adds their partials to its own accumulator and writes C
+      // directly.  Otherwise it falls back to the counted path below, which
+      // never waits, so no CTA depends on another being resident.
+      if (split && e == 0 && lane == 0) {
+        int fast_ok = 0;
+        if (worker == w_first) {
+          const uint64_t t0 = global_timer_ns();
+          for (;;) {
+            const unsigned long long seen = *reinterpret_cast<volatile unsigned long long*>(ctr);
+            const uint32_t count =
+                (static_cast<uint32_t>(seen >> 32) == sk.epoch) ? static_cast<uint32_t>(seen) : 0u;
+            if (count + 1u == static_cast<uint32_t>(segments)) { fast_ok = 1; break; }
+            if (global_timer_ns() - t0 > kSkPollNs) break;
+            __nanosleep(128);
+          }
+        }
+        bar->sk_last = fast_ok ? 2 : 0;
+        __threadfence();
+      }
       if (!epi_bar_and(ok != 0 && !cta->abort)) break;
+      const bool fast = split && bar->sk_last == 2;
       tc_fence_after();
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
       const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
+      // Partial tiles are stored column-quad-major, row innermost: float4 i of
+      // chunk c of row r in slot p at ((p * BN/64 + c) * 16 + i) * 128 + r, so
+      // the 32 lanes of a warp (32 consecutive rows) touch 512 contiguous bytes.
+      // Slot of (worker w, its first/last split segment j, CTA rank): (2w + j) * CTAS + rank.
+      const int my_slot = (2 * worker + (my_start >= tile_start ? 0 : 1)) * Sh::CTAS + rank;
 #pragma unroll 1
       for (int c = 0; c < BN / kUmmaEpiCols; ++c) {
         uint32_t v[64];
@@ -414,26 +429,32 @@ __global__ void __launch_bounds__(192, 1)
               mbar_arrive(&bar->acc_empty[a]);
           }
         }
-        if (writer) {
-          float4* dst = reinterpret_cast<float4*>(
-              sk.workspace + (static_cast<size_t>(blockIdx.x) * Sh::A_ROWS + row) * BN + c * kUmmaEpiCols);
+        if (fast) {
+          // own segment first (it holds K step 0), then the others in K order
+          for (int w = w_first + 1; w <= w_last; ++w) {
+            const int64_t ws = WorkIter::range_start(w, units, workers);
+            if (ws >= WorkIter::range_start(w + 1, units, workers)) continue;   // empty range: no segment
+            const float4* src = reinterpret_cast<const float4*>(sk.workspace) +
+                                (static_cast<size_t>((2 * w) * Sh::CTAS + rank) * (BN / kUmmaEpiCols) + c) * 16 *
+                                    Sh::A_ROWS +
+                                row;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float4 p = __ldcg(src + i * Sh::A_ROWS);
+              v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + p.x);
+              v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + p.y);
+              v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + p.z);
+              v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + p.w);
+            }
+          }
+        } else if (split) {
+          float4* dst = reinterpret_cast<float4*>(sk.workspace) +
+                        (static_cast<size_t>(my_slot) * (BN / kUmmaEpiCols) + c) * 16 * Sh::A_ROWS + row;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            __stcg(dst + i, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                        __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+            __stcg(dst + i * Sh::A_ROWS, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
           continue;
-        }
-        for (int w = w_first; w <= w_last; ++w) {
-          const float4* src = reinterpret_cast<const float4*>(
-              sk.workspace + (static_cast<size_t>(w * Sh::CTAS + rank) * Sh::A_ROWS + row) * BN + c * kUmmaEpiCols);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float4 p = __ldcg(src + i);
-            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + p.x);
-            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + p.y);
-            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + p.z);
-            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + p.w);
-          }
         }
         if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
@@ -441,11 +462,59 @@ __global__ void __launch_bounds__(192, 1)
         stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
         sb ^= 1;
       }
-      if (writer) {
-        // publish the partial: every epilogue thread's stores, then the flag
+      if (!split || fast) continue;
+      // count this segment in; the tile's counter is tagged with the launch epoch
+      __threadfence();
+      epi_bar_sync();
+      if (e == 0 && lane == 0) {
+        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+        uint32_t count;
+        for (;;) {
+          count = (static_cast<uint32_t>(old >> 32) == sk.epoch) ? static_cast<uint32_t>(old) : 0u;
+          const unsigned long long want = (static_cast<unsigned long long>(sk.epoch) << 32) | (count + 1u);
+          const unsigned long long seen = atomicCAS(ctr, old, want);
+          if (seen == old) break;
+          old = seen;
+        }
+        bar->sk_last = (count + 1u == static_cast<uint32_t>(segments)) ? 1 : 0;
         __threadfence();
-        epi_bar_sync();
-        if (e == 0 && lane == 0) st_release_u32(sk.flags + blockIdx.x, sk.epoch);
+      }
+      epi_bar_sync();
+      if (!bar->sk_last) continue;
+#pragma unroll 1
+      for (int c = 0; c < BN / kUmmaEpiCols; ++c) {
+        uint32_t v[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = 0u;
+        bool first = true;
+        for (int w = w_first; w <= w_last; ++w) {
+          const int64_t ws = WorkIter::range_start(w, units, workers);
+          if (ws >= WorkIter::range_start(w + 1, units, workers)) continue;   // empty range: no segment
+          const int slot = (2 * w + (ws >= tile_start ? 0 : 1)) * Sh::CTAS + rank;
+          const float4* src = reinterpret_cast<const float4*>(sk.workspace) +
+                              (static_cast<size_t>(slot) * (BN / kUmmaEpiCols) + c) * 16 * Sh::A_ROWS + row;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 p = __ldcg(src + i * Sh::A_ROWS);
+            if (first) {
+              v[4 * i] = __float_as_uint(p.x);
+              v[4 * i + 1] = __float_as_uint(p.y);
+              v[4 * i + 2] = __float_as_uint(p.z);
+              v[4 * i + 3] = __float_as_uint(p.w);
+            } else {
+              v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + p.x);
+              v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + p.y);
+              v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + p.z);
+              v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + p.w);
+            }
+          }
+          first = false;
+        }
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        const int x = nb * BN + c * kUmmaEpiCols;
+        stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
+        sb ^= 1;
       }
     }
     if (lane == 0) bulk_wait<0>();
@@ -692,11 +761,6 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
     attr[n].val.clusterDim.x = 2;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
-    ++n;
-  }
-  if (p.sk_tiles > 0) {
-    attr[n].id = cudaLaunchAttributeCooperative;   // stream-K workers wait on each other: all must be resident
-    attr[n].val.cooperative = 1;
     ++n;
   }
   cfg.attrs = attr;

@@ -37,7 +37,7 @@ WORKLOADS = {
                  "FP32 SGEMM M=N=K=1024 on the FFMA path, row-major, U[-1,1]"),
         Workload("i8_4096", "i8", "row_col", 4096, 4096, 4096, (2, 3, 4, 6), ("pipelined", "pingpong", "nopipe"),
                  "INT8 IGEMM M=N=K=4096, A row-major, B column-major, uniform int8, INT32 out"),
-        Workload("f16_4096", "f16", "row_col", 4096, 4096, 4096, (2, 3, 4, 6), ("pipelined", "pingpong", "nopipe"),
+        Workload("f16_4096", "f16", "row_col", 4096, 4096, 4096, (2, 3, 4, 5, 6), ("pipelined", "pingpong", "nopipe"),
                  "FP16 GEMM M=N=K=4096, A row-major, B column-major, U[-1,1], FP32 accumulate, FP16 out"),
         Workload("bf16_8192_k256", "bf16", "row_col", 8192, 8192, 256, tuple(range(2, 9))),
         Workload("bf16_8192_k1024", "bf16", "row_col", 8192, 8192, 1024, tuple(range(2, 9))),

@@ -141,7 +141,8 @@ def test_small_n_picks_narrow_tile(gp):
 
 
 def test_default_stages_and_variant_stage_rules(gp):
-    assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pipelined")["stages"] == 4
+    assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pipelined")["stages"] == 6
+    assert gp.gemm_plan(512, 512, 512, "i8", "row_col", 0, "pipelined")["stages"] == 4
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pingpong")["stages"] == 2
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "nopipe")["stages"] == 1
     assert gp.gemm_plan(512, 512, 512, "f32", "row_row", 0, "pipelined")["stages"] == 3
@@ -152,7 +153,7 @@ def test_compute_load_ratio_is_the_published_formula(gp):
         p = gp.gemm_plan(4096, 4096, 4096, dtype, layout, 2, "pipelined", bn=bn)
         bm, bn, bk = p["bm"], p["bn"], p["bk"]
         assert p["compute_load_ratio"] == pytest.approx(2 * bm * bn * bk / ((bm * bk + bk * bn) * esize))
-    # FP16 128x256x64 on one CTA: 2*128*256*64 / ((128*64 + 64*256) * 2) = 85.33 FLOP/byte
+    # FP16 128x64x64 on one CTA: 2*128*64*64 / ((128*64 + 64*64) * 2) FLOP per byte
     p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 7, "pipelined", bn=64)
     assert p["compute_load_ratio"] == pytest.approx(2 * 128 * 64 * 64 / ((128 * 64 + 64 * 64) * 2))
     p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 4, "pipelined", bn=128)
