@@ -84,6 +84,7 @@ typedef enum {
 #define GP_ERR_CUDA (-4)        /* a CUDA runtime call or the launch failed (detail in gp_stats.cuda_error) */
 #define GP_ERR_TIMEOUT (-5)     /* a bounded wait inside the kernel gave up; reported by gemm_stats(sync=1) */
 #define GP_ERR_SIZE (-6)        /* a dimension exceeds what the variant can address (see gemm_pipelined) */
+#define GP_ERR_SCRATCH (-7)     /* gemm_pipelined_noalloc: the plan needs more scratch than its fixed array holds */
 
 /* Tile, stage and resource choice for one problem ("pipeline-gpu-kernel",
  * Step 1 "shared-memory budget" and Step 2 "compute/load ratio"; "Part 4 --
@@ -185,6 +186,36 @@ const char* gemm_strerror(int code);
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch. */
 int gemm_abi_version(void);
+
+/*
+ * gemm_pipelined_noalloc -- the FP16/BF16 TMA-ring GEMM (GP_PIPELINED,
+ * GP_A_ROW_B_COL) without any device memory allocation.  The pages describe
+ * no such call; it exists for callers that cannot allocate device memory
+ * while they run: a framework that owns all device memory through its own
+ * pool and forbids allocations behind its back, a serving loop where the
+ * implicit device-wide synchronisation of cudaMalloc would stall other
+ * streams, or a process whose memory budget is fixed at start-up.
+ *
+ *   A, B, C, M, N, K, stages, stream: as gemm_pipelined; dtype must be
+ *   GP_F16_F32ACC_F16OUT or GP_BF16_F32ACC_BF16OUT (else GP_ERR_UNSUPPORTED).
+ *
+ * gemm_pipelined keeps the stream-K partial tiles of a split launch in a
+ * workspace it allocates on first use for each stream.  This entry point
+ * uses instead a fixed array compiled into the library: 40 MiB of partial
+ * tiles and 64 KiB of counters, held by every GPU that loads the library until
+ * the process exits.  That covers every split plan on a 152-SM GB300; a plan
+ * needing more returns GP_ERR_SCRATCH before anything is launched.
+ *
+ * The first call on a device looks up the array's device address and zeroes
+ * its counters (cudaGetSymbolAddress, cudaMemset; neither allocates), so make
+ * that first call before any stream capture.  All calls on a device share the
+ * one array and it keeps the previous call's contents: calls whose kernels
+ * overlap on the GPU (different streams, no ordering between them) race on
+ * it and may produce wrong results; calls ordered on one stream are safe.
+ * Returns and stats as gemm_pipelined.
+ */
+int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
+                           int stages, void* stream);
 
 #ifdef __cplusplus
 }

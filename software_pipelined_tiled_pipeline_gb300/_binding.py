@@ -30,6 +30,7 @@ GP_ERR_SMEM = -3
 GP_ERR_CUDA = -4
 GP_ERR_TIMEOUT = -5
 GP_ERR_SIZE = -6
+GP_ERR_SCRATCH = -7
 
 DTYPES = {"i8": GP_I8_I32, "f16": GP_F16_F32ACC_F16OUT, "bf16": GP_BF16_F32ACC_BF16OUT, "f32": GP_F32}
 LAYOUTS = {"row_col": GP_A_ROW_B_COL, "row_row": GP_A_ROW_B_ROW}
@@ -37,7 +38,7 @@ VARIANTS = {"pingpong": GP_PINGPONG, "pipelined": GP_PIPELINED, "nopipe": GP_NOP
 
 # exported symbols, in header order
 SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_stats", "gemm_strerror", "gemm_abi_version",
-           "gemm_probe_peak"]
+           "gemm_pipelined_noalloc", "gemm_probe_peak"]
 
 
 class GpPlan(ctypes.Structure):
@@ -109,6 +110,8 @@ def lib():
     L.gemm_strerror.restype = ctypes.c_char_p
     L.gemm_abi_version.argtypes = []
     L.gemm_abi_version.restype = ci
+    L.gemm_pipelined_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, vp]
+    L.gemm_pipelined_noalloc.restype = ci
     L.gemm_probe_peak.argtypes = [ci, ctypes.POINTER(ctypes.c_double), vp]
     L.gemm_probe_peak.restype = ci
     _lib = L
@@ -157,6 +160,17 @@ def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined
                                  s or None, ctypes.byref(opts))
     if check and rc != GP_OK:
         raise GemmError(rc, "gemm_pipelined")
+    return rc
+
+
+def gemm_pipelined_noalloc(A, B, C, M, N, K, dtype, stages=0, stream=0, check=True) -> int:
+    """FP16/BF16 TMA-ring GEMM through the allocation-free entry point: its
+    scratch is a fixed device array inside the library (see the C header)."""
+    s = getattr(stream, "cuda_stream", stream)
+    rc = lib().gemm_pipelined_noalloc(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K),
+                                      _enum(dtype, DTYPES, "dtype"), int(stages), s or None)
+    if check and rc != GP_OK:
+        raise GemmError(rc, "gemm_pipelined_noalloc")
     return rc
 
 

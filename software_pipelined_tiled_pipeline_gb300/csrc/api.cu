@@ -441,6 +441,49 @@ cudaError_t launch_zero_fill(void* C, int64_t bytes, cudaStream_t stream) {
 
 }  // namespace gp
 
+namespace gp {
+// ---------------------------------------------------------------------------
+// allocation-free entry point (gemm_pipelined_noalloc): fixed scratch array
+// ---------------------------------------------------------------------------
+// Stream-K scratch of gemm_pipelined_noalloc: FP32 partial tiles followed by
+// the split-tile counters.  It is a static device array, so every GPU that
+// loads this library holds it (41 MiB + 64 KiB) until the process exits, and
+// no call ever allocates.  40 MiB of partials covers every split plan of the
+// FP16/BF16 ring on a 152-SM GB300 (152 CTAs x 2 slots x 128 x 256 x 4 B).
+constexpr size_t kNoAllocPartialBytes = size_t(40) << 20;
+constexpr size_t kNoAllocCounterBytes = size_t(64) << 10;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocPartialBytes + kNoAllocCounterBytes];
+
+namespace {
+struct NoAllocDevice {
+  unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+  uint32_t epoch = 0;                 // tag of the counts of the latest call on this device
+};
+NoAllocDevice g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: translate the array's host-side
+// name into its device address and zero the counters.  Returns the address
+// and the epoch for this call.
+cudaError_t noalloc_setup(int dev, unsigned char** scratch, uint32_t* epoch) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.scratch) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(static_cast<unsigned char*>(p) + kNoAllocPartialBytes, 0, kNoAllocCounterBytes);
+    if (e != cudaSuccess) return e;
+    d.scratch = static_cast<unsigned char*>(p);
+  }
+  if (++d.epoch == 0) d.epoch = 1;
+  *scratch = d.scratch;
+  *epoch = d.epoch;
+  return cudaSuccess;
+}
+}  // namespace
+}  // namespace gp
+
 using namespace gp;
 
 extern "C" {
@@ -456,6 +499,7 @@ const char* gemm_strerror(int code) {
     case GP_ERR_CUDA: return "CUDA runtime or launch error";
     case GP_ERR_TIMEOUT: return "a bounded wait inside the kernel timed out";
     case GP_ERR_SIZE: return "a dimension is too large for this kernel";
+    case GP_ERR_SCRATCH: return "the plan needs more scratch memory than the fixed device array holds";
     default: return "unknown error code";
   }
 }
@@ -626,6 +670,88 @@ int gemm_stats(gp_stats* out, int sync) {
   }
   *out = s;
   return s.status;
+}
+
+int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
+                           int stages, void* stream) {
+  std::memset(&t_last.stats, 0, sizeof(t_last.stats));
+  t_last.stats.last_ms = -1.f;
+  t_last.kernel = nullptr;
+  t_last.timed = false;
+  t_last.stream = static_cast<cudaStream_t>(stream);
+  if (dtype != GP_F16_F32ACC_F16OUT && dtype != GP_BF16_F32ACC_BF16OUT) {
+    record(GP_ERR_UNSUPPORTED, 0);
+    return GP_ERR_UNSUPPORTED;
+  }
+  gp_plan plan;
+  int rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, 0, &plan);
+  if (rc != GP_OK) { record(rc, 0); return rc; }
+  t_last.stats.plan = plan;
+  if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }
+  if (!C || (K > 0 && (!A || !B))) { record(GP_ERR_ARG, 0); return GP_ERR_ARG; }
+  if (!alignment_ok(A, B, C, N, K, dtype)) { record(GP_ERR_UNSUPPORTED, 0); return GP_ERR_UNSUPPORTED; }
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (e == cudaSuccess) e = device_info(dev, &status, &sms);
+  unsigned char* scratch = nullptr;
+  uint32_t epoch = 0;
+  if (e == cudaSuccess) e = noalloc_setup(dev, &scratch, &epoch);
+  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  t_last.device = dev;
+  t_last.stats.sm_count = sms;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (K == 0) {
+    e = launch_zero_fill(C, M * N * out_elem_bytes(dtype), st);
+  } else {
+    rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, sms, &plan);
+    if (rc != GP_OK) { record(rc, 0); return rc; }
+    if (plan.cta_pair) {
+      int pairs = 0;
+      e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
+      if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (pairs < sms / 2) apply_stream_k(&plan, pairs, 2, true);
+    }
+    t_last.stats.plan = plan;
+    SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, epoch};
+    if (plan.sk_tiles > 0) {
+      const size_t counter_bytes = static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair ? 2 : 1) * 8;
+      if (static_cast<size_t>(plan.workspace_bytes) > kNoAllocPartialBytes || counter_bytes > kNoAllocCounterBytes) {
+        record(GP_ERR_SCRATCH, 0);
+        return GP_ERR_SCRATCH;
+      }
+      sk.workspace = reinterpret_cast<float*>(scratch);
+      sk.flags = reinterpret_cast<uint32_t*>(scratch + kNoAllocPartialBytes);
+    }
+    LaunchArgs a;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.M = static_cast<int32_t>(M);
+    a.N = static_cast<int32_t>(N);
+    a.K = static_cast<int32_t>(K);
+    a.dtype = dtype;
+    a.layout = GP_A_ROW_B_COL;
+    a.variant = GP_PIPELINED;
+    a.plan = plan;
+    a.stream = st;
+    a.ctl.status = status;
+    a.ctl.timeout_ns = kDefaultTimeoutNs;
+    a.ctl.inject_lost_load = 0;
+    a.sm_count = sms;
+    a.sk = sk;
+    const void* kernel = nullptr;
+    e = launch_umma(a, &kernel);
+    t_last.stats.plan = a.plan;
+    t_last.kernel = kernel;
+  }
+  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  record(GP_OK, 0);
+  return GP_OK;
 }
 
 }  // extern "C"
