@@ -56,10 +56,14 @@ typedef enum {
     GP_A_ROW_B_ROW = 1  /* A row-major, B row-major */
 } gp_layout;
 
-/* How the K-loop moves tiles from global to shared memory.  The MMA engine is
- * fixed by the dtype (tcgen05 UMMA with TMEM accumulators for FP16/BF16,
- * warp-level IMMA for INT8 -- sm_103a has no tcgen05 integer kind -- and FFMA
- * on the CUDA cores for FP32), so variants differ only in the data path. */
+/* How the K-loop moves tiles from global to shared memory.  The MMA engine
+ * follows the dtype: tcgen05 UMMA with TMEM accumulators for FP16/BF16; FFMA on
+ * the CUDA cores for FP32; for INT8, sm_103a has no tcgen05 integer kind, so
+ * GP_PIPELINED runs it on tcgen05 with the operands converted exactly to FP16
+ * and the FP32 accumulator restarted every 1024 K (all partial sums stay exact
+ * integers below 2^24), while the ping-pong and no-overlap variants (and
+ * GP_PIPELINED with gp_options.i8_imma) use warp-level IMMA.  Variants of one
+ * engine differ only in the data path. */
 typedef enum {
     /* Register-staged double buffer: global loads into registers, compute on
      * the current shared buffer, then store the registers into the other one
@@ -133,8 +137,9 @@ typedef struct gp_options {
     int32_t inject_lost_load;    /* test hook: the TMA producer skips the last tile load of the problem, so a
                                     consumer wait runs out and the call reports GP_ERR_TIMEOUT (no GPU fault) */
     int32_t no_stream_k;         /* 1: never split K-loops across CTAs (every tile computed whole) */
-    int32_t no_cta_pair;         /* 1: one CTA per output tile even where CTA pairs are available */
-    int32_t reserved[3];
+    int32_t no_cta_pair;         /* 1: one CTA per output tile even where CTA pairs are available (INT8: use IMMA) */
+    int32_t i8_imma;             /* INT8, GP_PIPELINED: 1 = warp-level IMMA ring instead of the tcgen05 path */
+    int32_t reserved[2];
 } gp_options;
 
 /*
@@ -170,6 +175,10 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
  */
 int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn,
               gp_plan* out);
+
+/* gemm_plan with the same options as gemm_pipelined_ex (opts may be NULL). */
+int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant,
+                 const gp_options* opts, gp_plan* out);
 
 /*
  * gemm_stats -- copy the calling thread's last-call record into *out.

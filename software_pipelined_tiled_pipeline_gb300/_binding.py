@@ -37,8 +37,8 @@ LAYOUTS = {"row_col": GP_A_ROW_B_COL, "row_row": GP_A_ROW_B_ROW}
 VARIANTS = {"pingpong": GP_PINGPONG, "pipelined": GP_PIPELINED, "nopipe": GP_NOPIPE}
 
 # exported symbols, in header order
-SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_stats", "gemm_strerror", "gemm_abi_version",
-           "gemm_pipelined_noalloc", "gemm_probe_peak"]
+SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_plan_ex", "gemm_stats", "gemm_strerror",
+           "gemm_abi_version", "gemm_pipelined_noalloc", "gemm_probe_peak"]
 
 
 class GpPlan(ctypes.Structure):
@@ -76,7 +76,7 @@ class GpOptions(ctypes.Structure):
     _fields_ = [
         ("bn", ctypes.c_int32), ("time_kernel", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
         ("inject_lost_load", ctypes.c_int32), ("no_stream_k", ctypes.c_int32), ("no_cta_pair", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("i8_imma", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -104,6 +104,8 @@ def lib():
     L.gemm_pipelined_ex.restype = ci
     L.gemm_plan.argtypes = [i64, i64, i64, ci, ci, ci, ci, ci, ctypes.POINTER(GpPlan)]
     L.gemm_plan.restype = ci
+    L.gemm_plan_ex.argtypes = [i64, i64, i64, ci, ci, ci, ci, ctypes.POINTER(GpOptions), ctypes.POINTER(GpPlan)]
+    L.gemm_plan_ex.restype = ci
     L.gemm_stats.argtypes = [ctypes.POINTER(GpStats), ci]
     L.gemm_stats.restype = ci
     L.gemm_strerror.argtypes = [ci]
@@ -142,12 +144,8 @@ def abi_version() -> int:
     return lib().gemm_abi_version()
 
 
-def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
-                   time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-                   check=True) -> int:
-    """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
-    stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0."""
-    s = getattr(stream, "cuda_stream", stream)
+def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
+             i8_imma=False):
     opts = GpOptions()
     opts.bn = int(bn)
     opts.time_kernel = 1 if time_kernel else 0
@@ -155,6 +153,17 @@ def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined
     opts.inject_lost_load = 1 if inject_lost_load else 0
     opts.no_stream_k = 1 if no_stream_k else 0
     opts.no_cta_pair = 1 if no_cta_pair else 0
+    opts.i8_imma = 1 if i8_imma else 0
+    return opts
+
+
+def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
+                   time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
+                   i8_imma=False, check=True) -> int:
+    """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
+    stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0."""
+    s = getattr(stream, "cuda_stream", stream)
+    opts = _options(bn, time_kernel, timeout_ns, inject_lost_load, no_stream_k, no_cta_pair, i8_imma)
     rc = lib().gemm_pipelined_ex(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"),
                                  _enum(layout, LAYOUTS, "layout"), int(stages), _enum(variant, VARIANTS, "variant"),
                                  s or None, ctypes.byref(opts))
@@ -174,10 +183,16 @@ def gemm_pipelined_noalloc(A, B, C, M, N, K, dtype, stages=0, stream=0, check=Tr
     return rc
 
 
-def gemm_plan(M, N, K, dtype, layout, stages=0, variant="pipelined", bn=0) -> dict:
+def gemm_plan(M, N, K, dtype, layout, stages=0, variant="pipelined", bn=0, **opts) -> dict:
+    """Tile/stage plan; keyword options as gemm_pipelined (then gemm_plan_ex is used)."""
     p = GpPlan()
-    rc = lib().gemm_plan(int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"), _enum(layout, LAYOUTS, "layout"),
-                         int(stages), _enum(variant, VARIANTS, "variant"), int(bn), ctypes.byref(p))
+    if opts:
+        o = _options(bn=bn, **opts)
+        rc = lib().gemm_plan_ex(int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"), _enum(layout, LAYOUTS, "layout"),
+                                int(stages), _enum(variant, VARIANTS, "variant"), ctypes.byref(o), ctypes.byref(p))
+    else:
+        rc = lib().gemm_plan(int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"), _enum(layout, LAYOUTS, "layout"),
+                             int(stages), _enum(variant, VARIANTS, "variant"), int(bn), ctypes.byref(p))
     if rc != GP_OK:
         raise GemmError(rc, "gemm_plan")
     return p.as_dict()

@@ -89,6 +89,8 @@ struct Workspace {
   uint32_t* flags = nullptr;
   size_t nflags = 0;
   uint32_t epoch = 0;
+  void* conv = nullptr;       // INT8 on tcgen05: FP16 copies of the operands
+  size_t conv_bytes = 0;
 };
 constexpr int kMaxWorkspaces = 64;
 Workspace g_ws[kMaxWorkspaces];
@@ -133,6 +135,34 @@ cudaError_t get_workspace(int dev, cudaStream_t stream, size_t bytes, size_t nfl
   *partials = w->partials;
   *flags = w->flags;
   *epoch = w->epoch;
+  return cudaSuccess;
+}
+
+// FP16 operand buffer of the INT8 tcgen05 path, per device and stream.
+cudaError_t get_conv_workspace(int dev, cudaStream_t stream, size_t bytes, void** conv) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace* w = nullptr;
+  for (auto& x : g_ws)
+    if (x.dev == dev && x.stream == stream) { w = &x; break; }
+  if (!w) {
+    for (auto& x : g_ws)
+      if (x.dev < 0) { w = &x; break; }
+    if (!w) return cudaErrorMemoryAllocation;
+    w->dev = dev;
+    w->stream = stream;
+  }
+  if (w->conv_bytes < bytes) {
+    cudaError_t e;
+    if (w->conv) {
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+      cudaFree(w->conv);
+      w->conv = nullptr;
+      w->conv_bytes = 0;
+    }
+    if ((e = cudaMalloc(&w->conv, bytes)) != cudaSuccess) return e;
+    w->conv_bytes = bytes;
+  }
+  *conv = w->conv;
   return cudaSuccess;
 }
 
@@ -203,7 +233,7 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
 
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
-              int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false) {
+              int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, bool i8_imma = false) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
@@ -232,6 +262,37 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->variant = variant;
   p->stages = S;
   const bool ring = variant == GP_PIPELINED;
+
+  const int i8_tc_stages = stages == 0 ? 6 : S;
+  if (fam == 1 && ring && !i8_imma && !no_pair && (bn_req == 0 || bn_req == 256) &&
+      ring_smem_total(i8_tc_stages * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax) {
+    // INT8 on tcgen05: FP16 operands, CTA pair per 256 x 256 tile, whole tiles.
+    // Deeper rings than this tile allows (7, 8 stages) run on the IMMA ring.
+    S = i8_tc_stages;
+    p->stages = S;
+    p->bm = 256;
+    p->bn = 256;
+    p->bk = kUmmaBK;
+    p->threads = 64 + 32 * 8;
+    p->stage_bytes = kUmmaPairStageBytes;
+    p->ring_bytes = S * p->stage_bytes;
+    p->smem_bytes = ring_smem_total(p->ring_bytes, kUmmaEpiBytes);
+    if (p->smem_bytes < kSmemPerCtaMax / 2 + 1024) p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
+    p->tmem_cols = 512;
+    p->persistent = 1;
+    p->cta_pair = 1;
+    p->kernel = "umma_i8_pair_ring";
+    p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
+    p->k_tiles = ceil_div(K, p->bk);
+    if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
+    p->grid = sm_count > 1 ? static_cast<int32_t>(2 * (p->tiles < sm_count / 2 ? p->tiles : sm_count / 2)) : 0;
+    p->dp_tiles = static_cast<int32_t>(p->tiles);
+    p->sk_tiles = 0;
+    p->workspace_bytes = (M + N) * K * 2;   // FP16 copies of A and B
+    // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B (FP16)
+    p->compute_load_ratio = 2.0 * 128 * 256 * p->bk / ((128.0 + 128.0) * p->bk * 2.0);
+    return GP_OK;
+  }
 
   int cands[3] = {0, 0, 0};
   int ncand = 0;
@@ -518,6 +579,22 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   return plan_impl(M, N, K, dtype, layout, stages, variant, bn, sms, out);
 }
 
+int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant,
+                 const gp_options* opts, gp_plan* out) {
+  if (!out) return GP_ERR_ARG;
+  int sms = 0;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  } else {
+    cudaGetLastError();
+  }
+  const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
+  return plan_impl(M, N, K, dtype, layout, stages, variant, opts ? opts->bn : 0, sms, out, opts && opts->no_stream_k,
+                   no_pair, opts && opts->i8_imma);
+}
+
 int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
                       int stages, int variant, void* stream, const gp_options* opts) {
   std::memset(&t_last.stats, 0, sizeof(t_last.stats));
@@ -529,7 +606,8 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
 
   // argument checks that need no device
   gp_plan plan;
-  int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan);
+  int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan, opts && opts->no_stream_k,
+                     opts && (opts->no_cta_pair || opts->inject_lost_load), opts && opts->i8_imma);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }   // empty output: nothing read or written
@@ -567,9 +645,18 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     e = launch_zero_fill(C, M * N * out_elem_bytes(dtype), st);
   } else {
     const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
-    rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair);
+    rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
+                   opts && opts->i8_imma);
     if (rc != GP_OK) { record(rc, 0); return rc; }
-    if (plan.cta_pair) {
+    void* conv = nullptr;
+    if (plan.cta_pair && dtype == GP_I8_I32) {
+      int pairs = 0;
+      e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
+      if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
+      if (e == cudaSuccess) e = get_conv_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), &conv);
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      plan.grid = static_cast<int32_t>(2 * (plan.tiles < pairs ? plan.tiles : pairs));
+    } else if (plan.cta_pair) {
       // pairs must sit on one TPC each: the resident count may be below SMs / 2
       int pairs = 0;
       e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
@@ -601,10 +688,11 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.ctl.inject_lost_load = opts ? opts->inject_lost_load : 0;
     a.sm_count = sms;
     a.sk = sk;
+    a.conv = conv;
     const void* kernel = nullptr;
     switch (family_of(dtype)) {
       case 0: e = launch_ffma(a, &kernel); break;
-      case 1: e = launch_imma(a, &kernel); break;
+      case 1: e = plan.cta_pair ? launch_umma_i8(a, &kernel) : launch_imma(a, &kernel); break;
       default: e = launch_umma(a, &kernel); break;
     }
     t_last.stats.plan = a.plan;
@@ -744,6 +832,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.ctl.inject_lost_load = 0;
     a.sm_count = sms;
     a.sk = sk;
+    a.conv = nullptr;
     const void* kernel = nullptr;
     e = launch_umma(a, &kernel);
     t_last.stats.plan = a.plan;

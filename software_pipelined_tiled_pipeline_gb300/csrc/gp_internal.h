@@ -93,6 +93,7 @@ struct LaunchArgs {
   cudaStream_t stream;
   KernelCtl ctl;
   SkParams sk;
+  void* conv;               // INT8 on tcgen05: FP16 copies of A then B, (M + N) * K halves
   int32_t sm_count;
 };
 
@@ -101,8 +102,10 @@ struct LaunchArgs {
 cudaError_t launch_ffma(LaunchArgs& a, const void** kernel);
 cudaError_t launch_imma(LaunchArgs& a, const void** kernel);
 cudaError_t launch_umma(LaunchArgs& a, const void** kernel);
-// CTA pairs of the FP16/BF16 pair kernel that fit on the device at once.
+// CTA pairs of the pair kernel for dtype (FP16/BF16 ring, or INT8 on tcgen05) that fit at once.
 cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs);
+// INT8 x INT8 -> INT32 on tcgen05 (FP16 operands, accumulator restarted every 1024 K).
+cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel);
 cudaError_t launch_zero_fill(void* C, int64_t bytes, cudaStream_t stream);
 
 // Tensor-map encoding (driver entry point obtained once through the runtime).

@@ -547,6 +547,292 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------
+// exact INT8 x INT8 -> INT32 on the tcgen05 tensor cores
+// ---------------------------------------------------------------------------
+// sm_103a has no integer kind of tcgen05.mma.  Every int8 value is exact in
+// FP16 and every product of two of them (|p| <= 2^14) is exact in FP32, so the
+// FP16 kind computes integer products exactly; an FP32 sum of such products
+// stays exact while its magnitude stays within 2^24, i.e. over at most
+// 2^24 / 2^14 = 1024 products.  The MMA therefore restarts the accumulator
+// every kI8ChunkSteps K steps (1024 elements), alternating the two TMEM
+// buffers, and the epilogue warps convert each finished chunk to int32 and add
+// it to a running int32 sum held in registers (wrapping modulo 2^32, as the
+// definition does).  The operands are converted to FP16 in global memory first
+// (i8_to_f16_kernel): converting inside the ring would triple the
+// shared-memory traffic per MMA.  Tile: 256 x 256 per CTA pair (each CTA
+// 128 rows of A and 128 of B, as for FP16), whole tiles only.
+constexpr int kI8ChunkSteps = 1024 / BK;   // 16 K steps of 64
+
+__global__ void i8_to_f16_kernel(const int8_t* __restrict__ a, __half* __restrict__ a16, int64_t na16,
+                                 const int8_t* __restrict__ b, __half* __restrict__ b16, int64_t nb16) {
+  const int64_t total = na16 + nb16;   // 16-element groups
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const bool is_a = i < na16;
+    const int64_t j = is_a ? i : i - na16;
+    const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(is_a ? a : b) + j);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int8_t lo = static_cast<int8_t>((w[q >> 1] >> (16 * (q & 1))) & 0xff);
+      const int8_t hi = static_cast<int8_t>((w[q >> 1] >> (16 * (q & 1) + 8)) & 0xff);
+      __half2 v = __halves2half2(__short2half_rn(lo), __short2half_rn(hi));
+      h[q] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(is_a ? a16 : b16) + 2 * j;
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+// Store one 32-row x 32-column INT32 chunk through a 4 KB swizzled staging
+// buffer and a TMA store (lane t holds row t).
+__device__ __forceinline__ void stage_and_store_i32(const uint32_t* v, uint8_t* buf, int lane, const CUtensorMap* tmap_c,
+                                                    int x, int y, bool in_bounds) {
+  const uint32_t base = smem_u32(buf);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + sw128_offset(lane, j)), "r"(v[4 * j]),
+                 "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                 : "memory");
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && in_bounds) tma_store_2d(tmap_c, base, x, y);
+  if (lane == 0) bulk_commit();
+}
+
+// Threads: warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 epilogue.
+// Epilogue warp w reads TMEM lane quarter w % 4 and column half (w - 2) / 4,
+// so each thread keeps the int32 running sums of 128 accumulator columns.
+constexpr int kI8EpiWarps = 8;
+constexpr int kI8Threads = 64 + 32 * kI8EpiWarps;
+
+__device__ __forceinline__ bool i8_epi_bar_and(bool pred) {   // the 8 epilogue warps only
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+template <bool PAIR>
+__global__ void __launch_bounds__(kI8Threads, 1)
+    umma_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl) {
+  constexpr int BN = 256;
+  constexpr int HALF = BN / 2;   // columns per epilogue thread
+  using Sh = RingShape<BN, PAIR>;
+  constexpr int STAGE = Sh::STAGE;
+  constexpr uint32_t IDESC = umma_idesc_f16(false, Sh::TILE_M, BN);
+  static_assert(kI8EpiWarps * kUmmaEpiBufBytes <= kUmmaEpiBytes, "staging region too small");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* ring = smem;
+  uint8_t* epi = smem + stages * STAGE;
+  UmmaBarriers* bar = reinterpret_cast<UmmaBarriers*>(epi + kUmmaEpiBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int m_blocks = (M + Sh::TILE_M - 1) / Sh::TILE_M;
+  const int n_blocks = (N + BN - 1) / BN;
+  const int tiles = m_blocks * n_blocks;
+  const int kt = (K + BK - 1) / BK;
+  const int chunks = (kt + kI8ChunkSteps - 1) / kI8ChunkSteps;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&bar->full[s], 1);
+      mbar_init(&bar->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bar->acc_full[a], 1);
+      mbar_init(&bar->acc_empty[a], Sh::CTAS * kI8EpiWarps);
+    }
+    mbar_init(&bar->drain, 1);
+    bar->ctl.abort = 0;
+    bar->consumed_hi = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    if (PAIR) {
+      tmem_alloc_pair(&bar->tmem_base, Sh::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bar->tmem_base, Sh::TMEM_COLS);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before();
+  if (PAIR) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_base;
+  CtaCtl* cta = &bar->ctl;
+  int issued = 0;
+
+  if (warp == 0) {
+    // ---------------- producer (every CTA) ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int tile = worker; tile < tiles && !cta->abort; tile += workers) {
+        int mb, nb;
+        tile_coords(tile, m_blocks, n_blocks, mb, nb);
+        const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
+        const int n_row = nb * BN + rank * Sh::B_ROWS;
+        for (int kb = 0; kb < kt; ++kb) {
+          if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto i8_producer_done;
+          uint8_t* slot = ring + s * STAGE;
+          if (PAIR) {
+            if (leader) mbar_arrive_expect_tx(&bar->full[s], 2 * STAGE);
+            const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), 0);
+            tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
+            tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
+          } else {
+            mbar_arrive_expect_tx(&bar->full[s], STAGE);
+            tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, m_row);
+            tma_load_2d(smem_u32(slot + Sh::A_BYTES), &tmB, &bar->full[s], kb * BK, n_row);
+          }
+          ++issued;
+          if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+      }
+    i8_producer_done:;
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: one accumulator buffer per 1024-element chunk of K ----------------
+    if (lane == 0 && leader) {
+      int s = 0;
+      uint32_t ph = 0;
+      int consumed = 0;
+      int t = 0;
+      bool ok = true;
+      for (int tile = worker; tile < tiles && ok; tile += workers) {
+        for (int c = 0; c < chunks && ok; ++c, ++t) {
+          const int a = t & 1;
+          if (!mbar_wait(&bar->acc_empty[a], ((t >> 1) & 1) ^ 1u, ctl, cta, kSiteMmaAccEmpty)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + a * BN;
+          const int kb0 = c * kI8ChunkSteps;
+          const int kb1 = min(kt, kb0 + kI8ChunkSteps);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(ring + s * STAGE);
+            const uint64_t da = umma_desc_sw128(a_addr);
+            const uint64_t db = umma_desc_sw128(a_addr + Sh::A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              const uint32_t acc = (kb == kb0 && kk == 0) ? 0u : 1u;
+              if (PAIR)
+                umma_f16_pair(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
+              else
+                umma_f16(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
+            }
+            if (PAIR) umma_commit_pair(&bar->empty[s], 0x3); else umma_commit(&bar->empty[s]);
+            ++consumed;
+            if (++s == stages) { s = 0; ph ^= 1u; }
+          }
+          if (!ok) break;
+          if (PAIR) umma_commit_pair(&bar->acc_full[a], 0x3); else umma_commit(&bar->acc_full[a]);
+        }
+      }
+      bar->consumed_hi = consumed;
+      if (PAIR) umma_commit_pair(&bar->drain, 0x1); else umma_commit(&bar->drain);
+      CtaCtl never_abort{0};
+      mbar_wait(&bar->drain, 0, ctl, &never_abort, kSiteDrain);
+    }
+  } else {
+    // ---------------- epilogue: int32 running sum of the exact FP32 chunk sums ----------------
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;     // column half of the accumulator
+    uint8_t* my_stage = epi + (warp - 2) * kUmmaEpiBufBytes;
+    int t = 0;
+    bool ok = true;
+    for (int tile = worker; tile < tiles && ok; tile += workers) {
+      int mb, nb;
+      tile_coords(tile, m_blocks, n_blocks, mb, nb);
+      uint32_t sum[HALF];
+#pragma unroll
+      for (int i = 0; i < HALF; ++i) sum[i] = 0u;
+      for (int c = 0; c < chunks; ++c, ++t) {
+        const int a = t & 1;
+        uint32_t w = 1;
+        if (lane == 0) w = mbar_wait(&bar->acc_full[a], (t >> 1) & 1, ctl, cta, kSiteEpilogueAccFull) ? 1u : 0u;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!i8_epi_bar_and(w != 0 && !cta->abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN + h * HALF;
+#pragma unroll
+        for (int sub = 0; sub < HALF / 32; ++sub) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(trow + sub * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)   // exact integers of magnitude <= 2^24 in FP32
+            sum[sub * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), 0));
+          else
+            mbar_arrive(&bar->acc_empty[a]);
+        }
+      }
+      if (!ok) break;
+      const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
+#pragma unroll
+      for (int sub = 0; sub < HALF / 32; ++sub) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        const int x = nb * BN + h * HALF + sub * 32;
+        stage_and_store_i32(sum + sub * 32, my_stage, lane, &tmC, x, y, (x < N) && (y < M));
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+
+  __syncthreads();
+  if (cta->abort && warp == 0 && lane == 0) {
+    CtaCtl never_abort{0};
+    if (PAIR) {
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+    } else {
+      for (int i = bar->consumed_hi; i < issued; ++i)
+        mbar_wait(&bar->full[i % stages], static_cast<uint32_t>((i / stages) & 1), ctl, &never_abort, kSiteDrain);
+    }
+  }
+  if (PAIR) {
+    tc_fence_before();
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    if (PAIR) tmem_dealloc_pair(tmem, Sh::TMEM_COLS); else tmem_dealloc(tmem, Sh::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // register-staged ping-pong and no-overlap variants (256 threads, one tile per CTA)
 // ---------------------------------------------------------------------------
 constexpr int kPPThreads = 256;
@@ -785,10 +1071,55 @@ cudaError_t launch_bn(LaunchArgs& a, const void** kernel) {
   return cudaGetLastError();
 }
 
-// Largest number of CTA pairs of the pair kernel that can be resident at once.
-cudaError_t max_pairs(bool bf16, int smem_bytes, int* pairs) {
-  const void* k = bf16 ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true>)
-                       : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true>);
+// INT8 on tcgen05: convert A and B to FP16 in the caller-stream workspace
+// (a.conv), then run the CTA-pair chunked-accumulation kernel on them.
+cudaError_t launch_i8(LaunchArgs& a, const void** kernel) {
+  using Sh = RingShape<256, true>;
+  const gp_plan& p = a.plan;
+  const uint64_t M = a.M, N = a.N, K = a.K;
+  __half* a16 = static_cast<__half*>(a.conv);
+  __half* b16 = a16 + M * K;
+  const int64_t na16 = static_cast<int64_t>(M * K / 16), nb16 = static_cast<int64_t>(N * K / 16);
+  int64_t blocks = (na16 + nb16 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(a.sm_count) * 16;
+  if (blocks > cap) blocks = cap;
+  i8_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, a.stream>>>(static_cast<const int8_t*>(a.A), a16, na16,
+                                                                    static_cast<const int8_t*>(a.B), b16, nb16);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap tmA, tmB, tmC;
+  if ((e = make_tmap_2d(&tmC, a.C, CU_TENSOR_MAP_DATA_TYPE_INT32, N, M, N * 4, 32, kUmmaEpiRows,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_2d(&tmA, a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, M, K * 2, BK, Sh::A_ROWS,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_2d(&tmB, b16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, N, K * 2, BK, Sh::B_ROWS,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  auto k = umma_i8_kernel<true>;
+  *kernel = reinterpret_cast<const void*>(k);
+  if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl);
+}
+
+// Largest number of CTA pairs of a pair kernel that can be resident at once.
+cudaError_t max_pairs(int kind, int smem_bytes, int* pairs) {
+  const void* k = kind == 2   ? reinterpret_cast<const void*>(umma_i8_kernel<true>)
+                  : kind == 1 ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true>)
+                              : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true>);
   cudaError_t e = ensure_smem_attr(k, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -823,7 +1154,9 @@ cudaError_t launch_umma(LaunchArgs& a, const void** kernel) {
 }
 
 cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs) {
-  return max_pairs(dtype == GP_BF16_F32ACC_BF16OUT, smem_bytes, pairs);
+  return max_pairs(dtype == GP_I8_I32 ? 2 : (dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0), smem_bytes, pairs);
 }
+
+cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel) { return launch_i8(a, kernel); }
 
 }  // namespace gp

@@ -129,27 +129,45 @@ def test_umma_single_cta_widths_follow_the_budget(gp, S):
 
 @pytest.mark.parametrize("S,bn", [(1, 128), (4, 128), (6, 128), (7, 128), (8, 64)])
 def test_imma_tile_shrinks_with_stages(gp, S, bn):
-    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined")
+    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", i8_imma=True)
+    assert p["kernel"] == "imma_ring" and p["cta_pair"] == 0
     assert p["bn"] == bn and p["bk"] == 128 and p["stage_bytes"] == (128 + bn) * 128
     assert p["k_tiles"] == 32 and p["smem_bytes"] <= 232448
+
+
+@pytest.mark.parametrize("S", range(1, 7))
+def test_int8_on_tcgen05_plan(gp, S):
+    # default INT8 ring: FP16 operands on CTA pairs, 256 x 256 tile, 32 KB per CTA per K step of 64
+    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined")
+    assert p["kernel"] == "umma_i8_pair_ring" and p["cta_pair"] == 1
+    assert (p["bm"], p["bn"], p["bk"], p["stages"]) == (256, 256, 64, S)
+    assert p["stage_bytes"] == (128 + 128) * 64 * 2 and p["tmem_cols"] == 512 and p["threads"] == 320
+    assert p["smem_bytes"] <= 232448 and p["k_tiles"] == 64 and p["tiles"] == 16 * 16
+    assert p["workspace_bytes"] == (4096 + 4096) * 4096 * 2
+    # bn=64 or an IMMA request selects the warp-level IMMA ring
+    assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", bn=64)["kernel"] == "imma_ring"
+    for deep in (7, 8):   # rings deeper than the pair tile allows run on IMMA
+        assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", deep, "pipelined")["kernel"] == "imma_ring"
+    assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", bn=128)["kernel"] == "imma_ring"
 
 
 def test_small_n_picks_narrow_tile(gp):
     assert gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 4, "pipelined")["bn"] == 128
     assert gp.gemm_plan(8192, 64, 8192, "bf16", "row_col", 4, "pipelined")["bn"] == 64
-    assert gp.gemm_plan(256, 100 + 4, 256, "i8", "row_col", 4, "pipelined")["bn"] == 128
+    assert gp.gemm_plan(256, 100 + 4, 256, "i8", "row_col", 4, "pipelined", i8_imma=True)["bn"] == 128
 
 
 def test_default_stages_and_variant_stage_rules(gp):
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pipelined")["stages"] == 6
-    assert gp.gemm_plan(512, 512, 512, "i8", "row_col", 0, "pipelined")["stages"] == 4
+    assert gp.gemm_plan(512, 512, 512, "i8", "row_col", 0, "pipelined")["stages"] == 6
+    assert gp.gemm_plan(512, 512, 512, "i8", "row_col", 0, "pipelined", i8_imma=True)["stages"] == 4
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pingpong")["stages"] == 2
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "nopipe")["stages"] == 1
     assert gp.gemm_plan(512, 512, 512, "f32", "row_row", 0, "pipelined")["stages"] == 3
 
 
 def test_compute_load_ratio_is_the_published_formula(gp):
-    for dtype, layout, esize, bn in (("f16", "row_col", 2, 128), ("i8", "row_col", 1, 0), ("f32", "row_row", 4, 0)):
+    for dtype, layout, esize, bn in (("f16", "row_col", 2, 128), ("i8", "row_col", 1, 64), ("f32", "row_row", 4, 0)):
         p = gp.gemm_plan(4096, 4096, 4096, dtype, layout, 2, "pipelined", bn=bn)
         bm, bn, bk = p["bm"], p["bn"], p["bk"]
         assert p["compute_load_ratio"] == pytest.approx(2 * bm * bn * bk / ((bm * bk + bk * bn) * esize))

@@ -242,3 +242,37 @@ def test_cta_pair_kernel(dtype, M, N, K, S):
         assert p["grid"] == 2 * (st["sm_count"] // 2) and p["dp_tiles"] + p["sk_tiles"] == p["tiles"]
         diff = (C.float() - Cd.float()).abs().max().item()
         assert diff <= 2.0 ** -6 * Cd.float().abs().max().item()
+
+
+@pytest.mark.parametrize("engine", ["tcgen05", "imma"])
+@pytest.mark.parametrize("stages", [1, 2, 4, 6])
+def test_int8_engines_every_depth(engine, stages):
+    M, N, K = 520, 260, 1040 + 2048
+    A, B = operands("i8", "row_col", M, N, K, seed=stages)
+    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined", stages=stages, i8_imma=(engine == "imma"))
+    assert st["plan"]["kernel"] == ("umma_i8_pair_ring" if engine == "tcgen05" else "imma_ring")
+    check_full("i8", "row_col", A, B, C, K)
+
+
+@pytest.mark.parametrize("K", [16, 1008, 1024, 1040, 2048, 4096, 5136])
+@pytest.mark.parametrize("fill", [(-128, -128), (-128, 127), (127, 127)])
+def test_int8_tcgen05_exact_at_extremes(K, fill):
+    # every product at the int8 extremes: |partial sums| reach 2^24 inside one
+    # 1024-element chunk of K and 2^26+ across chunks -- still bit-exact
+    M, N = 300, 136
+    A = np.full((M, K), fill[0], np.int8)
+    B = np.full((N, K), fill[1], np.int8)
+    A[::7, : K // 3] = 3
+    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined")
+    assert st["plan"]["kernel"] == "umma_i8_pair_ring"
+    check_full("i8", "row_col", A, B, C, K)
+
+
+def test_int8_tcgen05_sum_wraps_like_int32():
+    # 16384 * 131088 exceeds 2^31 - 1: the INT32 result wraps modulo 2^32
+    M, N, K = 128, 128, 131088
+    A = np.full((M, K), -128, np.int8)
+    B = np.full((N, K), -128, np.int8)
+    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined")
+    want = (16384 * K + (1 << 31)) % (1 << 32) - (1 << 31)
+    assert int(C[0, 0]) == want and bool((C == want).all())
