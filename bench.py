@@ -197,11 +197,15 @@ def sweep(torch, gp, dev, stream, names, steps):
         if w.dtype in ("f16", "bf16"):
             # the same ring on one CTA per 128-row tile, whole tiles only (no pairs, no stream-K)
             cases += [("pipelined", S, {"no_cta_pair": True, "no_stream_k": True}) for S in (4, 6)]
+        if w.dtype == "i8":
+            # the TMA ring feeding warp-level IMMA (the ping-pong and no-overlap rows use IMMA too)
+            cases += [("pipelined", S, {"i8_imma": True}) for S in w.stages]
         for variant, S, opts in cases:
             time_kernel(torch, gp, w, bufs, variant, S, 3, stream, **opts)      # warm-up
             avg, best, st = time_kernel(torch, gp, w, bufs, variant, S, steps, stream, **opts)
             p = st["plan"]
-            rows.append({"variant": variant, "stages": S, "bm": p["bm"], "bn": p["bn"], "cta_pair": p["cta_pair"],
+            rows.append({"variant": variant, "stages": S, "kernel": p["kernel"], "bm": p["bm"], "bn": p["bn"],
+                         "cta_pair": p["cta_pair"],
                          "sk_tiles": p["sk_tiles"], "ms": round(avg, 4), unit: round(w.ops / (avg * 1e-3) / 1e12, 2),
                          "regs": st["regs_per_thread"], "smem": p["smem_bytes"]})
         base = next(r for r in rows if r["variant"] == "pingpong")[unit]
@@ -453,6 +457,13 @@ def main():
                     "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
                     "peak_source": peaks["_source"] + ": dense bf16 burst (FP16 runs at the same tcgen05 rate)",
                     "kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5)}
+    elif w.dtype == "i8" and plan["kernel"].startswith("umma"):
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TOPS",
+                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
+                    "peak_source": peaks["_source"] + ": dense 16-bit tcgen05 rate (exact FP16 MMAs)",
+                    "kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5),
+                    "note": "launch time includes the int8->FP16 conversion kernel"}
     elif w.dtype == "i8":
         peak = gp.probe_peak("imma_s8", stream) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TOPS",
@@ -481,7 +492,7 @@ def main():
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
                 "d2h_bytes_per_step": int(hC.numel() * hC.element_size()), "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if plan["kernel"] == "umma_i8_pair_ring" else 1),
         "sustained": sustained,
         "clocks": ClockSampler.summarize(clock_rows, wall0, wall1),
     }
@@ -498,11 +509,20 @@ def main():
         i8 = sw.get("i8_4096")
         if i8:
             best = max((r for r in i8["rows"] if r["variant"] == "pipelined"), key=lambda r: r["TOPS"])
+            imma = max((r for r in i8["rows"] if r["kernel"] == "imma_ring"), key=lambda r: r["TOPS"])
             ipeak = gp.probe_peak("imma_s8", stream) / 1e12
-            line["int8"] = {"workload": "i8_4096", "value": best["TOPS"], "unit": "TOPS", "stages": best["stages"],
-                            "peak": round(ipeak, 1), "frac": round(best["TOPS"] / ipeak, 4),
-                            "peak_source": "measured IMMA mma.sync s8 probe (gemm_probe_peak)",
-                            "vs_pingpong": best["vs_pingpong"]}
+            tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+            line["int8"] = {
+                "workload": "i8_4096", "value": best["TOPS"], "unit": "TOPS", "stages": best["stages"],
+                "kernel": best["kernel"],
+                "peak": tpeak, "frac": round(best["TOPS"] / tpeak, 4),
+                "peak_source": peaks["_source"] + ": dense 16-bit tcgen05 rate (the INT8 products run as exact "
+                                                  "FP16 MMAs; includes the FP16 conversion pass)",
+                "imma_ceiling": round(ipeak, 1),
+                "imma_ceiling_source": "measured mma.sync s8 probe (gemm_probe_peak)",
+                "imma_ring": {"TOPS": imma["TOPS"], "stages": imma["stages"], "frac_of_imma_ceiling":
+                              round(imma["TOPS"] / ipeak, 4)},
+                "vs_pingpong": best["vs_pingpong"]}
         f16 = sw.get("f16_4096")
         if f16:
             best = max((r for r in f16["rows"] if r["variant"] == "pipelined"), key=lambda r: r["TFLOPS"])
