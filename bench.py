@@ -183,7 +183,41 @@ def time_kernel(torch, gp, w, bufs, variant, stages, n, stream, **opts):
     return statistics.mean(ms), min(ms), st
 
 
-def sweep(torch, gp, dev, stream, names, steps):
+def max_over_ranks(torch, dist, x, device):
+    """The largest x over all ranks (the slowest rank's time); x itself on one process."""
+    if dist is None:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ops_per_step, world, steps, total_ms):
+    """Whole-job rate in 1e12 units: every rank runs `steps` independent GEMMs in `total_ms`."""
+    return ops_per_step * world * steps / (total_ms * 1e-3) / 1e12
+
+
+FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12    # SMs x FP32 lanes x FMA x max SM clock
+
+
+def compute_peak(kernel, peaks, imma_peak):
+    """Peak FLOP/s (or OP/s) of the engine a kernel runs on, in units of 1e12."""
+    if kernel.startswith("umma"):
+        return peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    if kernel.startswith("imma"):
+        return imma_peak
+    return FFMA_PEAK_TFLOPS
+
+
+def roofline_row(w, kernel, ms, peaks, imma_peak):
+    """Which roof bounds this GEMM (compute or HBM, whichever takes longer) and the fraction of it reached."""
+    t_compute = w.ops / (compute_peak(kernel, peaks, imma_peak) * 1e12)
+    t_hbm = w.algorithmic_bytes / (peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9)
+    bound = "hbm" if t_hbm > t_compute else ("alu" if kernel.startswith("ffma") else "tensor")
+    return bound, round(max(t_compute, t_hbm) / (ms * 1e-3), 4)
+
+
+def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak):
     from software_pipelined_tiled_pipeline_gb300 import synth
     from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
     out = {}
@@ -208,6 +242,7 @@ def sweep(torch, gp, dev, stream, names, steps):
                          "cta_pair": p["cta_pair"],
                          "sk_tiles": p["sk_tiles"], "ms": round(avg, 4), unit: round(w.ops / (avg * 1e-3) / 1e12, 2),
                          "regs": st["regs_per_thread"], "smem": p["smem_bytes"]})
+            rows[-1]["bound"], rows[-1]["roofline_frac"] = roofline_row(w, p["kernel"], avg, peaks, imma_peak)
         base = next(r for r in rows if r["variant"] == "pingpong")[unit]
         for r in rows:
             r["vs_pingpong"] = round(r[unit] / base, 3) if base else None
@@ -373,12 +408,9 @@ def main():
         total_ms = t_start.elapsed_time(t_end)
         kern_ms = [a.elapsed_time(b) for a, b in evs]
 
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, pg, total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = w.ops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(w.ops, world, args.steps, total_ms)
     kavg = statistics.mean(kern_ms)
     achieved = w.ops / (kavg * 1e-3) / 1e12
 
@@ -437,11 +469,8 @@ def main():
         torch.cuda.synchronize()
         barrier()
         e2e_ms = e0.elapsed_time(e1)
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = w.ops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(torch, pg, e2e_ms, dev)
+    e2e_value = job_throughput(w.ops, world, e2e_steps, e2e_ms)
 
     if rank != 0:
         if pg is not None:
@@ -451,31 +480,29 @@ def main():
     plan = st["plan"]
     kernel_src = {"umma": "k_umma.cu", "imma": "k_imma.cu", "ffma": "k_ffma.cu"}[plan["kernel"].split("_")[0]]
     kernel_key = "%s@%s" % (plan["kernel"], w.name)
-    if w.dtype in ("f16", "bf16"):
-        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
-                    "peak_source": peaks["_source"] + ": dense bf16 burst (FP16 runs at the same tcgen05 rate)",
-                    "kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5)}
-    elif w.dtype == "i8" and plan["kernel"].startswith("umma"):
-        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TOPS",
-                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
-                    "peak_source": peaks["_source"] + ": dense 16-bit tcgen05 rate (exact FP16 MMAs)",
-                    "kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5),
-                    "note": "launch time includes the int8->FP16 conversion kernel"}
-    elif w.dtype == "i8":
-        peak = gp.probe_peak("imma_s8", stream) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TOPS",
-                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
-                    "peak_source": "measured IMMA mma.sync s8 probe (gemm_probe_peak)", "kernel": plan["kernel"],
-                    "kernel_avg_ms": round(kavg, 5)}
+    imma_peak = gp.probe_peak("imma_s8", stream) / 1e12 if plan["kernel"].startswith("imma") else None
+    bound, _ = roofline_row(w, plan["kernel"], kavg, peaks, imma_peak)
+    roofline = {"kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5),
+                "traffic": traffic_for(kernel_key, kernel_src)}
+    if bound == "hbm":
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        gbs = w.algorithmic_bytes / (kavg * 1e-3) / 1e9
+        roofline.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "algorithmic_bytes": w.algorithmic_bytes,
+                         "peak_source": peaks["_source"] + ": STREAM-style copy"})
     else:
-        peak = 152 * 128 * 2 * 2.07e9 / 1e12
-        roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": traffic_for(kernel_key, kernel_src),
-                    "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz", "kernel": plan["kernel"],
-                    "kernel_avg_ms": round(kavg, 5)}
+        peak = compute_peak(plan["kernel"], peaks, imma_peak)
+        roofline.update({"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
+                         "unit": "TOPS" if w.dtype == "i8" else "TFLOP/s", "frac": round(achieved / peak, 4)})
+        if plan["kernel"].startswith("umma") and w.dtype == "i8":
+            roofline.update({"peak_source": peaks["_source"] + ": dense 16-bit tcgen05 rate (exact FP16 MMAs)",
+                             "note": "launch time includes the int8->FP16 conversion kernel"})
+        elif plan["kernel"].startswith("umma"):
+            roofline["peak_source"] = peaks["_source"] + ": dense bf16 burst (FP16 runs at the same tcgen05 rate)"
+        elif plan["kernel"].startswith("imma"):
+            roofline["peak_source"] = "measured IMMA mma.sync s8 probe (gemm_probe_peak)"
+        else:
+            roofline["peak_source"] = "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz"
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -504,13 +531,14 @@ def main():
             names += ["bf16_8192_k256", "bf16_8192_k1024", "bf16_8192_k4096", "bf16_8192_k16384", "bf16_skinny"]
         del bufs
         torch.cuda.empty_cache()
-        sw = sweep(torch, gp, dev, stream, names, extra_steps)
+        imma_peak = gp.probe_peak("imma_s8", stream) / 1e12
+        sw = sweep(torch, gp, dev, stream, names, extra_steps, peaks, imma_peak)
         line["sweep"] = sw
         i8 = sw.get("i8_4096")
         if i8:
             best = max((r for r in i8["rows"] if r["variant"] == "pipelined"), key=lambda r: r["TOPS"])
             imma = max((r for r in i8["rows"] if r["kernel"] == "imma_ring"), key=lambda r: r["TOPS"])
-            ipeak = gp.probe_peak("imma_s8", stream) / 1e12
+            ipeak = imma_peak
             tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
             line["int8"] = {
                 "workload": "i8_4096", "value": best["TOPS"], "unit": "TOPS", "stages": best["stages"],

@@ -28,6 +28,13 @@ class Workload:
     def ops(self) -> int:
         return 2 * self.M * self.N * self.K
 
+    @property
+    def algorithmic_bytes(self) -> int:
+        """A and B read once, C written once: the least DRAM traffic of one GEMM."""
+        size_in = {"i8": 1, "f16": 2, "bf16": 2, "f32": 4}[self.dtype]
+        size_out = {"i8": 4, "f16": 2, "bf16": 2, "f32": 4}[self.dtype]
+        return (self.M + self.N) * self.K * size_in + self.M * self.N * size_out
+
 
 WORKLOADS = {
     w.name: w for w in [

@@ -1,0 +1,87 @@
+"""Host-side logic of the benchmark, on the CPU: which roof bounds each workload,
+the algorithmic bytes per GEMM, and the replicas' max-over-ranks timing run as
+two gloo processes."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from software_pipelined_tiled_pipeline_gb300.workloads import WORKLOADS
+
+PEAKS = {"hbm_gbs": 6780.0, "bf16_tflops": 1920.5, "bf16_tflops_sustained": 1716.2}
+
+
+def test_algorithmic_bytes():
+    # A + B read once, C written once
+    assert WORKLOADS["f16_4096"].algorithmic_bytes == 3 * 4096 * 4096 * 2
+    assert WORKLOADS["i8_4096"].algorithmic_bytes == 2 * 4096 * 4096 + 4096 * 4096 * 4
+    assert WORKLOADS["f32_1024"].algorithmic_bytes == 3 * 1024 * 1024 * 4
+    assert WORKLOADS["bf16_8192_k256"].algorithmic_bytes == 2 * 8192 * 256 * 2 + 8192 * 8192 * 2
+    assert WORKLOADS["bf16_skinny"].algorithmic_bytes == (8192 + 128) * 8192 * 2 + 8192 * 128 * 2
+
+
+@pytest.mark.parametrize("name,kernel,bound", [
+    ("f16_4096", "umma_pair_ring", "tensor"),
+    ("i8_4096", "umma_i8_pair_ring", "tensor"),
+    ("f32_1024", "ffma_ring", "alu"),
+    ("bf16_8192_k256", "umma_pair_ring", "hbm"),     # the 128 MiB C write outweighs 34 GFLOP
+    ("bf16_8192_k1024", "umma_pair_ring", "tensor"),
+    ("bf16_8192_k16384", "umma_pair_ring", "tensor"),
+    ("bf16_skinny", "umma_ring", "hbm"),             # the 128 MiB A read outweighs 17 GFLOP
+])
+def test_roofline_bound(name, kernel, bound):
+    w = WORKLOADS[name]
+    b, frac = bench.roofline_row(w, kernel, 1.0, PEAKS, 158.4)
+    assert b == bound
+    # a launch that takes exactly the roof's time is at fraction 1
+    t_roof = max(w.ops / (bench.compute_peak(kernel, PEAKS, 158.4) * 1e12), w.algorithmic_bytes / (6780.0 * 1e9))
+    assert bench.roofline_row(w, kernel, t_roof * 1e3, PEAKS, 158.4)[1] == pytest.approx(1.0, abs=1e-4)
+
+
+def test_imma_rows_use_the_imma_ceiling():
+    w = WORKLOADS["i8_4096"]
+    _, frac = bench.roofline_row(w, "imma_ring", w.ops / 158.4e12 * 1e3 * 2, PEAKS, 158.4)
+    assert frac == pytest.approx(0.5, abs=1e-4)
+
+
+def test_job_throughput_counts_every_rank():
+    # 4 ranks, 10 steps of 2*4096^3 each in 1 ms
+    assert bench.job_throughput(2 * 4096 ** 3, 4, 10, 1.0) == pytest.approx(4 * 10 * 2 * 4096 ** 3 / 1e-3 / 1e12)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, outdir):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        my_ms = 10.0 + 5.0 * rank                      # rank 1 is the slow one
+        total = bench.max_over_ranks(torch, dist, my_ms, "cpu")
+        value = bench.job_throughput(1e12, world, 3, total)
+        with open(os.path.join(outdir, "r%d.json" % rank), "w") as f:
+            json.dump({"total": total, "value": value}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_take_the_slowest_rank_gloo(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    res = [json.load(open(tmp_path / ("r%d.json" % r))) for r in range(world)]
+    for r in res:
+        assert r["total"] == 15.0
+        assert r["value"] == pytest.approx(1e12 * 2 * 3 / 15e-3 / 1e12)
+
+
+def test_single_process_needs_no_group():
+    assert bench.max_over_ranks(torch, None, 7.5, "cpu") == 7.5
