@@ -193,6 +193,15 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Tie every register of r to this point of the instruction stream: placed
+// right after tmem_wait_ld, it keeps the compiler from reading registers that
+// an earlier tcgen05.ld is still filling.
+template <int N>
+__device__ __forceinline__ void regs_after_wait(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // Shared-memory matrix descriptor (tcgen05 form) for a K-major operand tile
 // laid out by a TMA copy with 128-byte swizzling: rows of 128 bytes, 8-row
 // groups 1024 bytes apart.  Fields: start address >> 4 (bits 0-13), leading

@@ -86,11 +86,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 // store.  Lane t holds row (row0 + t).  The caller guarantees the staging
 // buffer is free (no TMA store still reading it).
 template <bool BF16>
-__device__ __forceinline__ void stage_and_store(const uint32_t (&v)[64], uint8_t* buf, int lane,
-                                                const CUtensorMap* tmap_c, int x, int y, bool in_bounds) {
-  uint32_t p[32];
+__device__ __forceinline__ void pack_chunk(const uint32_t (&v)[64], uint32_t (&p)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) p[i] = pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), BF16);
+}
+
+// Stage one packed 32-row x 64-column chunk (lane t: row t, 128 bytes) and store it with TMA.
+__device__ __forceinline__ void store_packed(const uint32_t (&p)[32], uint8_t* buf, int lane,
+                                             const CUtensorMap* tmap_c, int x, int y, bool in_bounds) {
   const uint32_t base = smem_u32(buf);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -105,12 +108,27 @@ __device__ __forceinline__ void stage_and_store(const uint32_t (&v)[64], uint8_t
   if (lane == 0) bulk_commit();
 }
 
-__device__ __forceinline__ void load_acc_chunk(uint32_t taddr, uint32_t (&v)[64]) {
+template <bool BF16>
+__device__ __forceinline__ void stage_and_store(const uint32_t (&v)[64], uint8_t* buf, int lane,
+                                                const CUtensorMap* tmap_c, int x, int y, bool in_bounds) {
+  uint32_t p[32];
+  pack_chunk<BF16>(v, p);
+  store_packed(p, buf, lane, tmap_c, x, y, in_bounds);
+}
+
+// Start reading 64 accumulator columns of this warp's 32 TMEM lanes into v;
+// v is valid after tmem_wait_ld().
+__device__ __forceinline__ void issue_acc_chunk(uint32_t taddr, uint32_t (&v)[64]) {
   uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
   uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
   tmem_ld_32x32b_x32(taddr, lo);
   tmem_ld_32x32b_x32(taddr + 32, hi);
+}
+
+__device__ __forceinline__ void load_acc_chunk(uint32_t taddr, uint32_t (&v)[64]) {
+  issue_acc_chunk(taddr, v);
   tmem_wait_ld();
+  regs_after_wait(v);
 }
 
 // Issue the four K=16 UMMAs of one 64-wide K step from slot (a_addr, b_addr).
@@ -171,20 +189,22 @@ struct WorkIter {
   }
 };
 
-__device__ __forceinline__ void epi_bar_sync() {   // the 4 epilogue warps only
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+template <int THREADS>
+__device__ __forceinline__ void epi_bar_sync() {   // the epilogue warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
 }
 
-// Barrier of the 4 epilogue warps that also ANDs a predicate over their 128 threads.
+// Barrier of the epilogue warps that also ANDs a predicate over their threads.
+template <int THREADS>
 __device__ __forceinline__ bool epi_bar_and(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}\n"
       : "=r"(r)
-      : "r"(pred ? 1u : 0u)
+      : "r"(pred ? 1u : 0u), "n"(THREADS)
       : "memory");
   return r != 0;
 }
@@ -199,6 +219,11 @@ __device__ __forceinline__ bool epi_bar_and(bool pred) {
 // signals it through the cluster window); the MMA commit releases slot s in
 // both CTAs at once, so the two producers run in lockstep; epilogue warps of
 // both CTAs hand an accumulator back by arriving on the even CTA's acc_empty.
+// Epilogue: warp w may read TMEM lanes 32 (w mod 4) .. +31 only, so four warps
+// cover the 128 rows, each taking every 64-column chunk of its rows.  (The
+// code also runs with eight, two per lane quarter splitting the columns; at
+// 10 warps a thread gets at most 168 registers, and the measured epilogue was
+// no faster, so the kernel uses four.)
 template <int BN, bool PAIR>
 struct RingShape {
   static constexpr int A_ROWS = 128;
@@ -208,10 +233,17 @@ struct RingShape {
   static constexpr int TILE_M = PAIR ? 2 * A_ROWS : A_ROWS;
   static constexpr int CTAS = PAIR ? 2 : 1;
   static constexpr uint32_t TMEM_COLS = 2 * BN;   // double-buffered 128 x BN FP32 accumulator per CTA
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int CHUNKS = BN / kUmmaEpiCols;                 // 64-column chunks per accumulator row
+  static constexpr int WARP_CHUNKS = CHUNKS / (EPI_WARPS / 4);     // chunks per epilogue warp
+  static constexpr int EPI_BUFS = kUmmaEpiBytes / (EPI_WARPS * kUmmaEpiBufBytes);   // staging buffers per warp
+  static_assert(EPI_BUFS >= 1 && WARP_CHUNKS >= 1, "epilogue split");
 };
 
 template <int BN, bool BF16, bool PAIR>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     umma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl,
                      SkParams sk) {
@@ -243,7 +275,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->acc_full[a], 1);
-      mbar_init(&bar->acc_empty[a], Sh::CTAS * kUmmaEpiWarps);
+      mbar_init(&bar->acc_empty[a], Sh::CTAS * Sh::EPI_WARPS);
     }
     mbar_init(&bar->drain, 1);
     bar->ctl.abort = 0;
@@ -353,7 +385,9 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int e = warp - 2;
     const int row = q * 32 + lane;      // accumulator row of this CTA that this thread holds
-    uint8_t* my_stage = epi + e * 2 * kUmmaEpiBufBytes;
+    const int c_begin = (e >> 2) * Sh::WARP_CHUNKS;   // this warp's 64-column chunks
+    const int c_end = c_begin + Sh::WARP_CHUNKS;
+    uint8_t* my_stage = epi + e * Sh::EPI_BUFS * kUmmaEpiBufBytes;
     const int64_t units = static_cast<int64_t>(sk.sk_tiles) * kt;
     const int64_t my_start = WorkIter::range_start(worker, units, workers);
     int sb = 0;
@@ -404,7 +438,7 @@ __global__ void __launch_bounds__(192, 1)
         bar->sk_last = fast_ok ? 2 : 0;
         __threadfence();
       }
-      if (!epi_bar_and(ok != 0 && !cta->abort)) break;
+      if (!epi_bar_and<Sh::EPI_THREADS>(ok != 0 && !cta->abort)) break;
       const bool fast = split && bar->sk_last == 2;
       tc_fence_after();
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
@@ -414,11 +448,45 @@ __global__ void __launch_bounds__(192, 1)
       // the 32 lanes of a warp (32 consecutive rows) touch 512 contiguous bytes.
       // Slot of (worker w, its first/last split segment j, CTA rank): (2w + j) * CTAS + rank.
       const int my_slot = (2 * worker + (my_start >= tile_start ? 0 : 1)) * Sh::CTAS + rank;
+      if (!split) {
+        // Whole tile: the TMEM load of chunk c + 1 is in flight while chunk c
+        // is converted, staged and stored (chunks unrolled, so no register
+        // that a load is still filling is carried around a loop).
+        uint32_t v[64];
+        issue_acc_chunk(trow + c_begin * kUmmaEpiCols, v);
+#pragma unroll
+        for (int j = 0; j < Sh::WARP_CHUNKS; ++j) {
+          const int c = c_begin + j;
+          tmem_wait_ld();
+          regs_after_wait(v);
+          uint32_t pk[32];
+          pack_chunk<BF16>(v, pk);
+          if (j + 1 < Sh::WARP_CHUNKS) {
+            issue_acc_chunk(trow + (c + 1) * kUmmaEpiCols, v);
+          } else {
+            // all of accumulator a has been read: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (PAIR)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), 0));
+              else
+                mbar_arrive(&bar->acc_empty[a]);
+            }
+          }
+          if (lane == 0) bulk_wait_read<Sh::EPI_BUFS - 1>();
+          __syncwarp();
+          const int x = nb * BN + c * kUmmaEpiCols;
+          store_packed(pk, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
+          if (++sb == Sh::EPI_BUFS) sb = 0;
+        }
+        continue;
+      }
 #pragma unroll 1
-      for (int c = 0; c < BN / kUmmaEpiCols; ++c) {
+      for (int c = c_begin; c < c_end; ++c) {
         uint32_t v[64];
         load_acc_chunk(trow + c * kUmmaEpiCols, v);
-        if (c == BN / kUmmaEpiCols - 1) {
+        if (c == c_end - 1) {
           // all of accumulator a is in registers: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
@@ -456,16 +524,16 @@ __global__ void __launch_bounds__(192, 1)
                                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
           continue;
         }
-        if (lane == 0) bulk_wait_read<1>();
+        if (lane == 0) bulk_wait_read<Sh::EPI_BUFS - 1>();
         __syncwarp();
         const int x = nb * BN + c * kUmmaEpiCols;
         stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
-        sb ^= 1;
+        if (++sb == Sh::EPI_BUFS) sb = 0;
       }
       if (!split || fast) continue;
       // count this segment in; the tile's counter is tagged with the launch epoch
       __threadfence();
-      epi_bar_sync();
+      epi_bar_sync<Sh::EPI_THREADS>();
       if (e == 0 && lane == 0) {
         unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
         uint32_t count;
@@ -479,10 +547,10 @@ __global__ void __launch_bounds__(192, 1)
         bar->sk_last = (count + 1u == static_cast<uint32_t>(segments)) ? 1 : 0;
         __threadfence();
       }
-      epi_bar_sync();
+      epi_bar_sync<Sh::EPI_THREADS>();
       if (!bar->sk_last) continue;
 #pragma unroll 1
-      for (int c = 0; c < BN / kUmmaEpiCols; ++c) {
+      for (int c = c_begin; c < c_end; ++c) {
         uint32_t v[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) v[i] = 0u;
@@ -510,11 +578,11 @@ __global__ void __launch_bounds__(192, 1)
           }
           first = false;
         }
-        if (lane == 0) bulk_wait_read<1>();
+        if (lane == 0) bulk_wait_read<Sh::EPI_BUFS - 1>();
         __syncwarp();
         const int x = nb * BN + c * kUmmaEpiCols;
         stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
-        sb ^= 1;
+        if (++sb == Sh::EPI_BUFS) sb = 0;
       }
     }
     if (lane == 0) bulk_wait<0>();
@@ -1037,7 +1105,7 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(p.threads);
+  cfg.blockDim = dim3(Sh::THREADS);   // the plan reports the same count
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[2];
@@ -1124,7 +1192,7 @@ cudaError_t max_pairs(int kind, int smem_bytes, int* pairs) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(kind == 2 ? kI8Threads : RingShape<256, true>::THREADS);
   cfg.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
