@@ -203,6 +203,9 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // FFMA: 3; IMMA: 4 (more buys nothing once the IMMA pipe is busy); tcgen05: 6
 // (the deepest ring the CTA-pair tile fits in 227 KB).
+// INT8 on tcgen05: bytes of the FP16 copies of A and B.
+int64_t i8_conv_bytes(int64_t M, int64_t N, int64_t K) { return (M + N) * K * 2; }
+
 int default_stages(int family) { return family == 0 ? 3 : (family == 1 ? 4 : 6); }
 
 // Persistent FP16/BF16 ring: when the output tiles do not fill whole waves of
@@ -288,7 +291,12 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     p->grid = sm_count > 1 ? static_cast<int32_t>(2 * (p->tiles < sm_count / 2 ? p->tiles : sm_count / 2)) : 0;
     p->dp_tiles = static_cast<int32_t>(p->tiles);
     p->sk_tiles = 0;
-    p->workspace_bytes = (M + N) * K * 2;   // FP16 copies of A and B
+    p->workspace_bytes = 0;
+    // Stream-K over the CTA pairs (int32 partials: exact in any order), only
+    // when the tiles do not fill one wave: with a partial last wave the
+    // heavier int32 split epilogue measured slower than whole tiles.
+    if (sm_count > 1 && p->tiles < sm_count / 2) apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
+    p->workspace_bytes += i8_conv_bytes(M, N, K);   // FP16 copies of A and B, after the partial tiles
     // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B (FP16)
     p->compute_load_ratio = 2.0 * 128 * 256 * p->bk / ((128.0 + 128.0) * p->bk * 2.0);
     return GP_OK;
@@ -649,26 +657,28 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
                    opts && opts->i8_imma);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     void* conv = nullptr;
-    if (plan.cta_pair && dtype == GP_I8_I32) {
-      int pairs = 0;
-      e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
-      if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
-      if (e == cudaSuccess) e = get_conv_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), &conv);
-      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
-      plan.grid = static_cast<int32_t>(2 * (plan.tiles < pairs ? plan.tiles : pairs));
-    } else if (plan.cta_pair) {
+    const bool i8_tc = plan.cta_pair && dtype == GP_I8_I32;
+    const int64_t conv_bytes = i8_tc ? i8_conv_bytes(M, N, K) : 0;
+    if (plan.cta_pair) {
       // pairs must sit on one TPC each: the resident count may be below SMs / 2
       int pairs = 0;
       e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
       if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
-      if (pairs < sms / 2) apply_stream_k(&plan, pairs, 2, !(opts && opts->no_stream_k));
+      if (pairs < sms / 2 && (!i8_tc || plan.tiles < pairs)) {
+        apply_stream_k(&plan, pairs, 2, !(opts && opts->no_stream_k));
+        plan.workspace_bytes += conv_bytes;
+      }
+      if (i8_tc) {
+        e = get_conv_workspace(dev, st, static_cast<size_t>(conv_bytes), &conv);
+        if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      }
     }
     SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, 0};
     if (plan.sk_tiles > 0) {
       const size_t counter_words = static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair ? 2 : 1) * 2;
-      e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), counter_words, &sk.workspace, &sk.flags,
-                        &sk.epoch);
+      e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes - conv_bytes), counter_words, &sk.workspace,
+                        &sk.flags, &sk.epoch);
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
     }
     LaunchArgs a;

@@ -149,11 +149,14 @@ __device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint32_t a_addr, ui
 // ---------------------------------------------------------------------------
 
 // The ordered list of work items of one worker (a CTA, or a CTA pair), walked
-// identically by the producer, the MMA issuer and the epilogue: whole tiles
-// first (w, w+W, ... below dp_tiles), then this worker's contiguous range of
-// the stream-K units (one unit = one K step of one of the sk_tiles tiles after
-// them), cut at tile boundaries.  An item is (tile, first K step, one past the
-// last K step).
+// identically by the producer, the MMA issuer and the epilogue: first this
+// worker's contiguous range of the stream-K units (one unit = one K step of
+// one of the sk_tiles tiles after the whole ones), cut at tile boundaries,
+// then its whole tiles (w, w+W, ... below dp_tiles).  Split tiles go first so
+// that their partial-tile traffic and fix-ups overlap the MMAs of the whole
+// tiles instead of trailing the last one (measured: the fix-up of a split
+// tile takes 6-8 us after its last MMA).  An item is (tile, first K step, one
+// past the last K step).
 struct WorkIter {
   int dp_tiles, kt, next_dp, step;
   int64_t u, u_end;
@@ -171,6 +174,15 @@ struct WorkIter {
     u_end = range_start(worker + 1, units, workers);
   }
   __device__ __forceinline__ bool next(int& tile, int& k0, int& k1) {
+    if (u < u_end) {
+      const int t = static_cast<int>(u / kt);
+      k0 = static_cast<int>(u - static_cast<int64_t>(t) * kt);
+      const int64_t left = u_end - u;
+      k1 = (left < kt - k0) ? k0 + static_cast<int>(left) : kt;
+      tile = dp_tiles + t;
+      u += k1 - k0;
+      return true;
+    }
     if (next_dp < dp_tiles) {
       tile = next_dp;
       k0 = 0;
@@ -178,16 +190,79 @@ struct WorkIter {
       next_dp += step;
       return true;
     }
-    if (u >= u_end) return false;
-    const int t = static_cast<int>(u / kt);
-    k0 = static_cast<int>(u - static_cast<int64_t>(t) * kt);
-    const int64_t left = u_end - u;
-    k1 = (left < kt - k0) ? k0 + static_cast<int>(left) : kt;
-    tile = dp_tiles + t;
-    u += k1 - k0;
-    return true;
+    return false;
   }
 };
+
+// One tile of the stream-K range as the epilogue sees it: the workers whose
+// unit ranges overlap its K steps (w_first .. w_last; a worker whose range is
+// empty holds no segment), the number of segments, and the tile's 64-bit
+// counter {launch epoch, segments counted} for this CTA rank.
+struct SplitTile {
+  int64_t start;     // stream-K unit of the tile's first K step
+  int64_t units;     // units of the whole stream-K range
+  int workers;
+  int w_first, w_last, segments;
+  unsigned long long* ctr;
+
+  __device__ __forceinline__ void init(int tile, int kt, const SkParams& sk, int workers_, int ctas, uint32_t rank) {
+    workers = workers_;
+    units = static_cast<int64_t>(sk.sk_tiles) * kt;
+    start = static_cast<int64_t>(tile - sk.dp_tiles) * kt;
+    const int64_t end = start + kt;
+    w_first = static_cast<int>(start * workers / units);
+    while (w_first + 1 < workers && WorkIter::range_start(w_first + 1, units, workers) <= start) ++w_first;
+    while (w_first > 0 && WorkIter::range_start(w_first, units, workers) > start) --w_first;
+    w_last = w_first;
+    while (w_last + 1 < workers && WorkIter::range_start(w_last + 1, units, workers) < end) ++w_last;
+    segments = 0;
+    for (int w = w_first; w <= w_last; ++w) segments += has_segment(w);
+    ctr = reinterpret_cast<unsigned long long*>(sk.flags) + static_cast<int64_t>(tile - sk.dp_tiles) * ctas + rank;
+  }
+  __device__ __forceinline__ bool has_segment(int w) const {
+    return WorkIter::range_start(w, units, workers) < WorkIter::range_start(w + 1, units, workers);
+  }
+  // Workspace slot of worker w's segment of this tile: (2w + j) * CTAs + rank,
+  // j = 0 if it is the worker's first segment, 1 if its last.
+  __device__ __forceinline__ int slot(int w, int ctas, uint32_t rank) const {
+    return (2 * w + (WorkIter::range_start(w, units, workers) >= start ? 0 : 1)) * ctas + static_cast<int>(rank);
+  }
+  __device__ __forceinline__ static uint32_t count_of(unsigned long long word, uint32_t epoch) {
+    return (static_cast<uint32_t>(word >> 32) == epoch) ? static_cast<uint32_t>(word) : 0u;
+  }
+  // The owner of the first K step: true if every other segment is counted
+  // within kSkPollNs (bounded; false means fall back to counting in).
+  __device__ __forceinline__ bool poll_others(uint32_t epoch) const {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+      if (count_of(*reinterpret_cast<volatile unsigned long long*>(ctr), epoch) + 1u ==
+          static_cast<uint32_t>(segments))
+        return true;
+      if (global_timer_ns() - t0 > kSkPollNs) return false;
+      __nanosleep(128);
+    }
+  }
+  // Count this segment in; true if it was the last one of the tile.
+  __device__ __forceinline__ bool count_in(uint32_t epoch) const {
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    for (;;) {
+      const uint32_t count = count_of(old, epoch);
+      const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (count + 1u);
+      const unsigned long long seen = atomicCAS(ctr, old, want);
+      if (seen == old) return count + 1u == static_cast<uint32_t>(segments);
+      old = seen;
+    }
+  }
+};
+
+// Partial tiles are stored column-quad-major, row innermost: 16-byte group i
+// (4 columns) of 64-column chunk c of row r in slot p at
+// ((p * BN/64 + c) * 16 + i) * 128 + r, so the 32 lanes of a warp (32
+// consecutive rows) touch 512 contiguous bytes.  Index in 16-byte units.
+template <int BN>
+__device__ __forceinline__ size_t partial_at(int slot, int c, int i, int row) {
+  return ((static_cast<size_t>(slot) * (BN / kUmmaEpiCols) + c) * 16 + i) * 128 + row;
+}
 
 template <int THREADS>
 __device__ __forceinline__ void epi_bar_sync() {   // the epilogue warps only
@@ -302,6 +377,11 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
   else
     __syncthreads();
   tc_fence_after();
+  // Launched as a programmatic dependent, the set-up above overlaps the tail
+  // of the previous kernel; from here on the operands, C and the stream-K
+  // workspace may be touched only once that kernel has completed.
+  pdl_launch_dependents();
+  pdl_wait();
   const uint32_t tmem = bar->tmem_base;
   CtaCtl* cta = &bar->ctl;
   int issued = 0;  // producer only
@@ -388,8 +468,6 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     const int c_begin = (e >> 2) * Sh::WARP_CHUNKS;   // this warp's 64-column chunks
     const int c_end = c_begin + Sh::WARP_CHUNKS;
     uint8_t* my_stage = epi + e * Sh::EPI_BUFS * kUmmaEpiBufBytes;
-    const int64_t units = static_cast<int64_t>(sk.sk_tiles) * kt;
-    const int64_t my_start = WorkIter::range_start(worker, units, workers);
     int sb = 0;
     for (int t = 0; it.next(tile, k0, k1); ++t) {
       int mb, nb;
@@ -398,21 +476,8 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       // A split tile (stream-K): every segment stores its FP32 partial; the
       // segment that completes last sums all of them in K order and writes C.
       const bool split = (k0 > 0) || (k1 < kt);
-      int64_t tile_start = 0;
-      int w_first = 0, w_last = -1, segments = 0;
-      unsigned long long* ctr = nullptr;
-      if (split) {
-        tile_start = static_cast<int64_t>(tile - sk.dp_tiles) * kt;
-        const int64_t tile_end = tile_start + kt;
-        w_first = static_cast<int>(tile_start * workers / units);
-        while (w_first + 1 < workers && WorkIter::range_start(w_first + 1, units, workers) <= tile_start) ++w_first;
-        while (w_first > 0 && WorkIter::range_start(w_first, units, workers) > tile_start) --w_first;
-        w_last = w_first;
-        while (w_last + 1 < workers && WorkIter::range_start(w_last + 1, units, workers) < tile_end) ++w_last;
-        for (int w = w_first; w <= w_last; ++w)   // workers with a non-empty range
-          segments += WorkIter::range_start(w, units, workers) < WorkIter::range_start(w + 1, units, workers);
-        ctr = reinterpret_cast<unsigned long long*>(sk.flags) + (tile - sk.dp_tiles) * Sh::CTAS + rank;
-      }
+      SplitTile sp;
+      if (split) sp.init(tile, kt, sk, workers, Sh::CTAS, rank);
       uint32_t ok = 1;
       if (lane == 0) ok = mbar_wait(&bar->acc_full[a], (t >> 1) & 1, ctl, cta, kSiteEpilogueAccFull) ? 1u : 0u;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -423,19 +488,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       // directly.  Otherwise it falls back to the counted path below, which
       // never waits, so no CTA depends on another being resident.
       if (split && e == 0 && lane == 0) {
-        int fast_ok = 0;
-        if (worker == w_first) {
-          const uint64_t t0 = global_timer_ns();
-          for (;;) {
-            const unsigned long long seen = *reinterpret_cast<volatile unsigned long long*>(ctr);
-            const uint32_t count =
-                (static_cast<uint32_t>(seen >> 32) == sk.epoch) ? static_cast<uint32_t>(seen) : 0u;
-            if (count + 1u == static_cast<uint32_t>(segments)) { fast_ok = 1; break; }
-            if (global_timer_ns() - t0 > kSkPollNs) break;
-            __nanosleep(128);
-          }
-        }
-        bar->sk_last = fast_ok ? 2 : 0;
+        bar->sk_last = (worker == sp.w_first && sp.poll_others(sk.epoch)) ? 2 : 0;
         __threadfence();
       }
       if (!epi_bar_and<Sh::EPI_THREADS>(ok != 0 && !cta->abort)) break;
@@ -443,11 +496,6 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       tc_fence_after();
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
       const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
-      // Partial tiles are stored column-quad-major, row innermost: float4 i of
-      // chunk c of row r in slot p at ((p * BN/64 + c) * 16 + i) * 128 + r, so
-      // the 32 lanes of a warp (32 consecutive rows) touch 512 contiguous bytes.
-      // Slot of (worker w, its first/last split segment j, CTA rank): (2w + j) * CTAS + rank.
-      const int my_slot = (2 * worker + (my_start >= tile_start ? 0 : 1)) * Sh::CTAS + rank;
       if (!split) {
         // Whole tile: the TMEM load of chunk c + 1 is in flight while chunk c
         // is converted, staged and stored (chunks unrolled, so no register
@@ -499,13 +547,10 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
         }
         if (fast) {
           // own segment first (it holds K step 0), then the others in K order
-          for (int w = w_first + 1; w <= w_last; ++w) {
-            const int64_t ws = WorkIter::range_start(w, units, workers);
-            if (ws >= WorkIter::range_start(w + 1, units, workers)) continue;   // empty range: no segment
+          for (int w = sp.w_first + 1; w <= sp.w_last; ++w) {
+            if (!sp.has_segment(w)) continue;
             const float4* src = reinterpret_cast<const float4*>(sk.workspace) +
-                                (static_cast<size_t>((2 * w) * Sh::CTAS + rank) * (BN / kUmmaEpiCols) + c) * 16 *
-                                    Sh::A_ROWS +
-                                row;
+                                partial_at<BN>(sp.slot(w, Sh::CTAS, rank), c, 0, row);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float4 p = __ldcg(src + i * Sh::A_ROWS);
@@ -516,8 +561,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
             }
           }
         } else if (split) {
-          float4* dst = reinterpret_cast<float4*>(sk.workspace) +
-                        (static_cast<size_t>(my_slot) * (BN / kUmmaEpiCols) + c) * 16 * Sh::A_ROWS + row;
+          float4* dst = reinterpret_cast<float4*>(sk.workspace) + partial_at<BN>(sp.slot(worker, Sh::CTAS, rank), c, 0, row);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             __stcg(dst + i * Sh::A_ROWS, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
@@ -535,16 +579,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       __threadfence();
       epi_bar_sync<Sh::EPI_THREADS>();
       if (e == 0 && lane == 0) {
-        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
-        uint32_t count;
-        for (;;) {
-          count = (static_cast<uint32_t>(old >> 32) == sk.epoch) ? static_cast<uint32_t>(old) : 0u;
-          const unsigned long long want = (static_cast<unsigned long long>(sk.epoch) << 32) | (count + 1u);
-          const unsigned long long seen = atomicCAS(ctr, old, want);
-          if (seen == old) break;
-          old = seen;
-        }
-        bar->sk_last = (count + 1u == static_cast<uint32_t>(segments)) ? 1 : 0;
+        bar->sk_last = sp.count_in(sk.epoch) ? 1 : 0;
         __threadfence();
       }
       epi_bar_sync<Sh::EPI_THREADS>();
@@ -555,12 +590,10 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) v[i] = 0u;
         bool first = true;
-        for (int w = w_first; w <= w_last; ++w) {
-          const int64_t ws = WorkIter::range_start(w, units, workers);
-          if (ws >= WorkIter::range_start(w + 1, units, workers)) continue;   // empty range: no segment
-          const int slot = (2 * w + (ws >= tile_start ? 0 : 1)) * Sh::CTAS + rank;
+        for (int w = sp.w_first; w <= sp.w_last; ++w) {
+          if (!sp.has_segment(w)) continue;
           const float4* src = reinterpret_cast<const float4*>(sk.workspace) +
-                              (static_cast<size_t>(slot) * (BN / kUmmaEpiCols) + c) * 16 * Sh::A_ROWS + row;
+                              partial_at<BN>(sp.slot(w, Sh::CTAS, rank), c, 0, row);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float4 p = __ldcg(src + i * Sh::A_ROWS);
@@ -631,27 +664,55 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
 // 128 rows of A and 128 of B, as for FP16), whole tiles only.
 constexpr int kI8ChunkSteps = 1024 / BK;   // 16 K steps of 64
 
-__global__ void i8_to_f16_kernel(const int8_t* __restrict__ a, __half* __restrict__ a16, int64_t na16,
-                                 const int8_t* __restrict__ b, __half* __restrict__ b16, int64_t nb16) {
+// Four int8 values (one 32-bit word) to four FP16 values, exactly.  With the
+// sign bit flipped, byte b holds u = x + 128 in [0, 255]; the FP16 bit pattern
+// 0x64 : u is 1024 + u (FP16 spacing is 1 on [1024, 2048)), so one byte
+// permute builds two such halves and subtracting 1152 = 1024 + 128 returns x
+// with no rounding.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x5140);   // bytes u0, 0x64, u1, 0x64
+  const uint32_t p23 = __byte_perm(u, 0x64646464u, 0x5342);   // bytes u2, 0x64, u3, 0x64
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+  __half2 h01 = __hsub2(*reinterpret_cast<const __half2*>(&p01), bias);
+  __half2 h23 = __hsub2(*reinterpret_cast<const __half2*>(&p23), bias);
+  lo = *reinterpret_cast<uint32_t*>(&h01);
+  hi = *reinterpret_cast<uint32_t*>(&h23);
+}
+
+__device__ __forceinline__ void i8x16_store_f16(const uint4 raw, uint4* dst) {
+  uint32_t h[8];
+  i8x4_to_f16x4(raw.x, h[0], h[1]);
+  i8x4_to_f16x4(raw.y, h[2], h[3]);
+  i8x4_to_f16x4(raw.z, h[4], h[5]);
+  i8x4_to_f16x4(raw.w, h[6], h[7]);
+  dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// A then B, 16 int8 values per step of a grid-stride loop that keeps two
+// 16-byte loads in flight per thread; the FP16 copies are written with normal
+// (L2-allocating) stores, since the GEMM reads them next.
+__global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ a, __half* __restrict__ a16,
+                                                        int64_t na16, const int8_t* __restrict__ b,
+                                                        __half* __restrict__ b16, int64_t nb16) {
   const int64_t total = na16 + nb16;   // 16-element groups
+  pdl_launch_dependents();   // the GEMM may start its set-up; it waits for this grid before reading
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const bool is_a = i < na16;
-    const int64_t j = is_a ? i : i - na16;
-    const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(is_a ? a : b) + j);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t h[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int8_t lo = static_cast<int8_t>((w[q >> 1] >> (16 * (q & 1))) & 0xff);
-      const int8_t hi = static_cast<int8_t>((w[q >> 1] >> (16 * (q & 1) + 8)) & 0xff);
-      __half2 v = __halves2half2(__short2half_rn(lo), __short2half_rn(hi));
-      h[q] = *reinterpret_cast<uint32_t*>(&v);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(is_a ? a16 : b16) + 2 * j;
-    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  auto src = [&](int64_t i) {
+    return i < na16 ? reinterpret_cast<const uint4*>(a) + i : reinterpret_cast<const uint4*>(b) + (i - na16);
+  };
+  auto dst = [&](int64_t i) {
+    return i < na16 ? reinterpret_cast<uint4*>(a16) + 2 * i : reinterpret_cast<uint4*>(b16) + 2 * (i - na16);
+  };
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + stride < total; i += 2 * stride) {
+    const uint4 r0 = __ldcs(src(i));
+    const uint4 r1 = __ldcs(src(i + stride));
+    i8x16_store_f16(r0, dst(i));
+    i8x16_store_f16(r1, dst(i + stride));
   }
+  if (i < total) i8x16_store_f16(__ldcs(src(i)), dst(i));
 }
 
 // Store one 32-row x 32-column INT32 chunk through a 4 KB swizzled staging
@@ -692,7 +753,8 @@ __device__ __forceinline__ bool i8_epi_bar_and(bool pred) {   // the 8 epilogue 
 template <bool PAIR>
 __global__ void __launch_bounds__(kI8Threads, 1)
     umma_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl) {
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl,
+                   SkParams sk) {
   constexpr int BN = 256;
   constexpr int HALF = BN / 2;   // columns per epilogue thread
   using Sh = RingShape<BN, PAIR>;
@@ -714,9 +776,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int m_blocks = (M + Sh::TILE_M - 1) / Sh::TILE_M;
   const int n_blocks = (N + BN - 1) / BN;
-  const int tiles = m_blocks * n_blocks;
   const int kt = (K + BK - 1) / BK;
-  const int chunks = (kt + kI8ChunkSteps - 1) / kI8ChunkSteps;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -749,21 +809,26 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   tc_fence_before();
   if (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();
+  pdl_wait();   // the FP16 copies are written by the conversion kernel launched just before
   const uint32_t tmem = bar->tmem_base;
   CtaCtl* cta = &bar->ctl;
   int issued = 0;
+  WorkIter it;
+  it.init(sk, kt, worker, workers);
+  int tile, k0, k1;
 
   if (warp == 0) {
     // ---------------- producer (every CTA) ----------------
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      for (int tile = worker; tile < tiles && !cta->abort; tile += workers) {
+      while (!cta->abort && it.next(tile, k0, k1)) {
         int mb, nb;
         tile_coords(tile, m_blocks, n_blocks, mb, nb);
         const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
         const int n_row = nb * BN + rank * Sh::B_ROWS;
-        for (int kb = 0; kb < kt; ++kb) {
+        for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto i8_producer_done;
           uint8_t* slot = ring + s * STAGE;
           if (PAIR) {
@@ -790,14 +855,14 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       int consumed = 0;
       int t = 0;
       bool ok = true;
-      for (int tile = worker; tile < tiles && ok; tile += workers) {
-        for (int c = 0; c < chunks && ok; ++c, ++t) {
+      while (ok && it.next(tile, k0, k1)) {
+        // chunks of at most kI8ChunkSteps K steps from k0: each FP32 sum stays exact
+        for (int kb0 = k0; kb0 < k1 && ok; kb0 += kI8ChunkSteps, ++t) {
           const int a = t & 1;
           if (!mbar_wait(&bar->acc_empty[a], ((t >> 1) & 1) ^ 1u, ctl, cta, kSiteMmaAccEmpty)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + a * BN;
-          const int kb0 = c * kI8ChunkSteps;
-          const int kb1 = min(kt, kb0 + kI8ChunkSteps);
+          const int kb1 = min(k1, kb0 + kI8ChunkSteps);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull)) { ok = false; break; }
             tc_fence_after();
@@ -828,17 +893,22 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   } else {
     // ---------------- epilogue: int32 running sum of the exact FP32 chunk sums ----------------
     const int q = warp & 3;
-    const int h = (warp - 2) >> 2;     // column half of the accumulator
-    uint8_t* my_stage = epi + (warp - 2) * kUmmaEpiBufBytes;
+    const int e = warp - 2;
+    const int h = e >> 2;              // column half of the accumulator
+    const int row = q * 32 + lane;     // accumulator row of this CTA that this thread holds
+    uint8_t* my_stage = epi + e * kUmmaEpiBufBytes;
     int t = 0;
     bool ok = true;
-    for (int tile = worker; tile < tiles && ok; tile += workers) {
+    while (ok && it.next(tile, k0, k1)) {
       int mb, nb;
       tile_coords(tile, m_blocks, n_blocks, mb, nb);
+      // A split tile (stream-K): each segment's int32 partial is exact, so the
+      // order in which the segments are added does not change the result.
+      const bool split = (k0 > 0) || (k1 < kt);
       uint32_t sum[HALF];
 #pragma unroll
       for (int i = 0; i < HALF; ++i) sum[i] = 0u;
-      for (int c = 0; c < chunks; ++c, ++t) {
+      for (int kb0 = k0; kb0 < k1; kb0 += kI8ChunkSteps, ++t) {
         const int a = t & 1;
         uint32_t w = 1;
         if (lane == 0) w = mbar_wait(&bar->acc_full[a], (t >> 1) & 1, ctl, cta, kSiteEpilogueAccFull) ? 1u : 0u;
@@ -847,13 +917,14 @@ __global__ void __launch_bounds__(kI8Threads, 1)
         tc_fence_after();
         const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN + h * HALF;
 #pragma unroll
-        for (int sub = 0; sub < HALF / 32; ++sub) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(trow + sub * 32, v);
+        for (int sub = 0; sub < HALF / 16; ++sub) {   // 16 columns at a time: sum[] holds 128 registers
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(trow + sub * 16, v);
           tmem_wait_ld();
+          regs_after_wait(v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)   // exact integers of magnitude <= 2^24 in FP32
-            sum[sub * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+          for (int i = 0; i < 16; ++i)   // exact integers of magnitude <= 2^24 in FP32
+            sum[sub * 16 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
         }
         tc_fence_before();
         __syncwarp();
@@ -865,6 +936,51 @@ __global__ void __launch_bounds__(kI8Threads, 1)
         }
       }
       if (!ok) break;
+      if (split) {
+        SplitTile sp;
+        sp.init(tile, kt, sk, workers, Sh::CTAS, rank);
+        // first-K-step owner: take the fast path if every other segment is in
+        if (e == 0 && lane == 0) {
+          bar->sk_last = (worker == sp.w_first && sp.poll_others(sk.epoch)) ? 2 : 0;
+          __threadfence();
+        }
+        i8_epi_bar_and(true);
+        const bool fast = bar->sk_last == 2;
+        if (!fast) {
+          // store this segment's partial, count it in; the last one adds them all
+          uint4* dst = reinterpret_cast<uint4*>(sk.workspace);
+          const int my = sp.slot(worker, Sh::CTAS, rank);
+#pragma unroll
+          for (int i = 0; i < HALF / 4; ++i)
+            __stcg(dst + partial_at<BN>(my, 2 * h + i / 16, i % 16, row),
+                   make_uint4(sum[4 * i], sum[4 * i + 1], sum[4 * i + 2], sum[4 * i + 3]));
+          __threadfence();
+          i8_epi_bar_and(true);
+          if (e == 0 && lane == 0) {
+            bar->sk_last = sp.count_in(sk.epoch) ? 1 : 0;
+            __threadfence();
+          }
+          i8_epi_bar_and(true);
+          if (!bar->sk_last) continue;
+#pragma unroll
+          for (int i = 0; i < HALF; ++i) sum[i] = 0u;
+        }
+        // add the other segments' partials (every segment, when counted in: its own included)
+        for (int w2 = sp.w_first; w2 <= sp.w_last; ++w2) {
+          if (!sp.has_segment(w2) || (fast && w2 == worker)) continue;
+          const uint4* src = reinterpret_cast<const uint4*>(sk.workspace);
+          const int sl = sp.slot(w2, Sh::CTAS, rank);
+#pragma unroll
+          for (int i = 0; i < HALF / 4; ++i) {
+            const uint4 p = __ldcg(src + partial_at<BN>(sl, 2 * h + i / 16, i % 16, row));
+            sum[4 * i] += p.x;
+            sum[4 * i + 1] += p.y;
+            sum[4 * i + 2] += p.z;
+            sum[4 * i + 3] += p.w;
+            if (i % 8 == 7) asm volatile("" ::: "memory");   // at most 8 loads in flight: sum[] keeps its registers
+          }
+        }
+      }
       const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
 #pragma unroll
       for (int sub = 0; sub < HALF / 32; ++sub) {
@@ -1117,6 +1233,9 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
     attr[n].val.clusterDim.z = 1;
     ++n;
   }
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait() in the kernel
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl, a.sk);
@@ -1173,14 +1292,16 @@ cudaError_t launch_i8(LaunchArgs& a, const void** kernel) {
   cfg.blockDim = dim3(p.threads);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlaps the conversion's tail
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl, a.sk);
 }
 
 // Largest number of CTA pairs of a pair kernel that can be resident at once.

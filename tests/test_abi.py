@@ -143,7 +143,9 @@ def test_int8_on_tcgen05_plan(gp, S):
     assert (p["bm"], p["bn"], p["bk"], p["stages"]) == (256, 256, 64, S)
     assert p["stage_bytes"] == (128 + 128) * 64 * 2 and p["tmem_cols"] == 512 and p["threads"] == 320
     assert p["smem_bytes"] <= 232448 and p["k_tiles"] == 64 and p["tiles"] == 16 * 16
-    assert p["workspace_bytes"] == (4096 + 4096) * 4096 * 2
+    # FP16 copies of A and B, after the stream-K partial tiles (two 128 x 256 int32 slots per CTA) if any
+    partials = p["grid"] * 2 * 128 * 256 * 4 if p["sk_tiles"] > 0 else 0
+    assert p["workspace_bytes"] == (4096 + 4096) * 4096 * 2 + partials
     # bn=64 or an IMMA request selects the warp-level IMMA ring
     assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", bn=64)["kernel"] == "imma_ring"
     for deep in (7, 8):   # rings deeper than the pair tile allows run on IMMA

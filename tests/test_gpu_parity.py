@@ -268,11 +268,37 @@ def test_int8_tcgen05_exact_at_extremes(K, fill):
     check_full("i8", "row_col", A, B, C, K)
 
 
+@pytest.mark.parametrize("M,N,K,S", [(1024, 1024, 4096, 4), (1280, 1536, 3136, 6), (1000, 776, 2064, 3),
+                                     (768, 2048, 8192, 2)])
+def test_int8_tcgen05_stream_k_exact(M, N, K, S):
+    # tiles whose K-loops are split across CTA pairs: int32 partials, so the
+    # result is bit-identical to whole-tile scheduling
+    A, B = operands("i8", "row_col", M, N, K, seed=M + N + K)
+    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined", stages=S)
+    p = st["plan"]
+    assert p["kernel"] == "umma_i8_pair_ring" and p["sk_tiles"] > 0
+    assert p["dp_tiles"] + p["sk_tiles"] == p["tiles"]
+    check_full("i8", "row_col", A, B, C, K)
+    C2, st2 = run("i8", "row_col", A, B, M, N, K, variant="pipelined", stages=S, no_stream_k=True)
+    assert st2["plan"]["sk_tiles"] == 0
+    assert torch.equal(C, C2)
+
+
+def test_int8_tcgen05_stream_k_repeated_launches():
+    # per-launch epochs on the tile counters: back-to-back launches stay exact
+    A, B = operands("i8", "row_col", 1024, 1024, 4096, seed=11)
+    outs = [run("i8", "row_col", A, B, 1024, 1024, 4096, stages=6)[0] for _ in range(3)]
+    check_full("i8", "row_col", A, B, outs[0], 4096)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
 def test_int8_tcgen05_sum_wraps_like_int32():
     # 16384 * 131088 exceeds 2^31 - 1: the INT32 result wraps modulo 2^32
     M, N, K = 128, 128, 131088
     A = np.full((M, K), -128, np.int8)
     B = np.full((N, K), -128, np.int8)
     C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined")
+    assert st["plan"]["sk_tiles"] == 1      # the one tile's K-loop is split over every CTA pair
     want = (16384 * K + (1 << 31)) % (1 << 32) - (1 << 31)
     assert int(C[0, 0]) == want and bool((C == want).all())
