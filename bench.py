@@ -217,7 +217,41 @@ def roofline_row(w, kernel, ms, peaks, imma_peak):
     return bound, round(max(t_compute, t_hbm) / (ms * 1e-3), 4)
 
 
-def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak):
+def rw_roof_us(w, rw):
+    """Least time to move A + B in and C out given the measured copy, pure-read and pure-write
+    bandwidths (GB/s): a stream of writes alone runs well below the copy rate on HBM."""
+    return max(w.algorithmic_bytes / rw["copy_gbs"], w.read_bytes / rw["read_gbs"],
+               w.write_bytes / rw["write_gbs"]) / 1e3
+
+
+def hbm_probe(torch, dev, nbytes=1 << 30, reps=10):
+    """Pure-write (fill), pure-read (sum) and copy bandwidth of this GPU, best of reps, CUDA events."""
+    x = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    y = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    x.fill_(1)
+    xf = x.view(torch.float32)
+
+    def best(fn):
+        ts = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return min(ts)
+    out = {"write_gbs": round(nbytes / best(lambda: x.fill_(3)) / 1e6, 1),
+           "read_gbs": round(nbytes / best(lambda: xf.sum()) / 1e6, 1),
+           "copy_gbs": round(2 * nbytes / best(lambda: y.copy_(x)) / 1e6, 1),
+           "how": "torch fill_ / sum / copy_ over 1 GiB, best of %d" % reps}
+    del x, y, xf
+    torch.cuda.empty_cache()
+    return out
+
+
+def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
     from software_pipelined_tiled_pipeline_gb300 import synth
     from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
     out = {}
@@ -243,6 +277,8 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak):
                          "sk_tiles": p["sk_tiles"], "ms": round(avg, 4), unit: round(w.ops / (avg * 1e-3) / 1e12, 2),
                          "regs": st["regs_per_thread"], "smem": p["smem_bytes"]})
             rows[-1]["bound"], rows[-1]["roofline_frac"] = roofline_row(w, p["kernel"], avg, peaks, imma_peak)
+            if rw and rows[-1]["bound"] == "hbm":
+                rows[-1]["rw_roof_frac"] = round(rw_roof_us(w, rw) / (avg * 1e3), 4)
         base = next(r for r in rows if r["variant"] == "pingpong")[unit]
         for r in rows:
             r["vs_pingpong"] = round(r[unit] / base, 3) if base else None
@@ -487,9 +523,11 @@ def main():
     if bound == "hbm":
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         gbs = w.algorithmic_bytes / (kavg * 1e-3) / 1e9
+        rw = hbm_probe(torch, dev)
         roofline.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "algorithmic_bytes": w.algorithmic_bytes,
-                         "peak_source": peaks["_source"] + ": STREAM-style copy"})
+                         "peak_source": peaks["_source"] + ": STREAM-style copy",
+                         "rw_probe": rw, "rw_roof_frac": round(rw_roof_us(w, rw) / (kavg * 1e3), 4)})
     else:
         peak = compute_peak(plan["kernel"], peaks, imma_peak)
         roofline.update({"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
@@ -532,7 +570,10 @@ def main():
         del bufs
         torch.cuda.empty_cache()
         imma_peak = gp.probe_peak("imma_s8", stream) / 1e12
-        sw = sweep(torch, gp, dev, stream, names, extra_steps, peaks, imma_peak)
+        rw = hbm_probe(torch, dev) if args.sweep_bf16 else None
+        sw = sweep(torch, gp, dev, stream, names, extra_steps, peaks, imma_peak, rw)
+        if rw:
+            line["hbm_probe"] = rw
         line["sweep"] = sw
         i8 = sw.get("i8_4096")
         if i8:

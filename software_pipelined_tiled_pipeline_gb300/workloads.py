@@ -29,6 +29,16 @@ class Workload:
         return 2 * self.M * self.N * self.K
 
     @property
+    def read_bytes(self) -> int:
+        """A and B, read once."""
+        return (self.M + self.N) * self.K * {"i8": 1, "f16": 2, "bf16": 2, "f32": 4}[self.dtype]
+
+    @property
+    def write_bytes(self) -> int:
+        """C, written once."""
+        return self.M * self.N * {"i8": 4, "f16": 2, "bf16": 2, "f32": 4}[self.dtype]
+
+    @property
     def algorithmic_bytes(self) -> int:
         """A and B read once, C written once: the least DRAM traffic of one GEMM."""
         size_in = {"i8": 1, "f16": 2, "bf16": 2, "f32": 4}[self.dtype]

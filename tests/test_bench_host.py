@@ -43,6 +43,15 @@ def test_roofline_bound(name, kernel, bound):
     assert bench.roofline_row(w, kernel, t_roof * 1e3, PEAKS, 158.4)[1] == pytest.approx(1.0, abs=1e-4)
 
 
+def test_read_write_roof_takes_the_slowest_stream():
+    rw = {"copy_gbs": 6800.0, "read_gbs": 6300.0, "write_gbs": 4000.0}
+    w = WORKLOADS["bf16_8192_k256"]          # 8 MB read, 134 MB written: the write stream bounds it
+    assert bench.rw_roof_us(w, rw) == pytest.approx(w.write_bytes / 4000.0 / 1e3)
+    w = WORKLOADS["bf16_skinny"]             # 138 MB read, 2 MB written: the read stream bounds it
+    assert bench.rw_roof_us(w, rw) == pytest.approx(w.read_bytes / 6300.0 / 1e3)
+    assert w.read_bytes + w.write_bytes == w.algorithmic_bytes
+
+
 def test_imma_rows_use_the_imma_ceiling():
     w = WORKLOADS["i8_4096"]
     _, frac = bench.roofline_row(w, "imma_ring", w.ops / 158.4e12 * 1e3 * 2, PEAKS, 158.4)
