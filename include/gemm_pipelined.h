@@ -110,10 +110,13 @@ typedef struct gp_plan {
     const char* kernel;          /* kernel family name, static string */
     int32_t dp_tiles;            /* persistent kernels: tiles computed whole by one CTA (raster order first) */
     int32_t sk_tiles;            /* tiles after those whose K-loops are split evenly over all CTAs (stream-K) */
-    int64_t workspace_bytes;     /* FP32 partial-tile workspace the split tiles use (per device and stream) */
+    int64_t workspace_bytes;     /* device workspace of the call (per device and stream, kept between calls):
+                                    partial tiles of split K-loops; for INT8 on tcgen05 also the FP16 copies */
     int32_t cta_pair;            /* 1: two CTAs (a cluster on one TPC) share each BM x BN tile, each holding
                                     BM/2 rows of A and BN/2 rows of B; stage_bytes and smem_bytes are per CTA */
-    int32_t reserved0;
+    int32_t k_splits;            /* FP32 FFMA path: CTAs that share each tile's K-loop, when the tiles alone
+                                    leave SMs idle (each writes a partial tile; the last to finish adds them in
+                                    split order, so results do not depend on timing); 1 = whole K-loops */
 } gp_plan;
 
 /* Record of the last gemm_pipelined call made by the calling host thread. */

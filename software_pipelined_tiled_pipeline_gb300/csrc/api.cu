@@ -260,6 +260,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   }
 
   std::memset(p, 0, sizeof(*p));
+  p->k_splits = 1;
   p->dtype = dtype;
   p->layout = layout;
   p->variant = variant;
@@ -394,6 +395,19 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->dp_tiles = static_cast<int32_t>(p->tiles);
   p->sk_tiles = 0;
   p->workspace_bytes = 0;
+  if (fam == 0 && sm_count > 0 && p->tiles < sm_count) {
+    // FFMA: fewer tiles than SMs -- share each tile's K-loop among up to
+    // kFfmaMaxSplits CTAs of at least kFfmaMinSplitSteps K steps each
+    constexpr int64_t kFfmaMaxSplits = 4, kFfmaMinSplitSteps = 16;
+    int64_t splits = sm_count / p->tiles;
+    if (splits > kFfmaMaxSplits) splits = kFfmaMaxSplits;
+    if (splits > p->k_tiles / kFfmaMinSplitSteps) splits = p->k_tiles / kFfmaMinSplitSteps;
+    if (splits >= 2) {
+      p->k_splits = static_cast<int32_t>(splits);
+      p->grid = static_cast<int32_t>(p->tiles * splits);
+      p->workspace_bytes = p->tiles * splits * p->bm * p->bn * 4;   // one FP32 partial tile per CTA
+    }
+  }
   if (fam == 2 && ring && sm_count > 0) {
     if (p->cta_pair)
       apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
@@ -483,8 +497,13 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (done.count({dev, kernel})) return cudaSuccess;
   }
-  if (bytes > kSmemPerCtaMax) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCtaMax);
+  // the opt-in limit covers static and dynamic shared memory together
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  const int max_dynamic = kSmemPerCtaMax - static_cast<int>(fa.sharedSizeBytes);
+  if (bytes > max_dynamic) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
   done.insert({dev, kernel});
@@ -681,6 +700,14 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
                         &sk.flags, &sk.epoch);
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
     }
+    FfmaSplit ks{plan.k_splits, nullptr, nullptr, 0};
+    if (plan.k_splits > 1) {
+      uint32_t* counters = nullptr;
+      e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), static_cast<size_t>(plan.tiles) * 2,
+                        &ks.workspace, &counters, &ks.epoch);
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      ks.counters = reinterpret_cast<unsigned long long*>(counters);
+    }
     LaunchArgs a;
     a.A = A;
     a.B = B;
@@ -698,6 +725,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.ctl.inject_lost_load = opts ? opts->inject_lost_load : 0;
     a.sm_count = sms;
     a.sk = sk;
+    a.ks = ks;
     a.conv = conv;
     const void* kernel = nullptr;
     switch (family_of(dtype)) {
@@ -842,6 +870,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.ctl.inject_lost_load = 0;
     a.sm_count = sms;
     a.sk = sk;
+    a.ks = FfmaSplit{1, nullptr, nullptr, 0};
     a.conv = nullptr;
     const void* kernel = nullptr;
     e = launch_umma(a, &kernel);

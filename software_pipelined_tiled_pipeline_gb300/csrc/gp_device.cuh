@@ -73,6 +73,23 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // programmatic attribute).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// per-launch counters of split tiles
+// ---------------------------------------------------------------------------
+// A 64-bit counter {epoch, count}: a value from an earlier launch (another
+// epoch) reads as 0, so the counters never need resetting between launches.
+// Adds one and returns the count before this call.
+__device__ __forceinline__ uint32_t epoch_count_in(unsigned long long* ctr, uint32_t epoch) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (;;) {
+    const uint32_t count = (static_cast<uint32_t>(old >> 32) == epoch) ? static_cast<uint32_t>(old) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (count + 1u);
+    const unsigned long long seen = atomicCAS(ctr, old, want);
+    if (seen == old) return count;
+    old = seen;
+  }
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(

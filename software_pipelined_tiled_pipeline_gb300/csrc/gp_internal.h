@@ -49,6 +49,18 @@ struct SkParams {
   uint32_t epoch;           // tag of this launch's counts
 };
 
+// FP32 FFMA path, K-loop split over k_splits CTAs per tile (plan.k_splits):
+// CTA b computes tile b % tiles over the K steps of split b / tiles.  With
+// more than one split each CTA stores its 128 x 128 FP32 partial in slot
+// tile * splits + split and counts itself on the tile's {epoch, count}
+// counter; the last one adds the partials in split order and writes C.
+struct FfmaSplit {
+  int32_t splits;
+  float* workspace;
+  unsigned long long* counters;
+  uint32_t epoch;
+};
+
 // ---------------------------------------------------------------------------
 // shared-memory budget
 // ---------------------------------------------------------------------------
@@ -93,6 +105,7 @@ struct LaunchArgs {
   cudaStream_t stream;
   KernelCtl ctl;
   SkParams sk;
+  FfmaSplit ks;
   void* conv;               // INT8 on tcgen05: FP16 copies of A then B, (M + N) * K halves
   int32_t sm_count;
 };

@@ -5,6 +5,9 @@
 // Occupancy", section 4.3, register tiling).  A is row-major M x K, B
 // row-major K x N, C row-major M x N.
 //
+// When the tiles alone would leave SMs idle, each tile's K-loop is split over
+// plan.k_splits CTAs (see FfmaSplit); every data path splits it the same way.
+//
 // Three data paths for the K-loop, sharing the shared-memory layout (A tile
 // [128][8], B tile [8][128], as a TMA box copy lays them out) and the compute:
 //  * ffma_ring_kernel    -- a TMA producer warp fills an S-slot ring guarded by
@@ -27,6 +30,7 @@ struct FfmaBarriers {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   int32_t consumed;
+  int32_t last;     // split K-loop: this CTA completed the tile
   CtaCtl ctl;
 };
 static_assert(sizeof(FfmaBarriers) <= kBarrierRegion, "barrier region too small");
@@ -97,21 +101,98 @@ __device__ __forceinline__ void ffma_store(float* C, int M, int N, int m0, int n
   }
 }
 
+// Barrier of the 256 compute threads (the ring kernel's producer warp is not in it).
+__device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Same barrier, returning the AND of pred over the 256 compute threads.
+__device__ __forceinline__ bool compute_bar_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// Work of CTA b: tile b % tiles, K steps [kb_begin, kb_end) of split b / tiles.
+struct FfmaWork {
+  int tile, split, kb_begin, kb_end;
+  __device__ __forceinline__ FfmaWork(int tiles, int kt, int splits) {
+    tile = static_cast<int>(blockIdx.x) % tiles;
+    split = static_cast<int>(blockIdx.x) / tiles;
+    kb_begin = static_cast<int>(static_cast<int64_t>(kt) * split / splits);
+    kb_end = static_cast<int>(static_cast<int64_t>(kt) * (split + 1) / splits);
+  }
+};
+
+// Write the accumulator: to C, or -- K-loop split over several CTAs -- as a
+// partial tile; the CTA whose partial completes the tile adds all of them in
+// split order (so the sum does not depend on which CTA finished last) and
+// writes C.  Called by all 256 compute threads (tid 0..255).
+__device__ __forceinline__ void ffma_finish(float* C, int M, int N, int m0, int n0, const FfmaWork& w,
+                                            const FfmaSplit& ks, int tx, int ty, int tid, const Acc& acc,
+                                            int32_t* last) {
+  if (ks.splits <= 1) {
+    ffma_store(C, M, N, m0, n0, tx, ty, acc);
+    return;
+  }
+  constexpr int TILE = BM * BN;
+  float* base = ks.workspace + static_cast<size_t>(w.tile) * ks.splits * TILE;
+  float* mine = base + static_cast<size_t>(w.split) * TILE;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      __stcg(reinterpret_cast<float4*>(mine + (ty + 16 * i) * BN + h * 64 + tx * 4),
+             make_float4(acc.c[i][4 * h], acc.c[i][4 * h + 1], acc.c[i][4 * h + 2], acc.c[i][4 * h + 3]));
+  compute_bar();
+  if (tid == 0) {
+    __threadfence();
+    *last = (epoch_count_in(ks.counters + w.tile, ks.epoch) + 1u == static_cast<uint32_t>(ks.splits)) ? 1 : 0;
+    __threadfence();
+  }
+  compute_bar();
+  if (!*last) return;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = ty + 16 * i;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int off = r * BN + h * 64 + tx * 4;
+      float4 sum = __ldcg(reinterpret_cast<const float4*>(base + off));
+      for (int j = 1; j < ks.splits; ++j) {
+        const float4 p = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(j) * TILE + off));
+        sum.x += p.x;
+        sum.y += p.y;
+        sum.z += p.z;
+        sum.w += p.w;
+      }
+      const int gr = m0 + r, gc = n0 + h * 64 + tx * 4;
+      if (gr < M && gc < N) *reinterpret_cast<float4*>(C + static_cast<size_t>(gr) * N + gc) = sum;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
-// TMA ring: 8 compute warps + 1 producer warp, one tile per CTA
+// TMA ring: 8 compute warps + 1 producer warp, one (tile, K split) per CTA
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
     ffma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     float* __restrict__ C, int M, int N, int K, int stages, KernelCtl ctl) {
+                     float* __restrict__ C, int M, int N, int K, int stages, KernelCtl ctl, FfmaSplit ks) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align1024(smem_raw);
   FfmaBarriers* bar = reinterpret_cast<FfmaBarriers*>(ring + stages * STAGE);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
-  int mb, nb;
-  tile_coords(blockIdx.x, m_blocks, n_blocks, mb, nb);
   const int kt = (K + BK - 1) / BK;
+  const FfmaWork wk(m_blocks * n_blocks, kt, ks.splits > 1 ? ks.splits : 1);
+  int mb, nb;
+  tile_coords(wk.tile, m_blocks, n_blocks, mb, nb);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -133,9 +214,9 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
       int s = 0;
       uint32_t ph = 0;
       const bool last_tile = blockIdx.x == gridDim.x - 1;
-      for (int kb = 0; kb < kt; ++kb) {
+      for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
         if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) break;
-        if (!(ctl.inject_lost_load && last_tile && kb == kt - 1)) {
+        if (!(ctl.inject_lost_load && last_tile && kb == wk.kb_end - 1)) {
           uint8_t* slot = ring + s * STAGE;
           mbar_arrive_expect_tx(&bar->full[s], STAGE);
           tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, mb * BM);
@@ -153,7 +234,7 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
     uint32_t ph = 0;
     bool ok = true;
     int consumed = 0;
-    for (int kb = 0; kb < kt; ++kb) {
+    for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
       const bool w = mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       const float* As = reinterpret_cast<const float*>(ring + s * STAGE);
@@ -163,7 +244,8 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
       ++consumed;
       if (++s == stages) { s = 0; ph ^= 1u; }
     }
-    if (ok) ffma_store(C, M, N, mb * BM, nb * BN, tx, ty, acc);
+    // one decision for all compute warps: a timed-out warp must not leave the others at a barrier
+    if (compute_bar_and(ok)) ffma_finish(C, M, N, mb * BM, nb * BN, wk, ks, tx, ty, threadIdx.x, acc, &bar->last);
     if (threadIdx.x == 0) bar->consumed = consumed;
   }
 
@@ -204,33 +286,37 @@ struct RegStage {
 template <bool PINGPONG>
 __global__ void __launch_bounds__(kComputeThreads, 1)
     ffma_staged_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C, int M, int N,
-                       int K) {
+                       int K, FfmaSplit ks) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int32_t last;
   uint8_t* ring = align1024(smem_raw);
   const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
-  int mb, nb;
-  tile_coords(blockIdx.x, m_blocks, n_blocks, mb, nb);
-  const int m0 = mb * BM, n0 = nb * BN;
   const int kt = (K + BK - 1) / BK;
+  const FfmaWork wk(m_blocks * n_blocks, kt, ks.splits > 1 ? ks.splits : 1);
+  int mb, nb;
+  tile_coords(wk.tile, m_blocks, n_blocks, mb, nb);
+  const int m0 = mb * BM, n0 = nb * BN;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
 
   Acc acc;
   acc.zero();
   RegStage rs;
   if (PINGPONG) {
-    rs.load(A, B, M, N, K, m0, n0, 0);
-    rs.store(ring);
+    if (wk.kb_begin < wk.kb_end) {
+      rs.load(A, B, M, N, K, m0, n0, wk.kb_begin);
+      rs.store(ring);
+    }
     __syncthreads();
-    for (int kb = 0; kb < kt; ++kb) {
-      const int cur = kb & 1;
-      if (kb + 1 < kt) rs.load(A, B, M, N, K, m0, n0, kb + 1);   // in flight during the compute
+    for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
+      const int cur = (kb - wk.kb_begin) & 1;
+      if (kb + 1 < wk.kb_end) rs.load(A, B, M, N, K, m0, n0, kb + 1);   // in flight during the compute
       const float* As = reinterpret_cast<const float*>(ring + cur * STAGE);
       ffma_kblock(As, As + A_FLOATS, tx, ty, acc);
-      if (kb + 1 < kt) rs.store(ring + (cur ^ 1) * STAGE);   // last read in iteration kb-1
+      if (kb + 1 < wk.kb_end) rs.store(ring + (cur ^ 1) * STAGE);   // last read in iteration kb-1
       __syncthreads();
     }
   } else {
-    for (int kb = 0; kb < kt; ++kb) {
+    for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
       rs.load(A, B, M, N, K, m0, n0, kb);
       rs.store(ring);
       __syncthreads();
@@ -239,7 +325,7 @@ __global__ void __launch_bounds__(kComputeThreads, 1)
       __syncthreads();
     }
   }
-  ffma_store(C, M, N, m0, n0, tx, ty, acc);
+  ffma_finish(C, M, N, m0, n0, wk, ks, tx, ty, threadIdx.x, acc, &last);
 }
 
 }  // namespace
@@ -259,13 +345,13 @@ cudaError_t launch_ffma(LaunchArgs& a, const void** kernel) {
     *kernel = reinterpret_cast<const void*>(ffma_ring_kernel);
     if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
     ffma_ring_kernel<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(tmA, tmB, static_cast<float*>(a.C), a.M, a.N,
-                                                                     a.K, p.stages, a.ctl);
+                                                                     a.K, p.stages, a.ctl, a.ks);
   } else {
     auto k = (a.variant == GP_PINGPONG) ? ffma_staged_kernel<true> : ffma_staged_kernel<false>;
     *kernel = reinterpret_cast<const void*>(k);
     if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
     k<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(static_cast<const float*>(a.A), static_cast<const float*>(a.B),
-                                                      static_cast<float*>(a.C), a.M, a.N, a.K);
+                                                      static_cast<float*>(a.C), a.M, a.N, a.K, a.ks);
   }
   return cudaGetLastError();
 }

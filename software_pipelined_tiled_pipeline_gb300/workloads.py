@@ -50,7 +50,7 @@ WORKLOADS = {
     w.name: w for w in [
         Workload("i8_256", "i8", "row_col", 256, 256, 256, (2, 3, 4), ("pipelined", "pingpong", "nopipe"),
                  "INT8 GEMM M=N=K=256, A row-major, B column-major, uniform int8, INT32 out"),
-        Workload("f32_1024", "f32", "row_row", 1024, 1024, 1024, (2,), ("pipelined", "pingpong", "nopipe"),
+        Workload("f32_1024", "f32", "row_row", 1024, 1024, 1024, (2, 3, 4), ("pipelined", "pingpong", "nopipe"),
                  "FP32 SGEMM M=N=K=1024 on the FFMA path, row-major, U[-1,1]"),
         Workload("i8_4096", "i8", "row_col", 4096, 4096, 4096, (2, 3, 4, 6), ("pipelined", "pingpong", "nopipe"),
                  "INT8 IGEMM M=N=K=4096, A row-major, B column-major, uniform int8, INT32 out"),

@@ -268,6 +268,43 @@ def test_int8_tcgen05_exact_at_extremes(K, fill):
     check_full("i8", "row_col", A, B, C, K)
 
 
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (500, 372, 1000), (256, 128, 4104), (130, 260, 2052)])
+def test_ffma_split_k_every_variant(M, N, K):
+    # fewer 128 x 128 tiles than SMs: each tile's K-loop is shared by k_splits
+    # CTAs whose partials are added in split order, the same in every variant
+    A, B = operands("f32", "row_row", M, N, K, seed=M + 3 * N + K)
+    C, st = run("f32", "row_row", A, B, M, N, K, variant="pipelined", stages=3)
+    p = st["plan"]
+    assert p["k_splits"] >= 2 and p["grid"] == p["tiles"] * p["k_splits"]
+    check_full("f32", "row_row", A, B, C, K)
+    for variant, S in (("pipelined", 2), ("pipelined", 8), ("pingpong", 0), ("nopipe", 0)):
+        C2, st2 = run("f32", "row_row", A, B, M, N, K, variant=variant, stages=S)
+        assert st2["plan"]["k_splits"] == p["k_splits"]
+        assert torch.equal(C2, C), (variant, S)
+
+
+def test_ffma_short_k_is_not_split():
+    A, B = operands("f32", "row_row", 128, 128, 40, seed=5)
+    C, st = run("f32", "row_row", A, B, 128, 128, 40, variant="pipelined", stages=3)
+    assert st["plan"]["k_splits"] == 1
+    check_full("f32", "row_row", A, B, C, 40)
+
+
+def test_ffma_split_k_lost_load_reports_timeout():
+    M, N, K = 512, 512, 2048
+    A, B = operands("f32", "row_row", M, N, K, seed=6)
+    tA, tB = to_dev(A, "f32"), to_dev(B, "f32")
+    tC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    gp.gemm_pipelined(tA, tB, tC, M, N, K, "f32", "row_row", 3, "pipelined", torch.cuda.current_stream(),
+                      timeout_ns=20_000_000, inject_lost_load=True)
+    st = gp.gemm_stats(sync=True)
+    assert st["plan"]["k_splits"] > 1
+    assert st["status"] == gp.GP_ERR_TIMEOUT
+    C, st2 = run("f32", "row_row", A, B, M, N, K)
+    assert st2["device_status"] == 0
+    check_full("f32", "row_row", A, B, C, K)
+
+
 @pytest.mark.parametrize("M,N,K,S", [(1024, 1024, 4096, 4), (1280, 1536, 3136, 6), (1000, 776, 2064, 3),
                                      (768, 2048, 8192, 2)])
 def test_int8_tcgen05_stream_k_exact(M, N, K, S):
