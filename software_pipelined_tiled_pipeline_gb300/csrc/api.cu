@@ -206,6 +206,9 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // INT8 on tcgen05: bytes of the FP16 copies of A and B.
 int64_t i8_conv_bytes(int64_t M, int64_t N, int64_t K) { return (M + N) * K * 2; }
 
+// FP16/BF16 GEMMs with K up to this many elements run one CTA per tile, not CTA pairs.
+constexpr int64_t kShortK = 256;
+
 int default_stages(int family) { return family == 0 ? 3 : (family == 1 ? 4 : 6); }
 
 // Persistent FP16/BF16 ring: when the output tiles do not fill whole waves of
@@ -257,6 +260,10 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   } else {
     if (stages < 0 || stages > kMaxStages) return GP_ERR_ARG;
     S = stages == 0 ? default_stages(fam) : stages;
+    // FP16/BF16 with only a few K steps (K <= kShortK): one CTA per 128 x 256
+    // tile beats the CTA pair (measured at 8192 x 8192 x 256, where C's write
+    // dominates); its widest tile fits 4 stages.
+    if (stages == 0 && family_of(dtype) == 2 && K <= kShortK && N > 128) S = 4;
   }
 
   std::memset(p, 0, sizeof(*p));
@@ -336,7 +343,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   };
   auto fits = [&](int bn) { return ring_smem_total(S * stage_bytes(bn), extra) <= kSmemPerCtaMax; };
 
-  const bool pair_ok = fam == 2 && ring && !no_pair && (bn_req == 0 || bn_req == 256) && N > 128 &&
+  const bool pair_ok = fam == 2 && ring && !no_pair && (bn_req == 0 || bn_req == 256) && N > 128 && K > kShortK &&
                        ring_smem_total(S * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax;
   int bn = 0;
   if (pair_ok) {

@@ -107,6 +107,17 @@ def test_umma_pairs_up_to_six_stages(gp, S):
     assert p["compute_load_ratio"] == pytest.approx(128.0)
 
 
+def test_short_k_runs_one_cta_per_tile(gp):
+    # K <= 256: a few K steps per tile, C's write dominates -- one CTA per 128 x 256 tile at 4 stages
+    for K in (64, 200, 256):
+        p = gp.gemm_plan(8192, 8192, K, "bf16", "row_col", 0, "pipelined")
+        assert (p["cta_pair"], p["bn"], p["stages"]) == (0, 256, 4), K
+    p = gp.gemm_plan(8192, 8192, 320, "bf16", "row_col", 0, "pipelined")
+    assert (p["cta_pair"], p["stages"]) == (1, 6)
+    assert gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 6, "pipelined")["cta_pair"] == 0
+    assert gp.gemm_plan(8192, 128, 256, "bf16", "row_col", 0, "pipelined")["stages"] == 6   # N <= 128: BN 128
+
+
 @pytest.mark.parametrize("S", range(1, 9))
 def test_umma_single_cta_widths_follow_the_budget(gp, S):
     # one CTA per 128 x BN tile: the widths the 227 KB budget admits at this depth

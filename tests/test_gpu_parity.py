@@ -222,8 +222,8 @@ def test_stream_k_lost_load_reports_timeout():
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("M,N,K,S", [(256, 256, 64, 1), (200, 264, 136, 2), (384, 520, 1000, 3), (1000, 776, 2056, 4),
-                                     (128, 256, 512, 5), (2304, 2560, 640, 6), (4096, 2048, 192, 4)])
+@pytest.mark.parametrize("M,N,K,S", [(256, 256, 320, 1), (200, 264, 264, 2), (384, 520, 1000, 3), (1000, 776, 2056, 4),
+                                     (128, 256, 512, 5), (2304, 2560, 640, 6), (4096, 2048, 328, 4)])
 def test_cta_pair_kernel(dtype, M, N, K, S):
     # 256 x 256 tile per CTA pair (each CTA 128 rows of A and of B), ragged in M, N, K
     lay = "row_col"
