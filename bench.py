@@ -10,7 +10,7 @@ line (rank 0).  The INT8 4096^3 result, the stage sweep and the FP32
 ping-pong-vs-async comparison ride along as sub-objects.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--stages S] [--no-sweep] [--sweep-bf16]
+                  [--workload NAME] [--stages S] [--no-sweep] [--no-sweep-bf16]
 
 --impl reference times the CPU oracle (the reference arm of this build) on a
 bounded row sample of the same workload on the host cores.
@@ -44,7 +44,9 @@ def parse():
     ap.add_argument("--stages", type=int, default=0, help="ring depth (0 = the library's default)")
     ap.add_argument("--variant", default="pipelined")
     ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--sweep-bf16", action="store_true")
+    ap.add_argument("--sweep-bf16", action="store_true", default=True,
+                    help="include the BF16 stage/ratio sweep (default on)")
+    ap.add_argument("--no-sweep-bf16", dest="sweep_bf16", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sustained-s", type=float, default=3.0,
@@ -168,19 +170,34 @@ def device_sets(torch, w, A, B, dev, sets):
 
 
 def time_kernel(torch, gp, w, bufs, variant, stages, n, stream, **opts):
-    """Average device time of n launches (CUDA events around each launch on `stream`)."""
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    """Average device time per launch of n back-to-back launches: CUDA events on `stream` before the
+    first and after the last (an event between two launches would stop the next one's set-up from
+    overlapping the previous one's tail, as it does in a stream of GEMMs)."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
     for i in range(n):
         a, b, c = bufs[i % len(bufs)]
-        evs[i][0].record(stream)
         gp.gemm_pipelined(a, b, c, w.M, w.N, w.K, w.dtype, w.layout, stages, variant, stream, **opts)
-        evs[i][1].record(stream)
+    e1.record(stream)
     stream.synchronize()
     st = gp.gemm_stats(sync=True)
     if st["status"] != 0:
         raise RuntimeError("kernel status %d" % st["status"])
-    ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    return statistics.mean(ms), min(ms), st
+    ms = e0.elapsed_time(e1) / n
+    return ms, ms, st
+
+
+def isolated_launch_ms(torch, gp, gemm, n, stream):
+    """Mean device time of n launches each bracketed by its own pair of CUDA events (no overlap
+    with the neighbouring launches)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        evs[i][0].record(stream)
+        gemm(i)
+        evs[i][1].record(stream)
+    stream.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
 def max_over_ranks(torch, dist, x, device):
@@ -420,9 +437,9 @@ def main():
 
         sampler = ClockSampler(local)
         sampler.start()
-        # ---- timed region: K steps, barrier + synchronize on both sides ----
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+        # ---- timed region: K steps back to back, barrier + synchronize on both sides ----
+        # (events only at its ends: one between launches would stop each launch's set-up
+        # from overlapping the previous one's tail)
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         barrier()
@@ -430,9 +447,7 @@ def main():
         wall0 = time.time()
         t_start.record(stream)
         for i in range(args.steps):
-            evs[i][0].record(stream)
             gemm(i)
-            evs[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         wall1 = time.time()
@@ -442,12 +457,12 @@ def main():
         if st["status"] != 0:
             raise RuntimeError("timed region failed: status %d" % st["status"])
         total_ms = t_start.elapsed_time(t_end)
-        kern_ms = [a.elapsed_time(b) for a, b in evs]
+        iso_ms = isolated_launch_ms(torch, gp, gemm, min(args.steps, 50), stream)
 
     total_ms = max_over_ranks(torch, pg, total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = job_throughput(w.ops, world, args.steps, total_ms)
-    kavg = statistics.mean(kern_ms)
+    kavg = total_ms / args.steps    # average launch duration over the timed region (slowest rank)
     achieved = w.ops / (kavg * 1e-3) / 1e12
 
     # ---- sustained: the same step back to back for a few seconds (clocks settle under the power cap) ----
@@ -519,6 +534,8 @@ def main():
     imma_peak = gp.probe_peak("imma_s8", stream) / 1e12 if plan["kernel"].startswith("imma") else None
     bound, _ = roofline_row(w, plan["kernel"], kavg, peaks, imma_peak)
     roofline = {"kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5),
+                "kernel_avg_how": "timed-region CUDA events / steps (launches back to back)",
+                "launch_isolated_ms": round(iso_ms, 5),
                 "traffic": traffic_for(kernel_key, kernel_src)}
     if bound == "hbm":
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
