@@ -27,7 +27,17 @@
  *    which hold no ownership).  Every base pointer must be 16-byte aligned.
  *  - Calls are asynchronous on the caller's CUDA stream (a cudaStream_t passed
  *    as void*; NULL is the legacy default stream).  Nothing synchronises
- *    unless a function says so.
+ *    unless a function says so.  The tcgen05 kernels are launched as
+ *    programmatic dependents of the work before them in the stream: they may
+ *    start their set-up (barriers, tensor memory, descriptor prefetch) while
+ *    that work drains, but touch no global memory until it has completed, so
+ *    stream order is kept exactly as for an ordinary launch.
+ *  - Device workspace: split K-loops (stream-K tails of the tcgen05 kernels,
+ *    split FFMA K-loops) and the FP16 copies of INT8 operands live in a
+ *    workspace the library allocates per (device, stream) on first need,
+ *    grows when a larger plan needs it and keeps (gp_plan.workspace_bytes is
+ *    the size a call uses).  Growing it synchronises that stream once.
+ *    gemm_pipelined_noalloc uses a fixed static array instead.
  *  - Return value: GP_OK (0) or a negative GP_ERR_* code.  Argument errors are
  *    detected on the host before anything is launched; the output is then
  *    untouched.  gemm_strerror() names every code.
