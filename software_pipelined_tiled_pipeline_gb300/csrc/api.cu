@@ -343,11 +343,19 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   };
   auto fits = [&](int bn) { return ring_smem_total(S * stage_bytes(bn), extra) <= kSmemPerCtaMax; };
 
-  const bool pair_ok = fam == 2 && ring && !no_pair && (bn_req == 0 || bn_req == 256) && N > 128 && K > kShortK &&
-                       ring_smem_total(S * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax;
+  // CTA pairs (FP16/BF16 ring): a 256 x 256 tile per pair while S stages of 32 KB fit, else a
+  // 256 x 128 tile (24 KB per CTA per K step, up to 8 stages) -- also the tile for 64 < N <= 128.
+  auto pair_fits = [&](int pbn) {
+    return ring_smem_total(S * (kUmmaBM + pbn / 2) * kUmmaBK * 2, kUmmaEpiBytes) <= kSmemPerCtaMax;
+  };
+  const bool pair_base = fam == 2 && ring && !no_pair && K > kShortK;
+  const bool pair256 = pair_base && (bn_req == 0 || bn_req == 256) && N > 128 && pair_fits(256);
+  const bool pair128 = pair_base && !pair256 && bn_req == 0 && N > 64 && M > 128 && pair_fits(128);
+  const bool pair_ok = pair256 || pair128;
+  const int pair_bn = pair256 ? 256 : 128;
   int bn = 0;
   if (pair_ok) {
-    bn = 256;   // the pair kernel below replaces the single-CTA fields
+    bn = pair_bn;   // the pair kernel below replaces the single-CTA fields
   } else if (bn_req) {
     bool known = false;
     for (int i = 0; i < ncand; ++i) known |= (cands[i] == bn_req);
@@ -367,7 +375,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     if (!bn) return GP_ERR_SMEM;
   }
   p->bn = bn;
-  p->stage_bytes = pair_ok ? kUmmaPairStageBytes : stage_bytes(bn);
+  p->stage_bytes = pair_ok ? (kUmmaBM + pair_bn / 2) * kUmmaBK * 2 : stage_bytes(bn);
   p->ring_bytes = S * p->stage_bytes;
   p->smem_bytes = ring_smem_total(p->ring_bytes, extra);
   if (fam == 2) {
@@ -378,16 +386,17 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     }
   }
   p->persistent = (ring && fam != 0) ? 1 : 0;
-  // FP16/BF16 ring on CTA pairs: 256 x 256 tile per pair, 32 KB per CTA per K step
+  // FP16/BF16 ring on CTA pairs: 256 x BN tile per pair; per CTA per K step 128 rows of A and
+  // BN/2 rows of B (32 KB for BN 256, 24 KB for BN 128)
   if (pair_ok) {
     p->cta_pair = 1;
     p->bm = 256;
-    p->bn = 256;
-    p->stage_bytes = kUmmaPairStageBytes;
+    p->bn = pair_bn;
+    p->stage_bytes = (kUmmaBM + pair_bn / 2) * kUmmaBK * 2;
     p->ring_bytes = S * p->stage_bytes;
     p->smem_bytes = ring_smem_total(p->ring_bytes, kUmmaEpiBytes);
     if (p->smem_bytes < kSmemPerCtaMax / 2 + 1024) p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
-    p->tmem_cols = 512;
+    p->tmem_cols = 2 * pair_bn;
     p->kernel = "umma_pair_ring";
   }
   p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);

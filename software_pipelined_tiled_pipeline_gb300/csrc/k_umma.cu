@@ -1327,7 +1327,8 @@ cudaError_t max_pairs(int kind, int smem_bytes, int* pairs) {
 
 template <bool BF16>
 cudaError_t launch_dtype(LaunchArgs& a, const void** kernel) {
-  if (a.plan.cta_pair) return launch_ring<256, BF16, true>(a, kernel);
+  if (a.plan.cta_pair)
+    return a.plan.bn == 128 ? launch_ring<128, BF16, true>(a, kernel) : launch_ring<256, BF16, true>(a, kernel);
   switch (a.plan.bn) {
     case 256: return launch_bn<256, BF16>(a, kernel);
     case 128: return launch_bn<128, BF16>(a, kernel);

@@ -134,8 +134,24 @@ def test_umma_single_cta_widths_follow_the_budget(gp, S):
             assert q["stage_bytes"] == (128 + b) * 64 * 2 and q["tmem_cols"] == 2 * b
             assert q["tiles"] == 32 * (4096 // b)
     if S > 6:
+        # the 256 x 256 pair tile does not fit 7-8 stages; the 256 x 128 pair tile does
         p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined")
-        assert p["cta_pair"] == 0 and p["bn"] == 64
+        assert p["cta_pair"] == 1 and (p["bm"], p["bn"]) == (256, 128)
+        assert p["stage_bytes"] == (128 + 64) * 64 * 2 and p["tmem_cols"] == 256
+        assert p["smem_bytes"] <= 232448 and p["tiles"] == 16 * 32
+
+
+def test_pair_tile_128_for_narrow_n(gp):
+    # 64 < N <= 128: 256 x 128 tile per CTA pair (each CTA 128 rows of A, 64 rows of B), up to 8 stages
+    for S in range(1, 9):
+        p = gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", S, "pipelined")
+        assert p["kernel"] == "umma_pair_ring" and (p["bm"], p["bn"], p["stages"]) == (256, 128, S)
+        assert p["ring_bytes"] == S * 24576
+    # N <= 64, M <= 128, K <= 256 or an explicit width: one CTA per tile
+    assert gp.gemm_plan(8192, 64, 8192, "bf16", "row_col", 6, "pipelined")["cta_pair"] == 0
+    assert gp.gemm_plan(128, 128, 8192, "bf16", "row_col", 6, "pipelined")["cta_pair"] == 0
+    assert gp.gemm_plan(8192, 128, 256, "bf16", "row_col", 6, "pipelined")["cta_pair"] == 0
+    assert gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 6, "pipelined", bn=128)["cta_pair"] == 0
 
 
 @pytest.mark.parametrize("S,bn", [(1, 128), (4, 128), (6, 128), (7, 128), (8, 64)])

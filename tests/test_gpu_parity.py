@@ -244,6 +244,31 @@ def test_cta_pair_kernel(dtype, M, N, K, S):
         assert diff <= 2.0 ** -6 * Cd.float().abs().max().item()
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K,S", [(512, 128, 1024, 8), (1000, 120, 2056, 7), (2304, 1280, 640, 8),
+                                     (520, 392, 1032, 7), (4096, 4096, 512, 8)])
+def test_cta_pair_128_kernel(dtype, M, N, K, S):
+    # 256 x 128 tile per CTA pair (each CTA 128 rows of A, 64 rows of B): 7-8 stages, or N <= 128
+    lay = "row_col"
+    A, B = operands(dtype, lay, M, N, K, seed=M * 5 + N + K)
+    C, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S)
+    p = st["plan"]
+    assert p["cta_pair"] == 1 and (p["bm"], p["bn"]) == (256, 128) and p["grid"] % 2 == 0
+    if M * N * K <= 3e9:
+        check_full(dtype, lay, A, B, C, K)
+    else:
+        check_sampled(dtype, lay, A, B, C, K, rows=[0, 1, 255, 256, 2049, M - 1], npts=2000, seed=S)
+    # whole tiles on pairs: the same MMA order as one CTA per 128 x 128 tile, bit for bit
+    Cd, std = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, no_stream_k=True)
+    assert std["plan"]["cta_pair"] == 1 and std["plan"]["sk_tiles"] == 0
+    C1, st1 = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=4, bn=128, no_stream_k=True)
+    assert st1["plan"]["cta_pair"] == 0 and st1["plan"]["bn"] == 128
+    assert torch.equal(Cd.view(torch.int16), C1.view(torch.int16))
+    if p["sk_tiles"] > 0:
+        diff = (C.float() - Cd.float()).abs().max().item()
+        assert diff <= 2.0 ** -6 * Cd.float().abs().max().item()
+
+
 @pytest.mark.parametrize("engine", ["tcgen05", "imma"])
 @pytest.mark.parametrize("stages", [1, 2, 4, 6])
 def test_int8_engines_every_depth(engine, stages):
