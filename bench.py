@@ -305,6 +305,26 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
     return out
 
 
+def ffma_tile_sweep(torch, gp, dev, stream, steps=10):
+    """The register-tile sweep: FP32 4096^3 on the FFMA ring (S = 3) with each thread tile TM x TN."""
+    from software_pipelined_tiled_pipeline_gb300 import synth
+    from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
+    w = WORKLOADS["f32_4096"]
+    A, B = synth.operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    bufs = device_sets(torch, w, A, B, dev, 2)
+    rows = []
+    for tile in ((4, 8), (8, 4), (8, 8), (8, 16), (16, 8), (16, 16)):
+        time_kernel(torch, gp, w, bufs, "pipelined", 3, 2, stream, ffma_tile=tile)
+        ms, _, st = time_kernel(torch, gp, w, bufs, "pipelined", 3, steps, stream, ffma_tile=tile)
+        tf = w.ops / (ms * 1e-3) / 1e12
+        rows.append({"tile": "%dx%d" % tile, "threads": st["plan"]["threads"], "ms": round(ms, 4),
+                     "TFLOPS": round(tf, 2), "frac_alu": round(tf / FFMA_PEAK_TFLOPS, 4),
+                     "regs": st["regs_per_thread"], "spill_bytes": st["local_bytes"]})
+    del bufs
+    torch.cuda.empty_cache()
+    return {"workload": "f32_4096", "stages": 3, "rows": rows}
+
+
 def source_sha(name):
     path = os.path.join(ROOT, "software_pipelined_tiled_pipeline_gb300", "csrc", name)
     h = hashlib.sha256()
@@ -642,6 +662,7 @@ def main():
             line["fp16_best_stage"] = {"stages": best["stages"], "TFLOPS": best["TFLOPS"],
                                        "frac": round(best["TFLOPS"] / peaks.get("bf16_tflops", 1920.0), 4)}
         line["ffma_peak_probe_tflops"] = round(gp.probe_peak("ffma_f32", stream) / 1e12, 2)
+        line["ffma_thread_tile_sweep"] = ffma_tile_sweep(torch, gp, dev, stream)
 
     if not args.no_cpu_baseline and world == 1:
         v, R, t, cores = oracle_sample(w, A, B, args.cpu_seconds)

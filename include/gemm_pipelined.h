@@ -152,7 +152,8 @@ typedef struct gp_options {
     int32_t no_stream_k;         /* 1: never split K-loops across CTAs (every tile computed whole) */
     int32_t no_cta_pair;         /* 1: one CTA per output tile even where CTA pairs are available (INT8: use IMMA) */
     int32_t i8_imma;             /* INT8, GP_PIPELINED: 1 = warp-level IMMA ring instead of the tcgen05 path */
-    int32_t reserved[2];
+    int32_t ffma_tm, ffma_tn;    /* FP32, GP_PIPELINED: outputs per thread, rows x columns (0, 0 = 8 x 8);
+                                    built: 4x8, 8x4, 8x8, 8x16, 16x8, 16x16 (else GP_ERR_UNSUPPORTED) */
 } gp_options;
 
 /*

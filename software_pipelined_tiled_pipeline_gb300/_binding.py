@@ -76,7 +76,7 @@ class GpOptions(ctypes.Structure):
     _fields_ = [
         ("bn", ctypes.c_int32), ("time_kernel", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
         ("inject_lost_load", ctypes.c_int32), ("no_stream_k", ctypes.c_int32), ("no_cta_pair", ctypes.c_int32),
-        ("i8_imma", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
+        ("i8_imma", ctypes.c_int32), ("ffma_tm", ctypes.c_int32), ("ffma_tn", ctypes.c_int32),
     ]
 
 
@@ -145,7 +145,7 @@ def abi_version() -> int:
 
 
 def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-             i8_imma=False):
+             i8_imma=False, ffma_tile=None):
     opts = GpOptions()
     opts.bn = int(bn)
     opts.time_kernel = 1 if time_kernel else 0
@@ -154,16 +154,19 @@ def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_s
     opts.no_stream_k = 1 if no_stream_k else 0
     opts.no_cta_pair = 1 if no_cta_pair else 0
     opts.i8_imma = 1 if i8_imma else 0
+    if ffma_tile:
+        opts.ffma_tm, opts.ffma_tn = int(ffma_tile[0]), int(ffma_tile[1])
     return opts
 
 
 def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
                    time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-                   i8_imma=False, check=True) -> int:
+                   i8_imma=False, ffma_tile=None, check=True) -> int:
     """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
-    stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0."""
+    stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0.
+    ffma_tile: (rows, columns) of outputs per thread of the FP32 ring (default 8 x 8)."""
     s = getattr(stream, "cuda_stream", stream)
-    opts = _options(bn, time_kernel, timeout_ns, inject_lost_load, no_stream_k, no_cta_pair, i8_imma)
+    opts = _options(bn, time_kernel, timeout_ns, inject_lost_load, no_stream_k, no_cta_pair, i8_imma, ffma_tile)
     rc = lib().gemm_pipelined_ex(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"),
                                  _enum(layout, LAYOUTS, "layout"), int(stages), _enum(variant, VARIANTS, "variant"),
                                  s or None, ctypes.byref(opts))

@@ -203,6 +203,18 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // FFMA: 3; IMMA: 4 (more buys nothing once the IMMA pipe is busy); tcgen05: 6
 // (the deepest ring the CTA-pair tile fits in 227 KB).
+// Kernel name of the FFMA ring for a thread tile (a static string).
+const char* ffma_ring_name(int tm, int tn) {
+  switch (tm * 100 + tn) {
+    case 408: return "ffma_ring_4x8";
+    case 804: return "ffma_ring_8x4";
+    case 816: return "ffma_ring_8x16";
+    case 1608: return "ffma_ring_16x8";
+    case 1616: return "ffma_ring_16x16";
+    default: return "ffma_ring";
+  }
+}
+
 // INT8 on tcgen05: bytes of the FP16 copies of A and B.
 int64_t i8_conv_bytes(int64_t M, int64_t N, int64_t K) { return (M + N) * K * 2; }
 
@@ -239,7 +251,8 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
 
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
-              int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, bool i8_imma = false) {
+              int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, bool i8_imma = false,
+              int ffma_tm = 0, int ffma_tn = 0) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
@@ -317,8 +330,12 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     p->bm = kFfmaBM;
     p->bk = kFfmaBK;
     cands[ncand++] = kFfmaBN;
-    p->threads = ring ? 288 : 256;
-    p->kernel = ring ? "ffma_ring" : (variant == GP_PINGPONG ? "ffma_pingpong" : "ffma_nopipe");
+    // thread tile of the ring (the register-staged variants build the pages' 8 x 8 only)
+    const int tm = ffma_tm ? ffma_tm : 8, tn = ffma_tn ? ffma_tn : 8;
+    const int compute_threads = ffma_ring_compute_threads(tm, tn);
+    if (ring ? compute_threads == 0 : (tm != 8 || tn != 8)) return GP_ERR_UNSUPPORTED;
+    p->threads = ring ? compute_threads + 32 : 256;
+    p->kernel = ring ? ffma_ring_name(tm, tn) : (variant == GP_PINGPONG ? "ffma_pingpong" : "ffma_nopipe");
   } else if (fam == 1) {
     p->bm = kImmaBM;
     p->bk = kImmaBK;
@@ -635,7 +652,7 @@ int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int sta
   }
   const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
   return plan_impl(M, N, K, dtype, layout, stages, variant, opts ? opts->bn : 0, sms, out, opts && opts->no_stream_k,
-                   no_pair, opts && opts->i8_imma);
+                   no_pair, opts && opts->i8_imma, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
 }
 
 int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
@@ -650,7 +667,8 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   // argument checks that need no device
   gp_plan plan;
   int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan, opts && opts->no_stream_k,
-                     opts && (opts->no_cta_pair || opts->inject_lost_load), opts && opts->i8_imma);
+                     opts && (opts->no_cta_pair || opts->inject_lost_load), opts && opts->i8_imma,
+                     opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }   // empty output: nothing read or written
@@ -689,7 +707,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   } else {
     const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
     rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
-                   opts && opts->i8_imma);
+                   opts && opts->i8_imma, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     void* conv = nullptr;
     const bool i8_tc = plan.cta_pair && dtype == GP_I8_I32;
@@ -742,6 +760,8 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.sm_count = sms;
     a.sk = sk;
     a.ks = ks;
+    a.ffma_tm = (opts && opts->ffma_tm) ? opts->ffma_tm : 8;
+    a.ffma_tn = (opts && opts->ffma_tn) ? opts->ffma_tn : 8;
     a.conv = conv;
     const void* kernel = nullptr;
     switch (family_of(dtype)) {
@@ -887,6 +907,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.sm_count = sms;
     a.sk = sk;
     a.ks = FfmaSplit{1, nullptr, nullptr, 0};
+    a.ffma_tm = a.ffma_tn = 8;
     a.conv = nullptr;
     const void* kernel = nullptr;
     e = launch_umma(a, &kernel);

@@ -106,6 +106,7 @@ struct LaunchArgs {
   KernelCtl ctl;
   SkParams sk;
   FfmaSplit ks;
+  int32_t ffma_tm, ffma_tn; // FFMA ring: thread tile
   void* conv;               // INT8 on tcgen05: FP16 copies of A then B, (M + N) * K halves
   int32_t sm_count;
 };
@@ -113,6 +114,8 @@ struct LaunchArgs {
 // Each family launcher fills *kernel with the function launched (for
 // cudaFuncGetAttributes) and returns a cudaError_t.
 cudaError_t launch_ffma(LaunchArgs& a, const void** kernel);
+// Compute threads of the FFMA ring for thread tile tm x tn (0: that tile is not built).
+int ffma_ring_compute_threads(int tm, int tn);
 cudaError_t launch_imma(LaunchArgs& a, const void** kernel);
 cudaError_t launch_umma(LaunchArgs& a, const void** kernel);
 // CTA pairs of the pair kernel for dtype (FP16/BF16 ring, or INT8 on tcgen05) that fit at once.

@@ -5,16 +5,29 @@
 // Occupancy", section 4.3, register tiling).  A is row-major M x K, B
 // row-major K x N, C row-major M x N.
 //
+// The thread tile TM x TN is a template parameter (8 x 8 by default): the
+// TMA ring also builds 4 x 8, 8 x 4, 8 x 16, 16 x 8 and 16 x 16, the
+// register-tile sweep of "Part 4", section 4.3 (larger tiles reuse more from
+// registers until the register file runs out and the compiler spills).
+//
 // When the tiles alone would leave SMs idle, each tile's K-loop is split over
 // plan.k_splits CTAs (see FfmaSplit); every data path splits it the same way.
 //
 // Three data paths for the K-loop, sharing the shared-memory layout (A tile
 // [128][8], B tile [8][128], as a TMA box copy lays them out) and the compute:
 //  * ffma_ring_kernel    -- a TMA producer warp fills an S-slot ring guarded by
-//                           mbarrier full/empty phases; 8 compute warps
+//                           mbarrier full/empty phases; the compute warps
 //                           consume it (Case 2 with TMA + mbarrier).
 //  * ffma_staged_kernel<PINGPONG=true>  -- register-staged double buffer (Case 1).
 //  * ffma_staged_kernel<PINGPONG=false> -- no overlap (Background).
+//
+// Shared-memory access pattern (no padding or swizzle is needed): a warp's
+// threads take consecutive tx and at most 32 / (128 / TN) values of ty, so an
+// A read (one float4 of 4 K values of a row) touches 1-4 rows 32 bytes apart
+// -- distinct 16-byte bank groups, one wavefront -- and a B read (a float4 of
+// one K row) touches 128 / TN consecutive float4, the minimum number of
+// wavefronts for the bytes read.  The register-staged stores write 512
+// contiguous bytes per warp.
 #include "gp_device.cuh"
 
 namespace gp {
@@ -23,8 +36,6 @@ namespace {
 constexpr int BM = kFfmaBM, BN = kFfmaBN, BK = kFfmaBK;
 constexpr int A_FLOATS = BM * BK;          // 1024
 constexpr int STAGE = kFfmaStageBytes;     // 8192
-constexpr int kComputeThreads = 256;
-constexpr int kComputeWarps = 8;
 
 struct FfmaBarriers {
   uint64_t full[kMaxStages];
@@ -50,70 +61,94 @@ __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks
   nb = in_group / gm;
 }
 
-// Thread (tx, ty) of the 16 x 16 compute grid owns rows ty + 16*i (i < 8) and
-// columns tx*4 + {0..3} and 64 + tx*4 + {0..3}.  Rows 16 apart put the two
-// rows a warp reads from A (ty = 0, 1) 32 bytes apart, in different banks.
+// Thread tile TM x TN of the 128 x 128 CTA tile.  Thread (tx, ty), tx < TX,
+// ty < TY, owns rows ty + TY*i (i < TM) and the float4 column groups
+// g*GSTRIDE + tx*4 + {0..3} (g < NG).
+template <int TM, int TN>
+struct Tile {
+  static constexpr int TY = BM / TM;
+  static constexpr int TX = BN / TN;
+  static constexpr int THREADS = TX * TY;    // compute threads
+  static constexpr int WARPS = THREADS / 32;
+  static constexpr int NG = TN / 4;
+  static constexpr int GSTRIDE = BN / NG;
+  static_assert(TN % 4 == 0 && THREADS % 32 == 0 && THREADS <= 1024, "thread tile");
+};
+
+template <int TM, int TN>
 struct Acc {
-  float c[8][8];
+  float c[TM][TN];
   __device__ __forceinline__ void zero() {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) c[i][j] = 0.f;
+      for (int j = 0; j < TN; ++j) c[i][j] = 0.f;
   }
 };
 
+template <int TM, int TN>
 __device__ __forceinline__ void ffma_kblock(const float* __restrict__ As, const float* __restrict__ Bs, int tx,
-                                            int ty, Acc& acc) {
+                                            int ty, Acc<TM, TN>& acc) {
+  using T = Tile<TM, TN>;
 #pragma unroll
   for (int kh = 0; kh < BK; kh += 4) {
-    float a[8][4];
+    float a[TM][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 v = *reinterpret_cast<const float4*>(As + (ty + 16 * i) * BK + kh);
+    for (int i = 0; i < TM; ++i) {
+      const float4 v = *reinterpret_cast<const float4*>(As + (ty + T::TY * i) * BK + kh);
       a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 b0 = *reinterpret_cast<const float4*>(Bs + (kh + q) * BN + tx * 4);
-      const float4 b1 = *reinterpret_cast<const float4*>(Bs + (kh + q) * BN + 64 + tx * 4);
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      float b[TN];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int g = 0; g < T::NG; ++g) {
+        const float4 v = *reinterpret_cast<const float4*>(Bs + (kh + q) * BN + g * T::GSTRIDE + tx * 4);
+        b[4 * g] = v.x; b[4 * g + 1] = v.y; b[4 * g + 2] = v.z; b[4 * g + 3] = v.w;
+      }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc.c[i][j] = fmaf(a[i][q], b[j], acc.c[i][j]);
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc.c[i][j] = fmaf(a[i][q], b[j], acc.c[i][j]);
     }
   }
 }
 
-__device__ __forceinline__ void ffma_store(float* C, int M, int N, int m0, int n0, int tx, int ty, const Acc& acc) {
+template <int TM, int TN>
+__device__ __forceinline__ void ffma_store(float* C, int M, int N, int m0, int n0, int tx, int ty,
+                                           const Acc<TM, TN>& acc) {
+  using T = Tile<TM, TN>;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = m0 + ty + 16 * i;
+  for (int i = 0; i < TM; ++i) {
+    const int r = m0 + ty + T::TY * i;
     if (r >= M) continue;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = n0 + h * 64 + tx * 4;
+    for (int g = 0; g < T::NG; ++g) {
+      const int col = n0 + g * T::GSTRIDE + tx * 4;
       if (col < N)   // N % 4 == 0: the float4 is entirely inside
         *reinterpret_cast<float4*>(C + static_cast<size_t>(r) * N + col) =
-            make_float4(acc.c[i][4 * h], acc.c[i][4 * h + 1], acc.c[i][4 * h + 2], acc.c[i][4 * h + 3]);
+            make_float4(acc.c[i][4 * g], acc.c[i][4 * g + 1], acc.c[i][4 * g + 2], acc.c[i][4 * g + 3]);
     }
   }
 }
 
-// Barrier of the 256 compute threads (the ring kernel's producer warp is not in it).
-__device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Barrier of the THREADS compute threads (the ring kernel's producer warp is not in it).
+template <int THREADS>
+__device__ __forceinline__ void compute_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+}
 
-// Same barrier, returning the AND of pred over the 256 compute threads.
+// Same barrier, returning the AND of pred over the compute threads.
+template <int THREADS>
 __device__ __forceinline__ bool compute_bar_and(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}\n"
       : "=r"(r)
-      : "r"(pred ? 1u : 0u)
+      : "r"(pred ? 1u : 0u), "n"(THREADS)
       : "memory");
   return r != 0;
 }
@@ -132,37 +167,39 @@ struct FfmaWork {
 // Write the accumulator: to C, or -- K-loop split over several CTAs -- as a
 // partial tile; the CTA whose partial completes the tile adds all of them in
 // split order (so the sum does not depend on which CTA finished last) and
-// writes C.  Called by all 256 compute threads (tid 0..255).
+// writes C.  Called by all compute threads (tid < THREADS).
+template <int TM, int TN>
 __device__ __forceinline__ void ffma_finish(float* C, int M, int N, int m0, int n0, const FfmaWork& w,
-                                            const FfmaSplit& ks, int tx, int ty, int tid, const Acc& acc,
+                                            const FfmaSplit& ks, int tx, int ty, int tid, const Acc<TM, TN>& acc,
                                             int32_t* last) {
+  using T = Tile<TM, TN>;
   if (ks.splits <= 1) {
-    ffma_store(C, M, N, m0, n0, tx, ty, acc);
+    ffma_store<TM, TN>(C, M, N, m0, n0, tx, ty, acc);
     return;
   }
   constexpr int TILE = BM * BN;
   float* base = ks.workspace + static_cast<size_t>(w.tile) * ks.splits * TILE;
   float* mine = base + static_cast<size_t>(w.split) * TILE;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-      __stcg(reinterpret_cast<float4*>(mine + (ty + 16 * i) * BN + h * 64 + tx * 4),
-             make_float4(acc.c[i][4 * h], acc.c[i][4 * h + 1], acc.c[i][4 * h + 2], acc.c[i][4 * h + 3]));
-  compute_bar();
+    for (int g = 0; g < T::NG; ++g)
+      __stcg(reinterpret_cast<float4*>(mine + (ty + T::TY * i) * BN + g * T::GSTRIDE + tx * 4),
+             make_float4(acc.c[i][4 * g], acc.c[i][4 * g + 1], acc.c[i][4 * g + 2], acc.c[i][4 * g + 3]));
+  compute_bar<T::THREADS>();
   if (tid == 0) {
     __threadfence();
     *last = (epoch_count_in(ks.counters + w.tile, ks.epoch) + 1u == static_cast<uint32_t>(ks.splits)) ? 1 : 0;
     __threadfence();
   }
-  compute_bar();
+  compute_bar<T::THREADS>();
   if (!*last) return;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = ty + 16 * i;
+  for (int i = 0; i < TM; ++i) {
+    const int r = ty + T::TY * i;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int off = r * BN + h * 64 + tx * 4;
+    for (int g = 0; g < T::NG; ++g) {
+      const int off = r * BN + g * T::GSTRIDE + tx * 4;
       float4 sum = __ldcg(reinterpret_cast<const float4*>(base + off));
       for (int j = 1; j < ks.splits; ++j) {
         const float4 p = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(j) * TILE + off));
@@ -171,18 +208,20 @@ __device__ __forceinline__ void ffma_finish(float* C, int M, int N, int m0, int 
         sum.z += p.z;
         sum.w += p.w;
       }
-      const int gr = m0 + r, gc = n0 + h * 64 + tx * 4;
+      const int gr = m0 + r, gc = n0 + g * T::GSTRIDE + tx * 4;
       if (gr < M && gc < N) *reinterpret_cast<float4*>(C + static_cast<size_t>(gr) * N + gc) = sum;
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// TMA ring: 8 compute warps + 1 producer warp, one (tile, K split) per CTA
+// TMA ring: compute warps + 1 producer warp, one (tile, K split) per CTA
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
+template <int TM, int TN>
+__global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
     ffma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      float* __restrict__ C, int M, int N, int K, int stages, KernelCtl ctl, FfmaSplit ks) {
+  using T = Tile<TM, TN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align1024(smem_raw);
   FfmaBarriers* bar = reinterpret_cast<FfmaBarriers*>(ring + stages * STAGE);
@@ -197,7 +236,7 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&bar->full[s], 1);
-      mbar_init(&bar->empty[s], kComputeWarps);
+      mbar_init(&bar->empty[s], T::WARPS);
     }
     bar->ctl.abort = 0;
     bar->consumed = 0;
@@ -207,7 +246,7 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
   CtaCtl* cta = &bar->ctl;
   int issued = 0;
 
-  if (warp == kComputeWarps) {
+  if (warp == T::WARPS) {
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
@@ -227,8 +266,8 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
       }
     }
   } else {
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    Acc acc;
+    const int tx = threadIdx.x % T::TX, ty = threadIdx.x / T::TX;
+    Acc<TM, TN> acc;
     acc.zero();
     int s = 0;
     uint32_t ph = 0;
@@ -238,19 +277,20 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
       const bool w = mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       const float* As = reinterpret_cast<const float*>(ring + s * STAGE);
-      ffma_kblock(As, As + A_FLOATS, tx, ty, acc);
+      ffma_kblock<TM, TN>(As, As + A_FLOATS, tx, ty, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->empty[s]);
       ++consumed;
       if (++s == stages) { s = 0; ph ^= 1u; }
     }
     // one decision for all compute warps: a timed-out warp must not leave the others at a barrier
-    if (compute_bar_and(ok)) ffma_finish(C, M, N, mb * BM, nb * BN, wk, ks, tx, ty, threadIdx.x, acc, &bar->last);
+    if (compute_bar_and<T::THREADS>(ok))
+      ffma_finish<TM, TN>(C, M, N, mb * BM, nb * BN, wk, ks, tx, ty, threadIdx.x, acc, &bar->last);
     if (threadIdx.x == 0) bar->consumed = consumed;
   }
 
   __syncthreads();
-  if (cta->abort && warp == kComputeWarps && lane == 0) {
+  if (cta->abort && warp == T::WARPS && lane == 0) {
     CtaCtl never_abort{0};
     for (int i = bar->consumed; i < issued; ++i)
       mbar_wait(&bar->full[i % stages], static_cast<uint32_t>((i / stages) & 1), ctl, &never_abort, kSiteDrain);
@@ -259,8 +299,10 @@ __global__ void __launch_bounds__((kComputeWarps + 1) * 32, 1)
 }
 
 // ---------------------------------------------------------------------------
-// register-staged ping-pong / no-overlap (256 threads)
+// register-staged ping-pong / no-overlap (the 8 x 8 thread tile, 256 threads)
 // ---------------------------------------------------------------------------
+constexpr int kStagedThreads = Tile<8, 8>::THREADS;
+
 struct RegStage {
   float4 a, b;
   // A: thread t loads row t/2, k-quad t%2; B: row t/32, column quad t%32
@@ -284,9 +326,10 @@ struct RegStage {
 };
 
 template <bool PINGPONG>
-__global__ void __launch_bounds__(kComputeThreads, 1)
+__global__ void __launch_bounds__(kStagedThreads, 1)
     ffma_staged_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C, int M, int N,
                        int K, FfmaSplit ks) {
+  using T = Tile<8, 8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int32_t last;
   uint8_t* ring = align1024(smem_raw);
@@ -296,9 +339,9 @@ __global__ void __launch_bounds__(kComputeThreads, 1)
   int mb, nb;
   tile_coords(wk.tile, m_blocks, n_blocks, mb, nb);
   const int m0 = mb * BM, n0 = nb * BN;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int tx = threadIdx.x % T::TX, ty = threadIdx.x / T::TX;
 
-  Acc acc;
+  Acc<8, 8> acc;
   acc.zero();
   RegStage rs;
   if (PINGPONG) {
@@ -311,7 +354,7 @@ __global__ void __launch_bounds__(kComputeThreads, 1)
       const int cur = (kb - wk.kb_begin) & 1;
       if (kb + 1 < wk.kb_end) rs.load(A, B, M, N, K, m0, n0, kb + 1);   // in flight during the compute
       const float* As = reinterpret_cast<const float*>(ring + cur * STAGE);
-      ffma_kblock(As, As + A_FLOATS, tx, ty, acc);
+      ffma_kblock<8, 8>(As, As + A_FLOATS, tx, ty, acc);
       if (kb + 1 < wk.kb_end) rs.store(ring + (cur ^ 1) * STAGE);   // last read in iteration kb-1
       __syncthreads();
     }
@@ -321,14 +364,34 @@ __global__ void __launch_bounds__(kComputeThreads, 1)
       rs.store(ring);
       __syncthreads();
       const float* As = reinterpret_cast<const float*>(ring);
-      ffma_kblock(As, As + A_FLOATS, tx, ty, acc);
+      ffma_kblock<8, 8>(As, As + A_FLOATS, tx, ty, acc);
       __syncthreads();
     }
   }
-  ffma_finish(C, M, N, m0, n0, wk, ks, tx, ty, threadIdx.x, acc, &last);
+  ffma_finish<8, 8>(C, M, N, m0, n0, wk, ks, tx, ty, threadIdx.x, acc, &last);
+}
+
+template <int TM, int TN>
+cudaError_t launch_ring_tile(LaunchArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, const void** kernel) {
+  const gp_plan& p = a.plan;
+  auto k = ffma_ring_kernel<TM, TN>;
+  *kernel = reinterpret_cast<const void*>(k);
+  cudaError_t e = ensure_smem_attr(*kernel, p.smem_bytes);
+  if (e != cudaSuccess) return e;
+  k<<<p.grid, Tile<TM, TN>::THREADS + 32, p.smem_bytes, a.stream>>>(tmA, tmB, static_cast<float*>(a.C), a.M, a.N,
+                                                                      a.K, p.stages, a.ctl, a.ks);
+  return cudaGetLastError();
 }
 
 }  // namespace
+
+// Compute threads of the FFMA ring for a thread tile (0 if that tile is not built).
+int ffma_ring_compute_threads(int tm, int tn) {
+  switch (tm * 100 + tn) {
+    case 408: case 804: case 808: case 816: case 1608: case 1616: return (BM / tm) * (BN / tn);
+    default: return 0;
+  }
+}
 
 cudaError_t launch_ffma(LaunchArgs& a, const void** kernel) {
   gp_plan& p = a.plan;
@@ -342,17 +405,21 @@ cudaError_t launch_ffma(LaunchArgs& a, const void** kernel) {
     if ((e = make_tmap_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, K, N * 4, BN, BK,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
       return e;
-    *kernel = reinterpret_cast<const void*>(ffma_ring_kernel);
-    if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
-    ffma_ring_kernel<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(tmA, tmB, static_cast<float*>(a.C), a.M, a.N,
-                                                                     a.K, p.stages, a.ctl, a.ks);
-  } else {
-    auto k = (a.variant == GP_PINGPONG) ? ffma_staged_kernel<true> : ffma_staged_kernel<false>;
-    *kernel = reinterpret_cast<const void*>(k);
-    if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
-    k<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(static_cast<const float*>(a.A), static_cast<const float*>(a.B),
-                                                      static_cast<float*>(a.C), a.M, a.N, a.K, a.ks);
+    switch (a.ffma_tm * 100 + a.ffma_tn) {
+      case 408: return launch_ring_tile<4, 8>(a, tmA, tmB, kernel);
+      case 804: return launch_ring_tile<8, 4>(a, tmA, tmB, kernel);
+      case 808: return launch_ring_tile<8, 8>(a, tmA, tmB, kernel);
+      case 816: return launch_ring_tile<8, 16>(a, tmA, tmB, kernel);
+      case 1608: return launch_ring_tile<16, 8>(a, tmA, tmB, kernel);
+      case 1616: return launch_ring_tile<16, 16>(a, tmA, tmB, kernel);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  auto k = (a.variant == GP_PINGPONG) ? ffma_staged_kernel<true> : ffma_staged_kernel<false>;
+  *kernel = reinterpret_cast<const void*>(k);
+  if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
+  k<<<p.grid, kStagedThreads, p.smem_bytes, a.stream>>>(static_cast<const float*>(a.A), static_cast<const float*>(a.B),
+                                                        static_cast<float*>(a.C), a.M, a.N, a.K, a.ks);
   return cudaGetLastError();
 }
 

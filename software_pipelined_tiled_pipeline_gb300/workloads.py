@@ -60,6 +60,8 @@ WORKLOADS = {
         Workload("bf16_8192_k1024", "bf16", "row_col", 8192, 8192, 1024, tuple(range(2, 9))),
         Workload("bf16_8192_k4096", "bf16", "row_col", 8192, 8192, 4096, tuple(range(2, 9))),
         Workload("bf16_8192_k16384", "bf16", "row_col", 8192, 8192, 16384, tuple(range(2, 9))),
+        Workload("f32_4096", "f32", "row_row", 4096, 4096, 4096, (3,), ("pipelined",),
+                 "FP32 SGEMM M=N=K=4096 on the FFMA path (the register-tile sweep's size)"),
         Workload("bf16_skinny", "bf16", "row_col", 8192, 128, 8192, tuple(range(2, 9)),
                  description="BF16 low compute/load ratio case M=8192, N=128, K=8192"),
     ]

@@ -107,6 +107,20 @@ def test_umma_pairs_up_to_six_stages(gp, S):
     assert p["compute_load_ratio"] == pytest.approx(128.0)
 
 
+def test_ffma_thread_tiles(gp):
+    # the register-tile sweep: outputs per thread TM x TN of the 128 x 128 CTA tile, plus a producer warp
+    for (tm, tn) in ((4, 8), (8, 4), (8, 8), (8, 16), (16, 8), (16, 16)):
+        p = gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 3, "pipelined", ffma_tile=(tm, tn))
+        assert p["threads"] == (128 // tm) * (128 // tn) + 32 and (p["bm"], p["bn"], p["bk"]) == (128, 128, 8)
+    for bad in ((4, 4), (8, 2), (32, 8), (12, 8)):
+        with pytest.raises(gp.GemmError):
+            gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 3, "pipelined", ffma_tile=bad)
+    # the register-staged variants build the pages' 8 x 8 only
+    with pytest.raises(gp.GemmError):
+        gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 2, "pingpong", ffma_tile=(16, 8))
+    assert gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 2, "pingpong", ffma_tile=(8, 8))["threads"] == 256
+
+
 def test_short_k_runs_one_cta_per_tile(gp):
     # K <= 256: a few K steps per tile, C's write dominates -- one CTA per 128 x 256 tile at 4 stages
     for K in (64, 200, 256):

@@ -308,6 +308,19 @@ def test_ffma_split_k_every_variant(M, N, K):
         assert torch.equal(C2, C), (variant, S)
 
 
+@pytest.mark.parametrize("tile", [(4, 8), (8, 4), (8, 16), (16, 8), (16, 16)])
+def test_ffma_thread_tiles_match_the_8x8_bits(tile):
+    # every thread tile runs each output's K sum in the same order: identical bits, ragged edges included
+    M, N, K = 300, 420, 1000
+    A, B = operands("f32", "row_row", M, N, K, seed=77)
+    ref, _ = run("f32", "row_row", A, B, M, N, K, variant="pipelined", stages=3)
+    check_full("f32", "row_row", A, B, ref, K)
+    C, st = run("f32", "row_row", A, B, M, N, K, variant="pipelined", stages=3, ffma_tile=tile)
+    assert st["plan"]["kernel"] == "ffma_ring_%dx%d" % tile
+    assert st["plan"]["threads"] == (128 // tile[0]) * (128 // tile[1]) + 32
+    assert torch.equal(C, ref)
+
+
 def test_ffma_short_k_is_not_split():
     A, B = operands("f32", "row_row", 128, 128, 40, seed=5)
     C, st = run("f32", "row_row", A, B, 128, 128, 40, variant="pipelined", stages=3)
