@@ -220,6 +220,8 @@ int64_t i8_conv_bytes(int64_t M, int64_t N, int64_t K) { return (M + N) * K * 2;
 
 // FP16/BF16 GEMMs with K up to this many elements run one CTA per tile, not CTA pairs.
 constexpr int64_t kShortK = 256;
+// FP16/BF16 GEMMs with K at least this long default to 5 ring stages (6 below).
+constexpr int64_t kLongK = 4096;
 
 int default_stages(int family) { return family == 0 ? 3 : (family == 1 ? 4 : 6); }
 
@@ -277,6 +279,10 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     // tile beats the CTA pair (measured at 8192 x 8192 x 256, where C's write
     // dominates); its widest tile fits 4 stages.
     if (stages == 0 && family_of(dtype) == 2 && K <= kShortK && N > 128) S = 4;
+    // Long K-loops run best at 5 stages, short ones at 6 (measured on the
+    // 8192^2 BF16 sweep: 0.99 vs 0.93 of the tensor roof at K = 4096, 0.85 vs
+    // 0.87 at K = 1024; equal at 4096^3).
+    if (stages == 0 && family_of(dtype) == 2 && K >= kLongK) S = 5;
   }
 
   std::memset(p, 0, sizeof(*p));

@@ -107,6 +107,13 @@ def test_umma_pairs_up_to_six_stages(gp, S):
     assert p["compute_load_ratio"] == pytest.approx(128.0)
 
 
+def test_default_depth_follows_k(gp):
+    # FP16/BF16 ring: 4 stages at K <= 256 (one CTA per tile), 6 below K = 4096, 5 from there on
+    for K, S in ((256, 4), (1024, 6), (2048, 6), (4096, 5), (16384, 5)):
+        assert gp.gemm_plan(8192, 8192, K, "bf16", "row_col", 0, "pipelined")["stages"] == S, K
+    assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined")["stages"] == 6
+
+
 def test_ffma_thread_tiles(gp):
     # the register-tile sweep: outputs per thread TM x TN of the 128 x 128 CTA tile, plus a producer warp
     for (tm, tn) in ((4, 8), (8, 4), (8, 8), (8, 16), (16, 8), (16, 16)):
