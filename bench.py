@@ -215,6 +215,7 @@ def job_throughput(ops_per_step, world, steps, total_ms):
 
 
 FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12    # SMs x FP32 lanes x FMA x max SM clock
+SUSTAINED_MS = 30.0   # a timed loop at least this long settles at the power-capped clock
 
 
 def compute_peak(kernel, peaks, imma_peak):
@@ -294,6 +295,11 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
                          "sk_tiles": p["sk_tiles"], "ms": round(avg, 4), unit: round(w.ops / (avg * 1e-3) / 1e12, 2),
                          "regs": st["regs_per_thread"], "smem": p["smem_bytes"]})
             rows[-1]["bound"], rows[-1]["roofline_frac"] = roofline_row(w, p["kernel"], avg, peaks, imma_peak)
+            if p["kernel"].startswith("umma") and rows[-1]["bound"] == "tensor" and avg * steps >= SUSTAINED_MS:
+                # a loop this long runs at the power-capped clock: its roof is the sustained peak
+                sus = dict(peaks, bf16_tflops=peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+                rows[-1]["roofline_frac"] = roofline_row(w, p["kernel"], avg, sus, imma_peak)[1]
+                rows[-1]["roof_peak"] = "sustained"
             if rw and rows[-1]["bound"] == "hbm":
                 rows[-1]["rw_roof_frac"] = round(rw_roof_us(w, rw) / (avg * 1e3), 4)
         base = next(r for r in rows if r["variant"] == "pingpong")[unit]
