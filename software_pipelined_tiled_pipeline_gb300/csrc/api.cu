@@ -283,6 +283,9 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     // 8192^2 BF16 sweep: 0.99 vs 0.93 of the tensor roof at K = 4096, 0.85 vs
     // 0.87 at K = 1024; equal at 4096^3).
     if (stages == 0 && family_of(dtype) == 2 && K >= kLongK) S = 5;
+    // 64 < N <= 128 (the 256 x 128 pair tile, 24 KB per stage): the operand
+    // stream bounds these GEMMs, so keep as many bytes in flight as fit.
+    if (stages == 0 && family_of(dtype) == 2 && N > 64 && N <= 128 && M > 128 && K > kShortK) S = kMaxStages;
   }
 
   std::memset(p, 0, sizeof(*p));

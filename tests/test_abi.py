@@ -112,6 +112,9 @@ def test_default_depth_follows_k(gp):
     for K, S in ((256, 4), (1024, 6), (2048, 6), (4096, 5), (16384, 5)):
         assert gp.gemm_plan(8192, 8192, K, "bf16", "row_col", 0, "pipelined")["stages"] == S, K
     assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined")["stages"] == 6
+    # 64 < N <= 128 on the 256 x 128 pair tile: the deepest ring
+    p = gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined")
+    assert (p["stages"], p["cta_pair"], p["bn"]) == (8, 1, 128)
 
 
 def test_ffma_thread_tiles(gp):
