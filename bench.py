@@ -285,7 +285,9 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
             cases += [("pipelined", S, {"no_cta_pair": True, "no_stream_k": True}) for S in (4, 6)]
         if w.dtype == "i8":
             # the TMA ring feeding warp-level IMMA (the ping-pong and no-overlap rows use IMMA too)
-            cases += [("pipelined", S, {"i8_imma": True}) for S in w.stages]
+            cases += [("pipelined", S, {"i8_engine": "imma"}) for S in w.stages]
+            # tcgen05 with the int8 -> FP16 conversion overlapped inside the GEMM kernel (one launch)
+            cases += [("pipelined", S, {"i8_engine": "tcgen05_overlap"}) for S in (4, 6)]
         for variant, S, opts in cases:
             time_kernel(torch, gp, w, bufs, variant, S, 3, stream, **opts)      # warm-up
             avg, best, st = time_kernel(torch, gp, w, bufs, variant, S, steps, stream, **opts)

@@ -72,7 +72,7 @@ typedef enum {
  * GP_PIPELINED runs it on tcgen05 with the operands converted exactly to FP16
  * and the FP32 accumulator restarted every 1024 K (all partial sums stay exact
  * integers below 2^24), while the ping-pong and no-overlap variants (and
- * GP_PIPELINED with gp_options.i8_imma) use warp-level IMMA.  Variants of one
+ * GP_PIPELINED with gp_options.i8_engine = 1) use warp-level IMMA.  Variants of one
  * engine differ only in the data path. */
 typedef enum {
     /* Register-staged double buffer: global loads into registers, compute on
@@ -151,7 +151,11 @@ typedef struct gp_options {
                                     consumer wait runs out and the call reports GP_ERR_TIMEOUT (no GPU fault) */
     int32_t no_stream_k;         /* 1: never split K-loops across CTAs (every tile computed whole) */
     int32_t no_cta_pair;         /* 1: one CTA per output tile even where CTA pairs are available (INT8: use IMMA) */
-    int32_t i8_imma;             /* INT8, GP_PIPELINED: 1 = warp-level IMMA ring instead of the tcgen05 path */
+    int32_t i8_engine;           /* INT8, GP_PIPELINED: 0 = default (2); 1 = warp-level IMMA ring; 2 = tcgen05
+                                    after a separate int8 -> FP16 pass; 3 = tcgen05 in one kernel whose
+                                    converter warps write the FP16 copies while the ring already consumes
+                                    the K steps they have finished (stages <= 5, else engine 2).  Every
+                                    engine gives the same exact int32 results; other values: GP_ERR_ARG */
     int32_t ffma_tm, ffma_tn;    /* FP32, GP_PIPELINED: outputs per thread, rows x columns (0, 0 = 8 x 8);
                                     built: 4x8, 8x4, 8x8, 8x16, 16x8, 16x16 (else GP_ERR_UNSUPPORTED) */
 } gp_options;

@@ -3,6 +3,7 @@
 // dispatch to the kernel families, and the per-thread last-call record.
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -91,6 +92,9 @@ struct Workspace {
   uint32_t epoch = 0;
   void* conv = nullptr;       // INT8 on tcgen05: FP16 copies of the operands
   size_t conv_bytes = 0;
+  uint32_t* ov_ctrs = nullptr;   // INT8 overlap engine: two counter sets of ov_kcap + 1 words
+  int32_t ov_kcap = 0;
+  uint32_t ov_launches = 0;
 };
 constexpr int kMaxWorkspaces = 64;
 Workspace g_ws[kMaxWorkspaces];
@@ -166,6 +170,43 @@ cudaError_t get_conv_workspace(int dev, cudaStream_t stream, size_t bytes, void*
   return cudaSuccess;
 }
 
+// Counters of the INT8 overlap engine, per device and stream: two sets of
+// {batch counter, kcap K-step counters}, used by alternate launches (each
+// launch zeroes the other set for its successor).  Zeroed when (re)allocated.
+cudaError_t get_overlap_ctrs(int dev, cudaStream_t stream, int64_t k_tiles, uint32_t** ctrs, int32_t* kcap,
+                             uint32_t* parity) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace* w = nullptr;
+  for (auto& x : g_ws)
+    if (x.dev == dev && x.stream == stream) { w = &x; break; }
+  if (!w) {
+    for (auto& x : g_ws)
+      if (x.dev < 0) { w = &x; break; }
+    if (!w) return cudaErrorMemoryAllocation;
+    w->dev = dev;
+    w->stream = stream;
+  }
+  cudaError_t e;
+  if (w->ov_kcap < k_tiles) {
+    if (w->ov_ctrs) {
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+      cudaFree(w->ov_ctrs);
+      w->ov_ctrs = nullptr;
+      w->ov_kcap = 0;
+    }
+    const int64_t cap = std::max<int64_t>(k_tiles, 64);
+    const size_t bytes = 2 * static_cast<size_t>(cap + 1) * sizeof(uint32_t);
+    if ((e = cudaMalloc(&w->ov_ctrs, bytes)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(w->ov_ctrs, 0, bytes, stream)) != cudaSuccess) return e;
+    w->ov_kcap = static_cast<int32_t>(cap);
+    w->ov_launches = 0;
+  }
+  *ctrs = w->ov_ctrs;
+  *kcap = w->ov_kcap;
+  *parity = (w->ov_launches++) & 1u;
+  return cudaSuccess;
+}
+
 // ---------------------------------------------------------------------------
 // per-thread last-call record
 // ---------------------------------------------------------------------------
@@ -215,6 +256,14 @@ const char* ffma_ring_name(int tm, int tn) {
   }
 }
 
+// INT8 engine with the int8 -> FP16 conversion in the producer warps (gp_options.i8_engine).
+constexpr int kI8EngineOverlap = 3;
+const char* const kI8OverlapKernelName = "umma_i8_overlap_pair_ring";
+constexpr int kI8OverlapDefaultStages = 5;   // the deepest ring that leaves room for int8 staging
+static_assert(i8_overlap_staging_slots(kI8OverlapDefaultStages) >= 2 &&
+                  i8_overlap_staging_slots(kI8OverlapDefaultStages + 1) < 2,
+              "overlap engine depth limit");
+
 // INT8 on tcgen05: bytes of the FP16 copies of A and B.
 int64_t i8_conv_bytes(int64_t M, int64_t N, int64_t K) { return (M + N) * K * 2; }
 
@@ -253,7 +302,7 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
 
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
-              int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, bool i8_imma = false,
+              int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, int i8_engine = 0,
               int ffma_tm = 0, int ffma_tn = 0) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
@@ -296,25 +345,33 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->stages = S;
   const bool ring = variant == GP_PIPELINED;
 
+  if (i8_engine < 0 || i8_engine > 3) return GP_ERR_ARG;
   const int i8_tc_stages = stages == 0 ? 6 : S;
-  if (fam == 1 && ring && !i8_imma && !no_pair && (bn_req == 0 || bn_req == 256) &&
+  if (fam == 1 && ring && i8_engine != 1 && !no_pair && (bn_req == 0 || bn_req == 256) &&
       ring_smem_total(i8_tc_stages * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax) {
     // INT8 on tcgen05: FP16 operands, CTA pair per 256 x 256 tile, whole tiles.
     // Deeper rings than this tile allows (7, 8 stages) run on the IMMA ring.
-    S = i8_tc_stages;
+    // The overlap engine numbers its conversion units (K step x 128-row panel) in 31 bits.
+    const int64_t conv_units = ceil_div(K, kUmmaBK) * (ceil_div(M, 128) + ceil_div(N, 128));
+    // It also stages int8 tiles in shared memory: deeper rings than kI8OverlapDefaultStages
+    // leave no room, and the two-pass engine runs them.
+    const bool overlap = i8_engine == kI8EngineOverlap && conv_units < (int64_t(1) << 30) &&
+                         (stages == 0 || i8_overlap_staging_slots(S) >= 2);
+    S = overlap && stages == 0 ? kI8OverlapDefaultStages : i8_tc_stages;
     p->stages = S;
     p->bm = 256;
     p->bn = 256;
     p->bk = kUmmaBK;
-    p->threads = 64 + 32 * 8;
+    p->threads = overlap ? 512 : 64 + 32 * 8;
     p->stage_bytes = kUmmaPairStageBytes;
     p->ring_bytes = S * p->stage_bytes;
-    p->smem_bytes = ring_smem_total(p->ring_bytes, kUmmaEpiBytes);
+    p->smem_bytes = overlap ? i8_overlap_smem_total(S, i8_overlap_staging_slots(S))
+                            : ring_smem_total(p->ring_bytes, kUmmaEpiBytes);
     if (p->smem_bytes < kSmemPerCtaMax / 2 + 1024) p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
     p->tmem_cols = 512;
     p->persistent = 1;
     p->cta_pair = 1;
-    p->kernel = "umma_i8_pair_ring";
+    p->kernel = overlap ? kI8OverlapKernelName : "umma_i8_pair_ring";
     p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
     p->k_tiles = ceil_div(K, p->bk);
     if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
@@ -325,7 +382,8 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     // Stream-K over the CTA pairs (int32 partials: exact in any order), only
     // when the tiles do not fill one wave: with a partial last wave the
     // heavier int32 split epilogue measured slower than whole tiles.
-    if (sm_count > 1 && p->tiles < sm_count / 2) apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
+    // (The overlap engine writes the same FP16 copies from inside the GEMM kernel; whole tiles only.)
+    if (!overlap && sm_count > 1 && p->tiles < sm_count / 2) apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
     p->workspace_bytes += i8_conv_bytes(M, N, K);   // FP16 copies of A and B, after the partial tiles
     // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B (FP16)
     p->compute_load_ratio = 2.0 * 128 * 256 * p->bk / ((128.0 + 128.0) * p->bk * 2.0);
@@ -661,7 +719,7 @@ int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int sta
   }
   const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
   return plan_impl(M, N, K, dtype, layout, stages, variant, opts ? opts->bn : 0, sms, out, opts && opts->no_stream_k,
-                   no_pair, opts && opts->i8_imma, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
+                   no_pair, opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
 }
 
 int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
@@ -676,7 +734,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   // argument checks that need no device
   gp_plan plan;
   int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan, opts && opts->no_stream_k,
-                     opts && (opts->no_cta_pair || opts->inject_lost_load), opts && opts->i8_imma,
+                     opts && (opts->no_cta_pair || opts->inject_lost_load), opts ? opts->i8_engine : 0,
                      opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
@@ -716,23 +774,31 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   } else {
     const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
     rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
-                   opts && opts->i8_imma, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
+                   opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     void* conv = nullptr;
-    const bool i8_tc = plan.cta_pair && dtype == GP_I8_I32;
+    const bool i8_overlap = plan.cta_pair && dtype == GP_I8_I32 && plan.kernel == kI8OverlapKernelName;
+    const bool i8_tc = plan.cta_pair && dtype == GP_I8_I32;   // both engines keep FP16 copies
     const int64_t conv_bytes = i8_tc ? i8_conv_bytes(M, N, K) : 0;
+    uint32_t* conv_ctrs = nullptr;
+    int32_t conv_kcap = 0;
+    uint32_t conv_parity = 0;
     if (plan.cta_pair) {
       // pairs must sit on one TPC each: the resident count may be below SMs / 2
       int pairs = 0;
-      e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
+      e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs, i8_overlap);
       if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
-      if (pairs < sms / 2 && (!i8_tc || plan.tiles < pairs)) {
+      if (pairs < sms / 2 && !i8_overlap && (!i8_tc || plan.tiles < pairs)) {
         apply_stream_k(&plan, pairs, 2, !(opts && opts->no_stream_k));
         plan.workspace_bytes += conv_bytes;
       }
       if (i8_tc) {
         e = get_conv_workspace(dev, st, static_cast<size_t>(conv_bytes), &conv);
+        if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      }
+      if (i8_overlap) {
+        e = get_overlap_ctrs(dev, st, plan.k_tiles, &conv_ctrs, &conv_kcap, &conv_parity);
         if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
       }
     }
@@ -772,12 +838,19 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.ffma_tm = (opts && opts->ffma_tm) ? opts->ffma_tm : 8;
     a.ffma_tn = (opts && opts->ffma_tn) ? opts->ffma_tn : 8;
     a.conv = conv;
+    a.i8_overlap = i8_overlap;
+    a.conv_ctrs = conv_ctrs;
+    a.conv_kcap = conv_kcap;
+    a.conv_parity = conv_parity;
     const void* kernel = nullptr;
     switch (family_of(dtype)) {
       case 0: e = launch_ffma(a, &kernel); break;
       case 1: e = plan.cta_pair ? launch_umma_i8(a, &kernel) : launch_imma(a, &kernel); break;
       default: e = launch_umma(a, &kernel); break;
     }
+    // A launch that did not start left its successor's counter set unzeroed: clear both sets.
+    if (e != cudaSuccess && i8_overlap)
+      cudaMemsetAsync(conv_ctrs, 0, 2 * static_cast<size_t>(conv_kcap + 1) * sizeof(uint32_t), st);
     t_last.stats.plan = a.plan;
     t_last.kernel = kernel;
   }
@@ -918,6 +991,10 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.ks = FfmaSplit{1, nullptr, nullptr, 0};
     a.ffma_tm = a.ffma_tn = 8;
     a.conv = nullptr;
+    a.i8_overlap = false;
+    a.conv_ctrs = nullptr;
+    a.conv_kcap = 0;
+    a.conv_parity = 0;
     const void* kernel = nullptr;
     e = launch_umma(a, &kernel);
     t_last.stats.plan = a.plan;

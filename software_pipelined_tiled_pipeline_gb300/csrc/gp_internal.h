@@ -23,6 +23,8 @@ enum WaitSite : uint32_t {
   kSiteEpilogueAccFull = 4,
   kSitePingPongMma = 5,
   kSiteDrain = 6,
+  kSiteConvReady = 7,     // INT8 overlap engine: producer waiting for a K step's FP16 copies
+  kSiteConvRing = 8,      // INT8 overlap engine: converter / signaller hand-off
 };
 
 struct KernelCtl {
@@ -92,6 +94,23 @@ __host__ __device__ constexpr int ring_smem_total(int ring_bytes, int extra) {
   return kSmemAlignSlack + ring_bytes + extra + kBarrierRegion;
 }
 
+// INT8 on tcgen05 with the conversion overlapped inside the GEMM kernel: the
+// two-pass engine's ring and epilogue staging, an int8 staging ring of G slots
+// (one conversion unit each: 128 rows x 64 int8) and the hand-off barriers.
+constexpr int kI8ConvUnitBytes = 128 * 64;
+constexpr int kI8MaxStg = 8;
+constexpr int kI8ConvBarrierBytes = 384;
+__host__ __device__ constexpr int i8_overlap_smem_total(int stages, int stg_slots) {
+  return ring_smem_total(stages * kUmmaPairStageBytes + stg_slots * kI8ConvUnitBytes + kI8ConvBarrierBytes,
+                         kUmmaEpiBytes);
+}
+// Staging slots that fit beside an S-slot ring (at most kI8MaxStg; fewer than 2: S is too deep).
+__host__ __device__ constexpr int i8_overlap_staging_slots(int stages) {
+  return (kSmemPerCtaMax - i8_overlap_smem_total(stages, 0)) / kI8ConvUnitBytes < kI8MaxStg
+             ? (kSmemPerCtaMax - i8_overlap_smem_total(stages, 0)) / kI8ConvUnitBytes
+             : kI8MaxStg;
+}
+
 // ---------------------------------------------------------------------------
 // launch interface between the API and the kernel translation units
 // ---------------------------------------------------------------------------
@@ -108,6 +127,10 @@ struct LaunchArgs {
   FfmaSplit ks;
   int32_t ffma_tm, ffma_tn; // FFMA ring: thread tile
   void* conv;               // INT8 on tcgen05: FP16 copies of A then B, (M + N) * K halves
+  bool i8_overlap;          // INT8 on tcgen05: the GEMM kernel writes the FP16 copies itself
+  uint32_t* conv_ctrs;      // ... its two counter sets: {batch counter, conv_kcap K-step counters}
+  int32_t conv_kcap;
+  uint32_t conv_parity;     // ... the set this launch uses (it zeroes the other)
   int32_t sm_count;
 };
 
@@ -118,8 +141,9 @@ cudaError_t launch_ffma(LaunchArgs& a, const void** kernel);
 int ffma_ring_compute_threads(int tm, int tn);
 cudaError_t launch_imma(LaunchArgs& a, const void** kernel);
 cudaError_t launch_umma(LaunchArgs& a, const void** kernel);
-// CTA pairs of the pair kernel for dtype (FP16/BF16 ring, or INT8 on tcgen05) that fit at once.
-cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs);
+// CTA pairs of the pair kernel for dtype (FP16/BF16 ring, or INT8 on tcgen05: two-pass or
+// conversion overlapped in the kernel) that fit at once.
+cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs, bool i8_overlap = false);
 // INT8 x INT8 -> INT32 on tcgen05 (FP16 operands, accumulator restarted every 1024 K).
 cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel);
 cudaError_t launch_zero_fill(void* C, int64_t bytes, cudaStream_t stream);

@@ -30,6 +30,7 @@
 // All three use the same tile shape, shared-memory layout (K-major tiles of
 // 128-byte rows with the 128-byte swizzle), MMA sequence and epilogue, so
 // they differ only in how tiles reach shared memory.
+#include <atomic>
 #include "gp_device.cuh"
 
 namespace gp {
@@ -1031,6 +1032,423 @@ __global__ void __launch_bounds__(kI8Threads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// exact INT8 on tcgen05 with the int8 -> FP16 conversion overlapped in-kernel
+// ---------------------------------------------------------------------------
+// The same CTA-pair tile, TMA ring over FP16 copies of A and B, MMA sequence
+// and int32 epilogue as umma_i8_kernel, but the copies are written by this
+// kernel while it runs instead of by a conversion pass before it.
+//
+// Conversion units: one K step (64 columns) of one 128-row panel of A or of B,
+// numbered K step major (unit u: K step u / P, panel u % P, P = ceil(M/128) +
+// ceil(N/128) panels, A's first).  In every CTA a loader thread claims units
+// (one, then four at a time) from a launch-wide counter (so the first K steps of every
+// panel are converted first, and every unit is converted by whichever CTAs
+// are resident: nothing depends on all CTAs running at once) and loads each
+// into an int8 staging slot of shared memory with TMA.  Four converter warps
+// read a slot, convert (i8x4_to_f16x4) and store the FP16 values with plain
+// global stores; a signalling thread then counts the unit on its K step's
+// counter (after a GPU-scope fence, one per group of units it finds ready).
+// The TMA producer issues the loads of K step kb only once that counter holds
+// all P units (then an acquire fence and a generic -> async proxy fence);
+// from the first time it sees every K step complete it stops checking.  The
+// counters come in two sets used by alternate launches: each launch zeroes
+// the other set for the next one (which reads it only after this launch has
+// completed).
+//
+// 512 threads = four warpgroups: converters (warps 0-3); TMA producer (warp
+// 4), MMA issuer and TMEM owner (warp 5), signaller (warp 6), loader (warp
+// 7); eight epilogue warps (8-15: TMEM lane quarter warp % 4, column half
+// (warp - 8) / 4).  Launched at 128 registers per thread; the second
+// warpgroup gives back to 48 and the epilogue warpgroups take 168 (their 128
+// running int32 sums): 4*32*128 + 4*32*48 + 8*32*168 = 65,536.
+constexpr int kOvThreads = 512;
+constexpr int kConvWarps = 4;
+constexpr int kOvLaunchRegs = 65536 / kOvThreads;   // what __launch_bounds__(512, 1) allows
+constexpr int kOvCtlRegs = 48;
+constexpr int kOvEpiRegs = 168;
+static_assert(4 * 32 * kOvLaunchRegs + 4 * 32 * kOvCtlRegs + 8 * 32 * kOvEpiRegs <= kOvThreads * kOvLaunchRegs,
+              "register split");
+constexpr int kConvUnitRows = 128;    // rows of one unit (one CTA's half of a pair tile)
+constexpr int kConvBatch = 4;         // units per claim
+constexpr int kConvRing = 8;          // converted units the signaller may lag behind
+static_assert(kConvUnitRows * BK == kI8ConvUnitBytes, "unit = 128 rows x one K step of int8");
+
+struct ConvBarriers {
+  uint64_t stg_full[kI8MaxStg];    // a unit's int8 tile landed (loader arrive + TMA bytes), or the end mark
+  uint64_t stg_empty[kI8MaxStg];   // the converter warps have read it (count kConvWarps)
+  uint64_t done[kConvRing];        // the converter warps stored a unit's FP16 values (count kConvWarps)
+  uint64_t free[kConvRing];        // the signaller counted it (count 1)
+  int32_t stg_unit[kI8MaxStg];     // unit in each staging slot; -1: no more units
+  int32_t done_unit[kConvRing];    // unit in each hand-off slot; -1: the converters have finished
+};
+static_assert(sizeof(ConvBarriers) <= kI8ConvBarrierBytes, "conversion barrier region too small");
+
+// Shape of the unit space of one launch.
+struct ConvUnits {
+  int pa, p, kt;               // A panels, all panels, K steps
+  int64_t units;               // kt * p
+  __device__ __forceinline__ void init(int M, int N, int K) {
+    pa = (M + kConvUnitRows - 1) / kConvUnitRows;
+    p = pa + (N + kConvUnitRows - 1) / kConvUnitRows;
+    kt = (K + BK - 1) / BK;
+    units = static_cast<int64_t>(kt) * p;
+  }
+  // K step, operand and first row of unit u
+  __device__ __forceinline__ void coords(int64_t u, int& kb, bool& is_a, int& row0) const {
+    kb = static_cast<int>(u / p);
+    const int pn = static_cast<int>(u % p);
+    is_a = pn < pa;
+    row0 = (is_a ? pn : pn - pa) * kConvUnitRows;
+  }
+};
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+  return *reinterpret_cast<const volatile uint32_t*>(p);
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kOvThreads, 1)
+    umma_i8_overlap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA8,
+                           const __grid_constant__ CUtensorMap tmB8, __half* a16, __half* b16, uint32_t* ctrs,
+                           int kcap, uint32_t parity, int M, int N, int K, int stages, int stg_slots,
+                           KernelCtl ctl) {
+  constexpr int BN = 256;
+  constexpr int HALF = BN / 2;
+  using Sh = RingShape<BN, true>;
+  constexpr int STAGE = Sh::STAGE;
+  constexpr uint32_t IDESC = umma_idesc_f16(false, Sh::TILE_M, BN);
+  static_assert(kI8EpiWarps * kUmmaEpiBufBytes <= kUmmaEpiBytes, "staging region too small");
+  static_assert(Sh::A_ROWS == kConvUnitRows && Sh::B_ROWS == kConvUnitRows, "a unit is one CTA's half tile");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* ring = smem;
+  uint8_t* stg = smem + stages * STAGE;
+  uint8_t* epi = stg + stg_slots * kI8ConvUnitBytes;
+  UmmaBarriers* bar = reinterpret_cast<UmmaBarriers*>(epi + kUmmaEpiBytes);
+  ConvBarriers* cbar = reinterpret_cast<ConvBarriers*>(epi + kUmmaEpiBytes + kBarrierRegion);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int worker = static_cast<int>(blockIdx.x >> 1);
+  const int workers = static_cast<int>(gridDim.x >> 1);
+  const int m_blocks = (M + Sh::TILE_M - 1) / Sh::TILE_M;
+  const int n_blocks = (N + BN - 1) / BN;
+  const int tiles = m_blocks * n_blocks;
+  ConvUnits cu;
+  cu.init(M, N, K);
+  const int kt = cu.kt;
+  // counter set `parity`: a batch counter and kcap >= kt K-step counters, zero at launch
+  uint32_t* claim_ctr = ctrs + parity * (kcap + 1);
+  uint32_t* kstep_ctr = claim_ctr + 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&bar->full[s], 1);
+      mbar_init(&bar->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bar->acc_full[a], 1);
+      mbar_init(&bar->acc_empty[a], 2 * kI8EpiWarps);
+    }
+    for (int g = 0; g < stg_slots; ++g) {
+      mbar_init(&cbar->stg_full[g], 1);
+      mbar_init(&cbar->stg_empty[g], kConvWarps);
+    }
+    for (int r = 0; r < kConvRing; ++r) {
+      mbar_init(&cbar->done[r], kConvWarps);
+      mbar_init(&cbar->free[r], 1);
+    }
+    mbar_init(&bar->drain, 1);
+    bar->ctl.abort = 0;
+    bar->consumed_hi = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc_pair(&bar->tmem_base, Sh::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 7 && lane == 0) {
+    tma_prefetch_desc(&tmA8);
+    tma_prefetch_desc(&tmB8);
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  pdl_launch_dependents();
+  pdl_wait();   // A and B may come from the previous kernel; it may still read the FP16 copies
+  const uint32_t tmem = bar->tmem_base;
+  CtaCtl* cta = &bar->ctl;
+
+  if (warp < kConvWarps) {
+    // ---------------- converters (every CTA): staging slot -> FP16 copy -> signaller ----------------
+    const int t = threadIdx.x;
+    const int c = t & 3;
+    const uint32_t stg0 = smem_u32(stg);
+    int g = 0, r = 0;
+    uint32_t gph = 0, fph = 0;
+    for (;;) {
+      // every lane observes the TMA bytes (acquire); the warp agrees on the outcome
+      const bool w = mbar_wait(&cbar->stg_full[g], gph, ctl, cta, kSiteConvRing);
+      if (!__all_sync(0xffffffffu, w)) break;
+      const int32_t u = cbar->stg_unit[g];
+      if (u >= 0) {
+        const uint32_t sa = stg0 + static_cast<uint32_t>(g) * kI8ConvUnitBytes;
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ld_shared_v4(sa + static_cast<uint32_t>(((t >> 2) + 32 * i) * BK + c * 16));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cbar->stg_empty[g]);
+        int kb, row0;
+        bool is_a;
+        cu.coords(u, kb, is_a, row0);
+        const int rows = is_a ? M : N;
+        __half* dst = is_a ? a16 : b16;
+        const int kx = kb * BK + c * 16;   // K % 16 == 0: a chunk is wholly inside or outside
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = row0 + (t >> 2) + 32 * i;
+          if (row < rows && kx < K)
+            i8x16_store_f16(v[i], reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * K + kx));
+        }
+      }
+      if (++g == stg_slots) { g = 0; gph ^= 1u; }
+      // hand the unit (or the end) to the signaller
+      uint32_t ok = 1;
+      if (lane == 0) ok = mbar_wait(&cbar->free[r], fph ^ 1u, ctl, cta, kSiteConvRing) ? 1u : 0u;
+      if (__shfl_sync(0xffffffffu, ok, 0) == 0) break;
+      __syncwarp();   // every lane's stores precede lane 0's release-arrive
+      if (lane == 0) {
+        if (warp == 0) cbar->done_unit[r] = u;
+        mbar_arrive(&cbar->done[r]);
+      }
+      if (++r == kConvRing) { r = 0; fph ^= 1u; }
+      if (u < 0) break;
+    }
+  } else if (warp < 8) {
+    regs_decrease<kOvCtlRegs>();
+    if (warp == 7 && lane == 0) {
+      // ---------------- loader: claim units, TMA their int8 tiles into the staging ring ----------------
+      if (blockIdx.x == 0) {   // the other counter set, for the next launch
+        uint32_t* next_set = ctrs + (parity ^ 1u) * (kcap + 1);
+        for (int i = 0; i <= kcap; ++i) next_set[i] = 0u;
+      }
+      int g = 0;
+      uint32_t gph = 0;
+      bool ok = true;
+      // The counter counts units.  A CTA's first claim is one unit, so the first
+      // K steps are spread over many CTAs and ready early; later claims take
+      // kConvBatch units (fewer atomics).
+      uint32_t b = atomicAdd(claim_ctr, 1u);
+      uint32_t bn = 1;
+      while (ok && b < cu.units) {
+        const uint32_t b_next = atomicAdd(claim_ctr, static_cast<uint32_t>(kConvBatch));   // in flight meanwhile
+        for (int i = 0; i < static_cast<int>(bn); ++i) {
+          const int64_t u = static_cast<int64_t>(b) + i;
+          if (u >= cu.units) break;
+          if (!mbar_wait(&cbar->stg_empty[g], gph ^ 1u, ctl, cta, kSiteConvRing)) { ok = false; break; }
+          int kb, row0;
+          bool is_a;
+          cu.coords(u, kb, is_a, row0);
+          cbar->stg_unit[g] = static_cast<int32_t>(u);
+          mbar_arrive_expect_tx(&cbar->stg_full[g], kI8ConvUnitBytes);
+          tma_load_2d(smem_u32(stg + g * kI8ConvUnitBytes), is_a ? &tmA8 : &tmB8, &cbar->stg_full[g], kb * BK, row0);
+          if (++g == stg_slots) { g = 0; gph ^= 1u; }
+        }
+        b = b_next;
+        bn = kConvBatch;
+      }
+      if (ok && mbar_wait(&cbar->stg_empty[g], gph ^ 1u, ctl, cta, kSiteConvRing)) {
+        cbar->stg_unit[g] = -1;   // end mark: a plain arrive completes the phase
+        mbar_arrive(&cbar->stg_full[g]);
+      }
+    } else if (warp == 6 && lane == 0) {
+      // ---------------- signaller: count converted units on their K steps ----------------
+      int r = 0;
+      uint32_t dph = 0;
+      bool end = false;
+      while (!end) {
+        if (!mbar_wait(&cbar->done[r], dph, ctl, cta, kSiteConvRing)) break;
+        // this unit and every later one already handed over, up to the end mark
+        int n = 0;
+        int rr = r;
+        uint32_t pp = dph;
+        for (;;) {
+          if (cbar->done_unit[rr] < 0) { end = true; break; }
+          ++n;
+          if (++rr == kConvRing) { rr = 0; pp ^= 1u; }
+          if (n == kConvRing || !mbar_try_wait(smem_u32(&cbar->done[rr]), pp)) break;
+        }
+        if (n == 0) break;
+        __threadfence();   // release at GPU scope: the converters' stores, seen through the barriers
+        for (int i = 0; i < n; ++i) {
+          atomicAdd(kstep_ctr + cbar->done_unit[r] / cu.p, 1u);
+          mbar_arrive(&cbar->free[r]);
+          if (++r == kConvRing) { r = 0; dph ^= 1u; }
+        }
+      }
+    } else if (warp == 4 && lane == 0) {
+      // ---------------- producer (every CTA): a K step's loads once all its units are converted ----------------
+      int s = 0;
+      uint32_t ph = 0;
+      int ready = 0;   // K steps [0, ready) are converted
+      for (int tile = worker; tile < tiles; tile += workers) {
+        int mb, nb;
+        tile_coords(tile, m_blocks, n_blocks, mb, nb);
+        const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
+        const int n_row = nb * BN + rank * Sh::B_ROWS;
+        for (int kb = 0; kb < kt; ++kb) {
+          if (kb >= ready) {
+            const uint64_t t0 = global_timer_ns();
+            for (;;) {
+              uint32_t c[8];   // eight independent loads in flight
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                c[i] = ready + i < kt ? ld_volatile_u32(kstep_ctr + ready + i) : 0u;
+              int adv = 0;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (adv == i && c[i] == static_cast<uint32_t>(cu.p)) adv = i + 1;
+              ready += adv;
+              if (kb < ready) break;
+              if (cta->abort) goto ov_producer_done;
+              if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                report_error(ctl.status, kDevErrTimeout, kSiteConvReady);
+                cta->abort = 1;
+                goto ov_producer_done;
+              }
+              __nanosleep(128);
+            }
+            __threadfence();             // acquire: the copies the counts stand for
+            fence_proxy_async_global();  // written by generic stores, read by TMA
+          }
+          if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto ov_producer_done;
+          uint8_t* slot = ring + s * STAGE;
+          if (leader) mbar_arrive_expect_tx(&bar->full[s], 2 * STAGE);
+          const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), 0);
+          tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
+          tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
+          if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+      }
+    ov_producer_done:;
+    } else if (warp == 5 && lane == 0 && leader) {
+      // ---------------- MMA issuer: one accumulator buffer per 1024-element chunk of K ----------------
+      int s = 0;
+      uint32_t ph = 0;
+      int t = 0;
+      bool ok = true;
+      for (int tile = worker; tile < tiles && ok; tile += workers) {
+        for (int kb0 = 0; kb0 < kt && ok; kb0 += kI8ChunkSteps, ++t) {
+          const int a = t & 1;
+          if (!mbar_wait(&bar->acc_empty[a], ((t >> 1) & 1) ^ 1u, ctl, cta, kSiteMmaAccEmpty)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + a * BN;
+          const int kb1 = min(kt, kb0 + kI8ChunkSteps);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(ring + s * STAGE);
+            const uint64_t da = umma_desc_sw128(a_addr);
+            const uint64_t db = umma_desc_sw128(a_addr + Sh::A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+              umma_f16_pair(d, da + 2 * kk, db + 2 * kk, IDESC, (kb == kb0 && kk == 0) ? 0u : 1u);
+            umma_commit_pair(&bar->empty[s], 0x3);
+            if (++s == stages) { s = 0; ph ^= 1u; }
+          }
+          if (!ok) break;
+          umma_commit_pair(&bar->acc_full[a], 0x3);
+        }
+      }
+      umma_commit_pair(&bar->drain, 0x1);
+      CtaCtl never_abort{0};
+      mbar_wait(&bar->drain, 0, ctl, &never_abort, kSiteDrain);
+    }
+  } else {
+    regs_increase<kOvEpiRegs>();
+    // ---------------- epilogue: int32 running sum of the exact FP32 chunk sums ----------------
+    const int q = warp & 3;
+    const int e = warp - 8;
+    const int h = e >> 2;              // column half of the accumulator
+    uint8_t* my_stage = epi + e * kUmmaEpiBufBytes;
+    int t = 0;
+    bool ok = true;
+    for (int tile = worker; tile < tiles && ok; tile += workers) {
+      int mb, nb;
+      tile_coords(tile, m_blocks, n_blocks, mb, nb);
+      uint32_t sum[HALF];
+#pragma unroll
+      for (int i = 0; i < HALF; ++i) sum[i] = 0u;
+      for (int kb0 = 0; kb0 < kt; kb0 += kI8ChunkSteps, ++t) {
+        const int a = t & 1;
+        uint32_t w = 1;
+        if (lane == 0) w = mbar_wait(&bar->acc_full[a], (t >> 1) & 1, ctl, cta, kSiteEpilogueAccFull) ? 1u : 0u;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!i8_epi_bar_and(w != 0 && !cta->abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN + h * HALF;
+#pragma unroll
+        for (int sub = 0; sub < HALF / 16; ++sub) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(trow + sub * 16, v);
+          tmem_wait_ld();
+          regs_after_wait(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)   // exact integers of magnitude <= 2^24 in FP32
+            sum[sub * 16 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), 0));
+      }
+      if (!ok) break;
+      const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
+#pragma unroll
+      for (int sub = 0; sub < HALF / 32; ++sub) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        const int x = nb * BN + h * HALF + sub * 32;
+        stage_and_store_i32(sum + sub * 32, my_stage, lane, &tmC, x, y, (x < N) && (y < M));
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+
+  __syncthreads();
+  // After an abort, give TMA loads still in flight and the partner's arrivals
+  // on this CTA's barriers time to land before the pair tears down.
+  if (cta->abort && threadIdx.x == 0) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+  }
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, Sh::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // register-staged ping-pong and no-overlap variants (256 threads, one tile per CTA)
 // ---------------------------------------------------------------------------
 constexpr int kPPThreads = 256;
@@ -1318,16 +1736,76 @@ cudaError_t launch_i8(LaunchArgs& a, const void** kernel) {
   return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl, a.sk);
 }
 
+// INT8 on tcgen05, the conversion overlapped inside the GEMM kernel: one launch.
+cudaError_t launch_i8_overlap(LaunchArgs& a, const void** kernel) {
+  using Sh = RingShape<256, true>;
+  const gp_plan& p = a.plan;
+  const uint64_t M = a.M, N = a.N, K = a.K;
+  __half* a16 = static_cast<__half*>(a.conv);
+  __half* b16 = a16 + M * K;
+  CUtensorMap tmA, tmB, tmC;
+  cudaError_t e;
+  if ((e = make_tmap_2d(&tmC, a.C, CU_TENSOR_MAP_DATA_TYPE_INT32, N, M, N * 4, 32, kUmmaEpiRows,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_2d(&tmA, a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, M, K * 2, BK, Sh::A_ROWS,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_2d(&tmB, b16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, N, K * 2, BK, Sh::B_ROWS,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  const int stg_slots = i8_overlap_staging_slots(p.stages);
+  if (stg_slots < 2) return cudaErrorInvalidValue;
+  CUtensorMap tmA8, tmB8;   // the int8 operands, one conversion unit (64 x 128) per box
+  if ((e = make_tmap_2d(&tmA8, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      cudaSuccess)
+    return e;
+  if ((e = make_tmap_2d(&tmB8, a.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, BK, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+      cudaSuccess)
+    return e;
+  auto k = umma_i8_overlap_kernel;
+  *kernel = reinterpret_cast<const void*>(k);
+  // The warpgroups' register split is sized for a launch at exactly 128
+  // registers per thread: with fewer, the epilogue's setmaxnreg.inc could not
+  // be satisfied.  Refuse such a build instead of launching it.
+  static std::atomic<int> launch_regs{-1};
+  if (launch_regs.load() < 0) {
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, k)) != cudaSuccess) return e;
+    launch_regs.store(fa.numRegs);
+  }
+  if (launch_regs.load() != kOvLaunchRegs) return cudaErrorInvalidConfiguration;
+  if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, tmA8, tmB8, a16, b16, a.conv_ctrs, a.conv_kcap, a.conv_parity,
+                            a.M, a.N, a.K, p.stages, stg_slots, a.ctl);
+}
+
 // Largest number of CTA pairs of a pair kernel that can be resident at once.
+// kind: 0 FP16 ring, 1 BF16 ring, 2 INT8 two-pass, 3 INT8 with the conversion overlapped.
 cudaError_t max_pairs(int kind, int smem_bytes, int* pairs) {
-  const void* k = kind == 2   ? reinterpret_cast<const void*>(umma_i8_kernel<true>)
+  const void* k = kind == 3   ? reinterpret_cast<const void*>(umma_i8_overlap_kernel)
+                  : kind == 2 ? reinterpret_cast<const void*>(umma_i8_kernel<true>)
                   : kind == 1 ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true>)
                               : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true>);
   cudaError_t e = ensure_smem_attr(k, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kind == 2 ? kI8Threads : RingShape<256, true>::THREADS);
+  cfg.blockDim = dim3(kind == 3 ? kOvThreads : kind == 2 ? kI8Threads : RingShape<256, true>::THREADS);
   cfg.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1357,10 +1835,13 @@ cudaError_t launch_umma(LaunchArgs& a, const void** kernel) {
   return a.dtype == GP_BF16_F32ACC_BF16OUT ? launch_dtype<true>(a, kernel) : launch_dtype<false>(a, kernel);
 }
 
-cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs) {
-  return max_pairs(dtype == GP_I8_I32 ? 2 : (dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0), smem_bytes, pairs);
+cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs, bool i8_overlap) {
+  const int kind = dtype == GP_I8_I32 ? (i8_overlap ? 3 : 2) : (dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0);
+  return max_pairs(kind, smem_bytes, pairs);
 }
 
-cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel) { return launch_i8(a, kernel); }
+cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel) {
+  return a.i8_overlap ? launch_i8_overlap(a, kernel) : launch_i8(a, kernel);
+}
 
 }  // namespace gp

@@ -180,7 +180,7 @@ def test_pair_tile_128_for_narrow_n(gp):
 
 @pytest.mark.parametrize("S,bn", [(1, 128), (4, 128), (6, 128), (7, 128), (8, 64)])
 def test_imma_tile_shrinks_with_stages(gp, S, bn):
-    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", i8_imma=True)
+    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", i8_engine="imma")
     assert p["kernel"] == "imma_ring" and p["cta_pair"] == 0
     assert p["bn"] == bn and p["bk"] == 128 and p["stage_bytes"] == (128 + bn) * 128
     assert p["k_tiles"] == 32 and p["smem_bytes"] <= 232448
@@ -204,16 +204,46 @@ def test_int8_on_tcgen05_plan(gp, S):
     assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", bn=128)["kernel"] == "imma_ring"
 
 
+@pytest.mark.parametrize("S", range(1, 7))
+def test_int8_overlap_engine_plan(gp, S):
+    # the two-pass engine's ring, tile and FP16 copies, in one 512-thread kernel that writes
+    # the copies itself through an int8 staging ring of 8 KB slots (as many as fit, up to 8,
+    # at least 2), with whole tiles only
+    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", i8_engine="tcgen05_overlap")
+    q = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", S, "pipelined", i8_engine="tcgen05_2pass")
+    assert q["kernel"] == "umma_i8_pair_ring" and q["threads"] == 320
+    if S == 6:   # no room left for staging: the two-pass engine runs
+        assert p == q
+        return
+    assert p["kernel"] == "umma_i8_overlap_pair_ring" and p["threads"] == 512 and p["sk_tiles"] == 0
+    for key in ("bm", "bn", "bk", "stages", "stage_bytes", "ring_bytes", "tmem_cols", "tiles", "grid", "cta_pair",
+                "compute_load_ratio", "workspace_bytes"):
+        assert p[key] == q[key], key
+    fixed = 1024 + 32768 + 256 + 384   # alignment slack, epilogue staging, ring and hand-off barriers
+    slots = min(8, (232448 - fixed - S * 32768) // 8192)
+    assert slots >= 2 and p["smem_bytes"] == max(fixed + S * 32768 + slots * 8192, 232448 // 2 + 1024) <= 232448
+    assert p["workspace_bytes"] == (4096 + 4096) * 4096 * 2
+    small = gp.gemm_plan(256, 256, 1024, "i8", "row_col", S, "pipelined", i8_engine="tcgen05_overlap")
+    assert small["sk_tiles"] == 0 and small["dp_tiles"] == 1
+    assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 7, "pipelined",
+                        i8_engine="tcgen05_overlap")["kernel"] == "imma_ring"
+
+
+def test_int8_overlap_default_depth(gp):
+    p = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined", i8_engine="tcgen05_overlap")
+    assert p["kernel"] == "umma_i8_overlap_pair_ring" and p["stages"] == 5
+
+
 def test_small_n_picks_narrow_tile(gp):
     assert gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 4, "pipelined")["bn"] == 128
     assert gp.gemm_plan(8192, 64, 8192, "bf16", "row_col", 4, "pipelined")["bn"] == 64
-    assert gp.gemm_plan(256, 100 + 4, 256, "i8", "row_col", 4, "pipelined", i8_imma=True)["bn"] == 128
+    assert gp.gemm_plan(256, 100 + 4, 256, "i8", "row_col", 4, "pipelined", i8_engine="imma")["bn"] == 128
 
 
 def test_default_stages_and_variant_stage_rules(gp):
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pipelined")["stages"] == 6
     assert gp.gemm_plan(512, 512, 512, "i8", "row_col", 0, "pipelined")["stages"] == 6
-    assert gp.gemm_plan(512, 512, 512, "i8", "row_col", 0, "pipelined", i8_imma=True)["stages"] == 4
+    assert gp.gemm_plan(512, 512, 512, "i8", "row_col", 0, "pipelined", i8_engine="imma")["stages"] == 4
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "pingpong")["stages"] == 2
     assert gp.gemm_plan(512, 512, 512, "f16", "row_col", 0, "nopipe")["stages"] == 1
     assert gp.gemm_plan(512, 512, 512, "f32", "row_row", 0, "pipelined")["stages"] == 3

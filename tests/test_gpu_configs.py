@@ -37,7 +37,7 @@ def test_i8_4096_bit_exact_every_stage_and_variant():
         C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
         assert torch.equal(C, ref)
     for S in w.stages:
-        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S, i8_imma=True)
+        C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S, i8_engine="imma")
         assert torch.equal(C, ref)
     for variant in ("pingpong", "nopipe"):
         C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant=variant)

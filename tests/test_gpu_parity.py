@@ -269,28 +269,65 @@ def test_cta_pair_128_kernel(dtype, M, N, K, S):
         assert diff <= 2.0 ** -6 * Cd.float().abs().max().item()
 
 
-@pytest.mark.parametrize("engine", ["tcgen05", "imma"])
+I8_KERNELS = {"tcgen05_2pass": "umma_i8_pair_ring", "tcgen05_overlap": "umma_i8_overlap_pair_ring",
+              "imma": "imma_ring"}
+
+
+@pytest.mark.parametrize("engine", sorted(I8_KERNELS))
 @pytest.mark.parametrize("stages", [1, 2, 4, 6])
 def test_int8_engines_every_depth(engine, stages):
     M, N, K = 520, 260, 1040 + 2048
     A, B = operands("i8", "row_col", M, N, K, seed=stages)
-    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined", stages=stages, i8_imma=(engine == "imma"))
-    assert st["plan"]["kernel"] == ("umma_i8_pair_ring" if engine == "tcgen05" else "imma_ring")
+    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined", stages=stages, i8_engine=engine)
+    too_deep = engine == "tcgen05_overlap" and stages == 6   # no room for int8 staging: two-pass runs
+    assert st["plan"]["kernel"] == I8_KERNELS["tcgen05_2pass" if too_deep else engine]
     check_full("i8", "row_col", A, B, C, K)
 
 
+@pytest.mark.parametrize("engine", ["tcgen05_2pass", "tcgen05_overlap"])
 @pytest.mark.parametrize("K", [16, 1008, 1024, 1040, 2048, 4096, 5136])
 @pytest.mark.parametrize("fill", [(-128, -128), (-128, 127), (127, 127)])
-def test_int8_tcgen05_exact_at_extremes(K, fill):
+def test_int8_tcgen05_exact_at_extremes(engine, K, fill):
     # every product at the int8 extremes: |partial sums| reach 2^24 inside one
     # 1024-element chunk of K and 2^26+ across chunks -- still bit-exact
     M, N = 300, 136
     A = np.full((M, K), fill[0], np.int8)
     B = np.full((N, K), fill[1], np.int8)
     A[::7, : K // 3] = 3
-    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined")
-    assert st["plan"]["kernel"] == "umma_i8_pair_ring"
+    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined", i8_engine=engine)
+    assert st["plan"]["kernel"] == I8_KERNELS[engine]
     check_full("i8", "row_col", A, B, C, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (1000, 3000, 2000), (256, 256, 16), (4104, 264, 1040)])
+def test_int8_overlapped_conversion_matches_two_pass(M, N, K):
+    # the same FP16 MMAs in the same order on the same exact values: identical int32 results
+    A, B = operands("i8", "row_col", M, N, K, seed=M ^ N ^ K)
+    C2, st2 = run("i8", "row_col", A, B, M, N, K, variant="pipelined", i8_engine="tcgen05_2pass",
+                  no_stream_k=True)
+    C3, st3 = run("i8", "row_col", A, B, M, N, K, variant="pipelined", i8_engine="tcgen05_overlap")
+    assert st3["plan"]["kernel"] == "umma_i8_overlap_pair_ring" and st3["plan"]["sk_tiles"] == 0
+    assert torch.equal(C2, C3)
+    if M * N * K <= 3e9:
+        check_full("i8", "row_col", A, B, C3, K)
+    else:
+        check_sampled("i8", "row_col", A, B, C3, K, rows=[0, 1, 255, 256, M - 1], npts=2000, seed=K)
+
+
+def test_int8_overlap_back_to_back_and_shape_changes():
+    # launches queued back to back on one stream share the copies and counters: the
+    # batch counter alternates between two words and every K-step count is epoch-tagged
+    shapes = [(1024, 768, 2048), (520, 260, 3088), (1024, 768, 2048), (256, 4096, 64)] * 3
+    ops = [operands("i8", "row_col", M, N, K, seed=i) for i, (M, N, K) in enumerate(shapes)]
+    tens = [(to_dev(A, "i8"), to_dev(B, "i8")) for A, B in ops]
+    outs = [torch.empty(M * N, dtype=torch.int32, device="cuda") for M, N, K in shapes]
+    for (M, N, K), (tA, tB), C in zip(shapes, tens, outs):
+        gp.gemm_pipelined(tA, tB, C, M, N, K, "i8", "row_col", 0, "pipelined", torch.cuda.current_stream(),
+                          i8_engine="tcgen05_overlap")
+    st = gp.gemm_stats(sync=True)
+    assert st["status"] == 0 and st["device_status"] == 0
+    for (M, N, K), (A, B), C in zip(shapes, ops, outs):
+        check_full("i8", "row_col", A, B, C.view(M, N).cpu(), K)
 
 
 @pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (500, 372, 1000), (256, 128, 4104), (130, 260, 2052)])

@@ -29,7 +29,7 @@ def _cases(dtype, n, seed):
         if dtype in ("f16", "bf16") and variant == "pipelined":
             opts = [{}, {"no_stream_k": True}, {"no_cta_pair": True}][int(rng.integers(0, 3))]
         if dtype == "i8" and variant == "pipelined" and rng.integers(0, 2):
-            opts = {"i8_imma": True}
+            opts = {"i8_engine": "imma"}
         if dtype == "f32" and variant == "pipelined" and rng.integers(0, 2):
             opts = {"ffma_tile": [(4, 8), (8, 4), (8, 16), (16, 8)][int(rng.integers(0, 4))]}
         out.append((M, N, K, variant, S, opts))
