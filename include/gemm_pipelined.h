@@ -127,6 +127,9 @@ typedef struct gp_plan {
     int32_t k_splits;            /* FP32 FFMA path: CTAs that share each tile's K-loop, when the tiles alone
                                     leave SMs idle (each writes a partial tile; the last to finish adds them in
                                     split order, so results do not depend on timing); 1 = whole K-loops */
+    int32_t half_tiles;          /* INT8 on tcgen05: the last tiles (after dp_tiles whole ones), each run as two
+                                    BM x BN/2 halves by two workers, when the whole tiles would leave a last
+                                    wave at most half full; 0 = none */
 } gp_plan;
 
 /* Record of the last gemm_pipelined call made by the calling host thread. */

@@ -50,7 +50,7 @@ class GpPlan(ctypes.Structure):
         ("grid", ctypes.c_int32), ("tiles", ctypes.c_int64), ("k_tiles", ctypes.c_int64),
         ("compute_load_ratio", ctypes.c_double), ("kernel", ctypes.c_char_p),
         ("dp_tiles", ctypes.c_int32), ("sk_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
-        ("cta_pair", ctypes.c_int32), ("k_splits", ctypes.c_int32),
+        ("cta_pair", ctypes.c_int32), ("k_splits", ctypes.c_int32), ("half_tiles", ctypes.c_int32),
     ]
 
     def as_dict(self):

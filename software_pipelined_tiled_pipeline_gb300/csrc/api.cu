@@ -300,6 +300,19 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
   p->workspace_bytes = static_cast<int64_t>(p->grid) * 2 * 128 * p->bn * 4;   // two 128 x BN FP32 slots per CTA
 }
 
+// INT8 on tcgen05 (two-pass engine), whole tiles over W workers: when the last
+// wave would hold r <= W/2 tiles, run those r tiles as 2r half tiles (BN/2
+// wide) on 2r workers instead -- the same MMAs split along N, so no partial
+// sums, and the last wave takes about half as long.
+void apply_i8_halves(gp_plan* p, int64_t workers) {
+  p->half_tiles = 0;
+  if (workers <= 0 || p->sk_tiles > 0 || p->tiles <= workers) return;
+  const int64_t r = p->tiles % workers;
+  if (r == 0 || 2 * r > workers) return;
+  p->half_tiles = static_cast<int32_t>(r);
+  p->dp_tiles = static_cast<int32_t>(p->tiles - r);
+}
+
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
               int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, int i8_engine = 0,
@@ -384,6 +397,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     // heavier int32 split epilogue measured slower than whole tiles.
     // (The overlap engine writes the same FP16 copies from inside the GEMM kernel; whole tiles only.)
     if (!overlap && sm_count > 1 && p->tiles < sm_count / 2) apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
+    if (!overlap && sm_count > 1) apply_i8_halves(p, sm_count / 2);
     p->workspace_bytes += i8_conv_bytes(M, N, K);   // FP16 copies of A and B, after the partial tiles
     // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B (FP16)
     p->compute_load_ratio = 2.0 * 128 * 256 * p->bk / ((128.0 + 128.0) * p->bk * 2.0);
@@ -676,7 +690,7 @@ using namespace gp;
 
 extern "C" {
 
-int gemm_abi_version(void) { return 10000; }
+int gemm_abi_version(void) { return 10100; }
 
 const char* gemm_strerror(int code) {
   switch (code) {
@@ -793,6 +807,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
         apply_stream_k(&plan, pairs, 2, !(opts && opts->no_stream_k));
         plan.workspace_bytes += conv_bytes;
       }
+      if (i8_tc && !i8_overlap) apply_i8_halves(&plan, pairs);
       if (i8_tc) {
         e = get_conv_workspace(dev, st, static_cast<size_t>(conv_bytes), &conv);
         if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }

@@ -765,16 +765,38 @@ __device__ __forceinline__ bool i8_epi_bar_and(bool pred) {   // the 8 epilogue 
   return r != 0;
 }
 
+// Work item of the INT8 pair kernel: items below half_from are whole 256 x 256
+// tiles (tile = item); each tile from half_from on is split along N into two
+// 256 x 128 items (the last partial wave of whole tiles would otherwise leave
+// most pairs idle: half tiles spread it over twice as many pairs, with no
+// partial sums to combine).
+struct I8Item {
+  int mb, n0;     // 256-row block; first column
+  bool half;      // 128 columns instead of 256
+  __device__ __forceinline__ void decode(int item, int half_from, int m_blocks, int n_blocks) {
+    int tile = item, hs = 0;
+    half = item >= half_from;
+    if (half) {
+      tile = half_from + (item - half_from) / 2;
+      hs = (item - half_from) & 1;
+    }
+    int nb;
+    tile_coords(tile, m_blocks, n_blocks, mb, nb);
+    n0 = nb * 256 + hs * 128;
+  }
+};
+
 template <bool PAIR>
 __global__ void __launch_bounds__(kI8Threads, 1)
     umma_i8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl,
-                   SkParams sk) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmBh, int M, int N,
+                   int K, int stages, KernelCtl ctl, SkParams sk, int half_from) {
   constexpr int BN = 256;
   constexpr int HALF = BN / 2;   // columns per epilogue thread
   using Sh = RingShape<BN, PAIR>;
   constexpr int STAGE = Sh::STAGE;
   constexpr uint32_t IDESC = umma_idesc_f16(false, Sh::TILE_M, BN);
+  constexpr uint32_t IDESC_HALF = umma_idesc_f16(false, Sh::TILE_M, BN / 2);
   static_assert(kI8EpiWarps * kUmmaEpiBufBytes <= kUmmaEpiBytes, "staging region too small");
 
   extern __shared__ uint8_t smem_raw[];
@@ -839,18 +861,20 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       int s = 0;
       uint32_t ph = 0;
       while (!cta->abort && it.next(tile, k0, k1)) {
-        int mb, nb;
-        tile_coords(tile, m_blocks, n_blocks, mb, nb);
-        const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
-        const int n_row = nb * BN + rank * Sh::B_ROWS;
+        I8Item w;
+        w.decode(tile, half_from, m_blocks, n_blocks);
+        const int m_row = w.mb * Sh::TILE_M + rank * Sh::A_ROWS;
+        // a half item: each CTA of the pair loads 64 of its 128 B rows
+        const int n_row = w.n0 + rank * (w.half ? Sh::B_ROWS / 2 : Sh::B_ROWS);
+        const uint32_t tx_bytes = w.half ? 2 * (Sh::A_ROWS + Sh::B_ROWS / 2) * BK * 2 : 2 * STAGE;
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto i8_producer_done;
           uint8_t* slot = ring + s * STAGE;
           if (PAIR) {
-            if (leader) mbar_arrive_expect_tx(&bar->full[s], 2 * STAGE);
+            if (leader) mbar_arrive_expect_tx(&bar->full[s], tx_bytes);
             const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), 0);
             tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
-            tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
+            tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), w.half ? &tmBh : &tmB, full_leader, kb * BK, n_row);
           } else {
             mbar_arrive_expect_tx(&bar->full[s], STAGE);
             tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, m_row);
@@ -871,6 +895,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       int t = 0;
       bool ok = true;
       while (ok && it.next(tile, k0, k1)) {
+        const uint32_t idesc = (PAIR && tile >= half_from) ? IDESC_HALF : IDESC;   // N = 128 for a half item
         // chunks of at most kI8ChunkSteps K steps from k0: each FP32 sum stays exact
         for (int kb0 = k0; kb0 < k1 && ok; kb0 += kI8ChunkSteps, ++t) {
           const int a = t & 1;
@@ -888,7 +913,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
             for (int kk = 0; kk < BK / UMMA_K; ++kk) {
               const uint32_t acc = (kb == kb0 && kk == 0) ? 0u : 1u;
               if (PAIR)
-                umma_f16_pair(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
+                umma_f16_pair(d, da + 2 * kk, db + 2 * kk, idesc, acc);
               else
                 umma_f16(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
             }
@@ -915,8 +940,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     int t = 0;
     bool ok = true;
     while (ok && it.next(tile, k0, k1)) {
-      int mb, nb;
-      tile_coords(tile, m_blocks, n_blocks, mb, nb);
+      I8Item wi;
+      wi.decode(tile, half_from, m_blocks, n_blocks);
+      const int mb = wi.mb;
+      const int cols = wi.half ? HALF / 2 : HALF;   // accumulator columns of this thread
       // A split tile (stream-K): each segment's int32 partial is exact, so the
       // order in which the segments are added does not change the result.
       const bool split = (k0 > 0) || (k1 < kt);
@@ -930,9 +957,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
         w = __shfl_sync(0xffffffffu, w, 0);
         if (!i8_epi_bar_and(w != 0 && !cta->abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN + h * HALF;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN + h * cols;
 #pragma unroll
         for (int sub = 0; sub < HALF / 16; ++sub) {   // 16 columns at a time: sum[] holds 128 registers
+          if (sub * 16 >= cols) break;
           uint32_t v[16];
           tmem_ld_32x32b_x16(trow + sub * 16, v);
           tmem_wait_ld();
@@ -999,9 +1027,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
 #pragma unroll
       for (int sub = 0; sub < HALF / 32; ++sub) {
+        if (sub * 32 >= cols) break;
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        const int x = nb * BN + h * HALF + sub * 32;
+        const int x = wi.n0 + h * cols + sub * 32;
         stage_and_store_i32(sum + sub * 32, my_stage, lane, &tmC, x, y, (x < N) && (y < M));
       }
     }
@@ -1716,6 +1745,10 @@ cudaError_t launch_i8(LaunchArgs& a, const void** kernel) {
   if ((e = make_tmap_2d(&tmB, b16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, N, K * 2, BK, Sh::B_ROWS,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
+  CUtensorMap tmBh;   // half items: 64 of a CTA's B rows per box
+  if ((e = make_tmap_2d(&tmBh, b16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, N, K * 2, BK, Sh::B_ROWS / 2,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
   auto k = umma_i8_kernel<true>;
   *kernel = reinterpret_cast<const void*>(k);
   if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
@@ -1733,7 +1766,11 @@ cudaError_t launch_i8(LaunchArgs& a, const void** kernel) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, a.M, a.N, a.K, p.stages, a.ctl, a.sk);
+  // work items: the whole tiles, then two half items per tile of the N-split tail
+  const int half_from = static_cast<int>(p.tiles - p.half_tiles);
+  SkParams sk = a.sk;
+  if (p.half_tiles > 0) sk.dp_tiles = static_cast<int32_t>(p.tiles + p.half_tiles);
+  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmC, tmBh, a.M, a.N, a.K, p.stages, a.ctl, sk, half_from);
 }
 
 // INT8 on tcgen05, the conversion overlapped inside the GEMM kernel: one launch.

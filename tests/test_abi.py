@@ -44,17 +44,38 @@ def test_library_exports_every_declared_function(gp):
 
 
 def test_version_and_strerror(gp):
-    assert gp.abi_version() == 10000
+    assert gp.abi_version() == 10100
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert gp.strerror(code) and "unknown" not in gp.strerror(code)
     assert "unknown" in gp.strerror(-99)
 
 
-def test_struct_sizes_match_c_layout():
+def test_struct_sizes_match_c_layout(tmp_path):
+    # the ctypes mirrors against the header as a C compiler lays it out (sizes and field offsets)
+    import shutil
+    import subprocess
     from software_pipelined_tiled_pipeline_gb300 import _binding as b
-    assert ctypes.sizeof(b.GpPlan) == 112
-    assert ctypes.sizeof(b.GpStats) == 144
-    assert ctypes.sizeof(b.GpOptions) == 40
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    include = os.path.join(ROOT, "include")
+    src = tmp_path / "sizes.c"
+    checks = [("gp_plan", b.GpPlan), ("gp_stats", b.GpStats), ("gp_options", b.GpOptions)]
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "gemm_pipelined.h"', "int main(void) {"]
+    for cname, cls in checks:
+        lines.append('  printf("%%s %%zu\\n", "%s", sizeof(%s));' % (cname, cname))
+        for f, _ in cls._fields_:
+            lines.append('  printf("%%s.%%s %%zu\\n", "%s", "%s", offsetof(%s, %s));' % (cname, f, cname, f))
+    lines.append("  return 0;\n}")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "sizes"
+    subprocess.run([cc, "-I", include, str(src), "-o", str(exe)], check=True)
+    out = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                          text=True).stdout.splitlines())
+    for cname, cls in checks:
+        assert int(out[cname]) == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert int(out["%s.%s" % (cname, f)]) == getattr(cls, f).offset, (cname, f)
 
 
 @pytest.mark.parametrize("args,code", [

@@ -299,6 +299,26 @@ def test_int8_tcgen05_exact_at_extremes(engine, K, fill):
     check_full("i8", "row_col", A, B, C, K)
 
 
+@pytest.mark.parametrize("M,N,K", [(1280, 4096, 528), (1240, 3976, 528), (4096, 4096, 1024)])
+def test_int8_half_tiles_in_the_last_wave(M, N, K):
+    # when the whole 256 x 256 tiles leave a last wave at most half full, those tiles run as
+    # two 256 x 128 halves on two pairs: exact, and identical to the IMMA engine's result
+    A, B = operands("i8", "row_col", M, N, K, seed=M + N + K)
+    C, st = run("i8", "row_col", A, B, M, N, K, variant="pipelined", i8_engine="tcgen05_2pass")
+    p = st["plan"]
+    W = p["grid"] // 2
+    r = p["tiles"] % W
+    expect = r if (p["tiles"] > W and 0 < 2 * r <= W) else 0
+    assert p["kernel"] == "umma_i8_pair_ring" and p["sk_tiles"] == 0
+    assert p["half_tiles"] == expect and p["dp_tiles"] == p["tiles"] - expect
+    if M * N * K <= 3e9:
+        check_full("i8", "row_col", A, B, C, K)
+    else:
+        check_sampled("i8", "row_col", A, B, C, K, rows=[0, 1, 255, 256, 2049, M - 1], npts=3000, seed=K)
+    C2, st2 = run("i8", "row_col", A, B, M, N, K, variant="pipelined", i8_engine="imma")
+    assert torch.equal(C, C2)
+
+
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (1000, 3000, 2000), (256, 256, 16), (4104, 264, 1040)])
 def test_int8_overlapped_conversion_matches_two_pass(M, N, K):
     # the same FP16 MMAs in the same order on the same exact values: identical int32 results
