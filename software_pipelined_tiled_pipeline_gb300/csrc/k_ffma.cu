@@ -169,32 +169,55 @@ __device__ __forceinline__ bool compute_bar_and(bool pred) {
 }
 
 // Work of CTA b: tile b % tiles, K steps [kb_begin, kb_end) of split b / tiles.
+// Work of one CTA.  The tiles' K-loops are laid end to end (unit u: tile
+// u / kt, K step u % kt) and dealt out to the G CTAs of the grid as equal
+// contiguous ranges.  With G = tiles every CTA gets one whole tile; with more
+// CTAs than tiles every tile's K-loop is shared by the CTAs whose ranges meet
+// it, and a range (shorter than a K-loop) meets at most two tiles: its
+// segment 0 (in its first tile) and segment 1.
 struct FfmaWork {
-  int tile, split, kb_begin, kb_end;
-  __device__ __forceinline__ FfmaWork(int tiles, int kt, int splits) {
-    tile = static_cast<int>(blockIdx.x) % tiles;
-    split = static_cast<int>(blockIdx.x) / tiles;
-    kb_begin = static_cast<int>(static_cast<int64_t>(kt) * split / splits);
-    kb_end = static_cast<int>(static_cast<int64_t>(kt) * (split + 1) / splits);
+  int64_t U, u, u_end;
+  int kt, G;
+  __device__ __forceinline__ FfmaWork(int tiles, int kt_) {
+    kt = kt_;
+    G = static_cast<int>(gridDim.x);
+    U = static_cast<int64_t>(tiles) * kt;
+    u = start(blockIdx.x);
+    u_end = start(blockIdx.x + 1);
+  }
+  __device__ __forceinline__ int64_t start(int64_t c) const { return c * U / G; }
+  // CTA whose range holds unit v
+  __device__ __forceinline__ int owner(int64_t v) const { return static_cast<int>(((v + 1) * G - 1) / U); }
+  // next segment of this CTA: tile, K steps [k0, k1), and its index (0 or 1) among this CTA's segments
+  __device__ __forceinline__ bool next(int& tile, int& k0, int& k1, int& seg) {
+    if (u >= u_end) return false;
+    tile = static_cast<int>(u / kt);
+    k0 = static_cast<int>(u - static_cast<int64_t>(tile) * kt);
+    k1 = (u_end - u < kt - k0) ? k0 + static_cast<int>(u_end - u) : kt;
+    seg = (tile == static_cast<int>(start(blockIdx.x) / kt)) ? 0 : 1;
+    u += k1 - k0;
+    return true;
   }
 };
 
-// Write the accumulator: to C, or -- K-loop split over several CTAs -- as a
-// partial tile; the CTA whose partial completes the tile adds all of them in
-// split order (so the sum does not depend on which CTA finished last) and
-// writes C.  Called by all compute threads (tid < THREADS).
+// Write the accumulator of one segment: to C when the segment is the whole
+// K-loop, else as a partial tile (slot 2 * CTA + segment); the CTA whose
+// partial completes the tile adds all of them in K order (so the sum does not
+// depend on which CTA finished last) and writes C.  Called by all compute
+// threads (tid < THREADS); acc is consumed (it holds the sum afterwards).
 template <int TM, int TN>
-__device__ __forceinline__ void ffma_finish(float* C, int M, int N, int m0, int n0, const FfmaWork& w,
-                                            const FfmaSplit& ks, int tx, int ty, int tid, const Acc<TM, TN>& acc,
-                                            int32_t* last) {
+__device__ __forceinline__ void ffma_finish(float* C, int M, int N, int m0, int n0, const FfmaWork& w, int tile,
+                                            int seg, const FfmaSplit& ks, int tx, int ty, int tid,
+                                            Acc<TM, TN>& acc, int32_t* last) {
   using T = Tile<TM, TN>;
-  if (ks.splits <= 1) {
+  const int64_t t0 = static_cast<int64_t>(tile) * w.kt;
+  const int c_first = w.owner(t0), c_last = w.owner(t0 + w.kt - 1);
+  if (c_first == c_last) {
     ffma_store<TM, TN>(C, M, N, m0, n0, tx, ty, acc);
     return;
   }
   constexpr int TILE = BM * BN;
-  float* base = ks.workspace + static_cast<size_t>(w.tile) * ks.splits * TILE;
-  float* mine = base + static_cast<size_t>(w.split) * TILE;
+  float* mine = ks.workspace + (2 * static_cast<size_t>(blockIdx.x) + seg) * TILE;
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -204,35 +227,48 @@ __device__ __forceinline__ void ffma_finish(float* C, int M, int N, int m0, int 
   compute_bar<T::THREADS>();
   if (tid == 0) {
     __threadfence();
-    *last = (epoch_count_in(ks.counters + w.tile, ks.epoch) + 1u == static_cast<uint32_t>(ks.splits)) ? 1 : 0;
+    *last = (epoch_count_in(ks.counters + tile, ks.epoch) + 1u == static_cast<uint32_t>(c_last - c_first + 1)) ? 1
+                                                                                                              : 0;
     __threadfence();
   }
   compute_bar<T::THREADS>();
   if (!*last) return;
+  // the partials in K order, CTA c_first's segment first, summed in place of
+  // this CTA's accumulator (already stored above)
+  Acc<TM, TN>& tot = acc;
+  for (int c = c_first; c <= c_last; ++c) {
+    // the tile is segment 0 of CTA c if c's range starts in it, else its segment 1
+    const int sc = (w.start(c) / w.kt == tile) ? 0 : 1;
+    const float* src = ks.workspace + (2 * static_cast<size_t>(c) + sc) * TILE;
 #pragma unroll
-  for (int i = 0; i < TM; ++i) {
-    const int r = ty + T::TY * i;
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int g = 0; g < T::NG; ++g) {
-      const int off = r * BN + g * T::GSTRIDE + tx * 4;
-      float4 sum = __ldcg(reinterpret_cast<const float4*>(base + off));
-      for (int j = 1; j < ks.splits; ++j) {
-        const float4 p = __ldcg(reinterpret_cast<const float4*>(base + static_cast<size_t>(j) * TILE + off));
-        sum.x += p.x;
-        sum.y += p.y;
-        sum.z += p.z;
-        sum.w += p.w;
+      for (int g = 0; g < T::NG; ++g) {
+        const float4 p = __ldcg(reinterpret_cast<const float4*>(src + (ty + T::TY * i) * BN + g * T::GSTRIDE + tx * 4));
+        float* d = &tot.c[i][4 * g];
+        if (c == c_first) {
+          d[0] = p.x;
+          d[1] = p.y;
+          d[2] = p.z;
+          d[3] = p.w;
+        } else {
+          d[0] += p.x;
+          d[1] += p.y;
+          d[2] += p.z;
+          d[3] += p.w;
+        }
       }
-      const int gr = m0 + r, gc = n0 + g * T::GSTRIDE + tx * 4;
-      if (gr < M && gc < N) *reinterpret_cast<float4*>(C + static_cast<size_t>(gr) * N + gc) = sum;
-    }
   }
+  ffma_store<TM, TN>(C, M, N, m0, n0, tx, ty, tot);
 }
 
 // ---------------------------------------------------------------------------
 // TMA ring: compute warps + 1 producer warp, one (tile, K split) per CTA
 // ---------------------------------------------------------------------------
-template <int TM, int TN>
+// SPLIT: some tile's K-loop is shared by several CTAs (else each CTA runs one
+// whole tile and stores it directly; a separate instantiation keeps the
+// fix-up code out of that kernel).
+template <int TM, int TN, bool SPLIT>
 __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
     ffma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      float* __restrict__ C, int M, int N, int K, int stages, KernelCtl ctl, FfmaSplit ks) {
@@ -244,9 +280,7 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
   const int kt = (K + BK - 1) / BK;
-  const FfmaWork wk(m_blocks * n_blocks, kt, ks.splits > 1 ? ks.splits : 1);
-  int mb, nb;
-  tile_coords(wk.tile, m_blocks, n_blocks, mb, nb);
+  const int tiles = m_blocks * n_blocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -260,6 +294,8 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
   __syncthreads();
   CtaCtl* cta = &bar->ctl;
   int issued = 0;
+  FfmaWork wk(tiles, kt);
+  int tile, k0, k1, seg;
 
   if (warp == T::WARPS) {
     if (lane == 0) {
@@ -267,40 +303,54 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
       tma_prefetch_desc(&tmB);
       int s = 0;
       uint32_t ph = 0;
-      const bool last_tile = blockIdx.x == gridDim.x - 1;
-      for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
-        if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) break;
-        if (!(ctl.inject_lost_load && last_tile && kb == wk.kb_end - 1)) {
-          uint8_t* slot = ring + s * STAGE;
-          mbar_arrive_expect_tx(&bar->full[s], STAGE);
-          tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, mb * BM);
-          tma_load_2d(smem_u32(slot + A_FLOATS * 4), &tmB, &bar->full[s], nb * BN, kb * BK);
-          ++issued;
+      const bool last_cta = blockIdx.x == gridDim.x - 1;
+      bool ok = true;
+      while (ok && wk.next(tile, k0, k1, seg)) {
+        int mb, nb;
+        tile_coords(tile, m_blocks, n_blocks, mb, nb);
+        for (int kb = k0; kb < k1; ++kb) {
+          if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) { ok = false; break; }
+          if (!(ctl.inject_lost_load && last_cta && wk.u >= wk.u_end && kb == k1 - 1)) {
+            uint8_t* slot = ring + s * STAGE;
+            mbar_arrive_expect_tx(&bar->full[s], STAGE);
+            tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, mb * BM);
+            tma_load_2d(smem_u32(slot + A_FLOATS * 4), &tmB, &bar->full[s], nb * BN, kb * BK);
+            ++issued;
+          }
+          if (++s == stages) { s = 0; ph ^= 1u; }
         }
-        if (++s == stages) { s = 0; ph ^= 1u; }
       }
     }
   } else {
     const int tx = threadIdx.x % T::TX, ty = threadIdx.x / T::TX;
-    Acc<TM, TN> acc;
-    acc.zero();
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
     int consumed = 0;
-    for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
-      const bool w = mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      const float* As = reinterpret_cast<const float*>(ring + s * STAGE);
-      ffma_kblock<TM, TN>(As, As + A_FLOATS, tx, ty, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar->empty[s]);
-      ++consumed;
-      if (++s == stages) { s = 0; ph ^= 1u; }
+    while (ok && wk.next(tile, k0, k1, seg)) {
+      int mb, nb;
+      tile_coords(tile, m_blocks, n_blocks, mb, nb);
+      Acc<TM, TN> acc;
+      acc.zero();
+      for (int kb = k0; kb < k1; ++kb) {
+        const bool w = mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        const float* As = reinterpret_cast<const float*>(ring + s * STAGE);
+        ffma_kblock<TM, TN>(As, As + A_FLOATS, tx, ty, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->empty[s]);
+        ++consumed;
+        if (++s == stages) { s = 0; ph ^= 1u; }
+      }
+      // one decision for all compute warps: a timed-out warp must not leave the others at a barrier
+      ok = compute_bar_and<T::THREADS>(ok);
+      if (ok) {
+        if (SPLIT)
+          ffma_finish<TM, TN>(C, M, N, mb * BM, nb * BN, wk, tile, seg, ks, tx, ty, threadIdx.x, acc, &bar->last);
+        else
+          ffma_store<TM, TN>(C, M, N, mb * BM, nb * BN, tx, ty, acc);
+      }
     }
-    // one decision for all compute warps: a timed-out warp must not leave the others at a barrier
-    if (compute_bar_and<T::THREADS>(ok))
-      ffma_finish<TM, TN>(C, M, N, mb * BM, nb * BN, wk, ks, tx, ty, threadIdx.x, acc, &bar->last);
     if (threadIdx.x == 0) bar->consumed = consumed;
   }
 
@@ -350,46 +400,46 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
   uint8_t* ring = align1024(smem_raw);
   const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
   const int kt = (K + BK - 1) / BK;
-  const FfmaWork wk(m_blocks * n_blocks, kt, ks.splits > 1 ? ks.splits : 1);
-  int mb, nb;
-  tile_coords(wk.tile, m_blocks, n_blocks, mb, nb);
-  const int m0 = mb * BM, n0 = nb * BN;
   const int tx = threadIdx.x % T::TX, ty = threadIdx.x / T::TX;
-
-  Acc<8, 8> acc;
-  acc.zero();
-  RegStage rs;
-  if (PINGPONG) {
-    if (wk.kb_begin < wk.kb_end) {
-      rs.load(A, B, M, N, K, m0, n0, wk.kb_begin);
-      rs.store(ring);
-    }
-    __syncthreads();
-    for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
-      const int cur = (kb - wk.kb_begin) & 1;
-      if (kb + 1 < wk.kb_end) rs.load(A, B, M, N, K, m0, n0, kb + 1);   // in flight during the compute
-      const float* As = reinterpret_cast<const float*>(ring + cur * STAGE);
-      ffma_kblock<8, 8>(As, As + A_FLOATS, tx, ty, acc);
-      if (kb + 1 < wk.kb_end) rs.store(ring + (cur ^ 1) * STAGE);   // last read in iteration kb-1
-      __syncthreads();
-    }
-  } else {
-    for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
-      rs.load(A, B, M, N, K, m0, n0, kb);
+  FfmaWork wk(m_blocks * n_blocks, kt);
+  int tile, k0, k1, seg;
+  while (wk.next(tile, k0, k1, seg)) {
+    int mb, nb;
+    tile_coords(tile, m_blocks, n_blocks, mb, nb);
+    const int m0 = mb * BM, n0 = nb * BN;
+    Acc<8, 8> acc;
+    acc.zero();
+    RegStage rs;
+    if (PINGPONG) {
+      rs.load(A, B, M, N, K, m0, n0, k0);
       rs.store(ring);
       __syncthreads();
-      const float* As = reinterpret_cast<const float*>(ring);
-      ffma_kblock<8, 8>(As, As + A_FLOATS, tx, ty, acc);
-      __syncthreads();
+      for (int kb = k0; kb < k1; ++kb) {
+        const int cur = (kb - k0) & 1;
+        if (kb + 1 < k1) rs.load(A, B, M, N, K, m0, n0, kb + 1);   // in flight during the compute
+        const float* As = reinterpret_cast<const float*>(ring + cur * STAGE);
+        ffma_kblock<8, 8>(As, As + A_FLOATS, tx, ty, acc);
+        if (kb + 1 < k1) rs.store(ring + (cur ^ 1) * STAGE);   // last read in iteration kb-1
+        __syncthreads();
+      }
+    } else {
+      for (int kb = k0; kb < k1; ++kb) {
+        rs.load(A, B, M, N, K, m0, n0, kb);
+        rs.store(ring);
+        __syncthreads();
+        const float* As = reinterpret_cast<const float*>(ring);
+        ffma_kblock<8, 8>(As, As + A_FLOATS, tx, ty, acc);
+        __syncthreads();
+      }
     }
+    ffma_finish<8, 8>(C, M, N, m0, n0, wk, tile, seg, ks, tx, ty, threadIdx.x, acc, &last);
   }
-  ffma_finish<8, 8>(C, M, N, m0, n0, wk, ks, tx, ty, threadIdx.x, acc, &last);
 }
 
 template <int TM, int TN>
 cudaError_t launch_ring_tile(LaunchArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, const void** kernel) {
   const gp_plan& p = a.plan;
-  auto k = ffma_ring_kernel<TM, TN>;
+  auto k = p.k_splits > 1 ? ffma_ring_kernel<TM, TN, true> : ffma_ring_kernel<TM, TN, false>;
   *kernel = reinterpret_cast<const void*>(k);
   cudaError_t e = ensure_smem_attr(*kernel, p.smem_bytes);
   if (e != cudaSuccess) return e;
