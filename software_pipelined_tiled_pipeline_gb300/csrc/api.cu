@@ -362,7 +362,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   const int i8_tc_stages = stages == 0 ? 6 : S;
   if (fam == 1 && ring && i8_engine != 1 && !no_pair && (bn_req == 0 || bn_req == 256) &&
       ring_smem_total(i8_tc_stages * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax) {
-    // INT8 on tcgen05: FP16 operands, CTA pair per 256 x 256 tile, whole tiles.
+    // INT8 on tcgen05: FP16 operands, CTA pair per 256 x 256 tile.
     // Deeper rings than this tile allows (7, 8 stages) run on the IMMA ring.
     // The overlap engine numbers its conversion units (K step x 128-row panel) in 31 bits.
     const int64_t conv_units = ceil_div(K, kUmmaBK) * (ceil_div(M, 128) + ceil_div(N, 128));
