@@ -676,7 +676,9 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
 // definition does).  The operands are converted to FP16 in global memory first
 // (i8_to_f16_kernel): converting inside the ring would triple the
 // shared-memory traffic per MMA.  Tile: 256 x 256 per CTA pair (each CTA
-// 128 rows of A and 128 of B, as for FP16), whole tiles only.
+// 128 rows of A and 128 of B, as for FP16); a last wave at most half full
+// runs as 256 x 128 half tiles (I8Item), and K-loops are split (stream-K,
+// exact int32 partials) only when the tiles do not fill one wave.
 constexpr int kI8ChunkSteps = 1024 / BK;   // 16 K steps of 64
 
 // Four int8 values (one 32-bit word) to four FP16 values, exactly.  With the
