@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -333,12 +334,21 @@ def ffma_tile_sweep(torch, gp, dev, stream, steps=10):
     return {"workload": "f32_4096", "stages": 3, "rows": rows}
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace collapsed: edits to comments do not
+    make a recorded capture stale, edits to code do."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_sha(name):
-    path = os.path.join(ROOT, "software_pipelined_tiled_pipeline_gb300", "csrc", name)
+    """Hash of the code of a kernel source file and the device headers it includes."""
+    csrc = os.path.join(ROOT, "software_pipelined_tiled_pipeline_gb300", "csrc")
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "software_pipelined_tiled_pipeline_gb300", "csrc", "gp_device.cuh")):
-        with open(p, "rb") as f:
-            h.update(f.read())
+    for p in (name, "gp_device.cuh", "gp_internal.h"):
+        with open(os.path.join(csrc, p)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

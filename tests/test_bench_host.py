@@ -94,3 +94,24 @@ def test_replicas_take_the_slowest_rank_gloo(tmp_path):
 
 def test_single_process_needs_no_group():
     assert bench.max_over_ranks(torch, None, 7.5, "cpu") == 7.5
+
+
+def test_capture_records_follow_code_not_comments():
+    # a recorded ncu capture stays valid across comment edits and goes stale on code edits
+    src = "int f(int x) {  // twice\n  return 2 * x; /* doubled */\n}\n"
+    same = "int f(int x) {\n  // a new remark\n  return 2 * x;\n}\n"
+    other = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+
+
+def test_traffic_records_are_well_formed():
+    # every committed DRAM-traffic record carries its read and write bytes and the hash of the
+    # kernel code it was taken on (the bench reports the traffic only while that hash matches)
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles", "traffic.json")
+    records = json.load(open(path))
+    assert records
+    for key, rec in records.items():
+        assert rec["dram_bytes_per_launch"] == rec["dram_read"] + rec["dram_write"] > 0, key
+        assert len(rec["source_sha"]) == 16 and int(rec["source_sha"], 16) >= 0, key
+        assert os.path.exists(os.path.join(os.path.dirname(path), os.path.basename(rec["capture"]))), key
