@@ -161,6 +161,9 @@ typedef struct gp_options {
                                     engine gives the same exact int32 results; other values: GP_ERR_ARG */
     int32_t ffma_tm, ffma_tn;    /* FP32, GP_PIPELINED: outputs per thread, rows x columns (0, 0 = 8 x 8);
                                     built: 4x8, 8x4, 8x8, 8x16, 16x8, 16x16 (else GP_ERR_UNSUPPORTED) */
+    int32_t plan_sms;            /* gemm_plan_ex only: plan for a device with this many SMs instead of the
+                                    current one, all of them available (0 = query the current device); a
+                                    launch always plans for the device it runs on */
 } gp_options;
 
 /*

@@ -77,6 +77,7 @@ class GpOptions(ctypes.Structure):
         ("bn", ctypes.c_int32), ("time_kernel", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
         ("inject_lost_load", ctypes.c_int32), ("no_stream_k", ctypes.c_int32), ("no_cta_pair", ctypes.c_int32),
         ("i8_engine", ctypes.c_int32), ("ffma_tm", ctypes.c_int32), ("ffma_tn", ctypes.c_int32),
+        ("plan_sms", ctypes.c_int32),
     ]
 
 
@@ -148,7 +149,7 @@ I8_ENGINES = {"default": 0, "imma": 1, "tcgen05_2pass": 2, "tcgen05_overlap": 3}
 
 
 def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-             ffma_tile=None, i8_engine=0):
+             ffma_tile=None, i8_engine=0, plan_sms=0):
     opts = GpOptions()
     opts.bn = int(bn)
     opts.time_kernel = 1 if time_kernel else 0
@@ -159,6 +160,7 @@ def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_s
     opts.i8_engine = _enum(i8_engine, I8_ENGINES, "i8_engine")
     if ffma_tile:
         opts.ffma_tm, opts.ffma_tn = int(ffma_tile[0]), int(ffma_tile[1])
+    opts.plan_sms = int(plan_sms)
     return opts
 
 

@@ -694,7 +694,7 @@ using namespace gp;
 
 extern "C" {
 
-int gemm_abi_version(void) { return 10100; }
+int gemm_abi_version(void) { return 10200; }
 
 const char* gemm_strerror(int code) {
   switch (code) {
@@ -727,9 +727,12 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
 int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant,
                  const gp_options* opts, gp_plan* out) {
   if (!out) return GP_ERR_ARG;
+  if (opts && opts->plan_sms < 0) return GP_ERR_ARG;
   int sms = 0;
   int ndev = 0;
-  if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+  if (opts && opts->plan_sms > 0) {
+    sms = opts->plan_sms;
+  } else if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   } else {

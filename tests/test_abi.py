@@ -44,7 +44,7 @@ def test_library_exports_every_declared_function(gp):
 
 
 def test_version_and_strerror(gp):
-    assert gp.abi_version() == 10100
+    assert gp.abi_version() == 10200
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert gp.strerror(code) and "unknown" not in gp.strerror(code)
     assert "unknown" in gp.strerror(-99)
@@ -313,3 +313,46 @@ def test_double_buffer_rule_matches_published_example():
     g = json.load(open(os.path.join(GOLDEN, "p2_smem_budget.json")))
     # single buffer 2 KB + 2 KB -> doubled 8 KB
     assert 2 * g["single_buffer_kb"] == g["double_buffer_kb"]
+
+
+def test_planner_for_a_152_sm_gb300(gp):
+    # the launch-time decisions, planned for a GB300's 152 SMs (76 CTA pairs) without a device
+    kw = dict(plan_sms=152)
+    f16 = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", **kw)
+    # 256 tiles on 76 pairs: two whole waves, the last 104 tiles' K-loops split evenly (stream-K)
+    assert (f16["kernel"], f16["stages"], f16["bn"], f16["grid"]) == ("umma_pair_ring", 5, 256, 152)
+    assert (f16["tiles"], f16["dp_tiles"], f16["sk_tiles"]) == (256, 152, 104)
+    assert f16["workspace_bytes"] == 152 * 2 * 128 * 256 * 4
+    i8 = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined", **kw)
+    # three whole waves, then the 28 tiles left over as 56 half tiles on 56 pairs
+    assert (i8["kernel"], i8["stages"], i8["grid"], i8["sk_tiles"]) == ("umma_i8_pair_ring", 6, 152, 0)
+    assert (i8["dp_tiles"], i8["half_tiles"]) == (228, 28)
+    assert i8["workspace_bytes"] == (4096 + 4096) * 4096 * 2
+    few = gp.gemm_plan(768, 2048, 8192, "i8", "row_col", 0, "pipelined", **kw)
+    # 24 tiles do not fill one wave: every K-loop is split over the 76 pairs, exact int32 partials
+    assert (few["dp_tiles"], few["sk_tiles"], few["half_tiles"], few["grid"]) == (0, 24, 0, 152)
+    assert few["workspace_bytes"] == 152 * 2 * 128 * 256 * 4 + (768 + 2048) * 8192 * 2
+    full = gp.gemm_plan(256 * 76, 256, 1024, "i8", "row_col", 0, "pipelined", **kw)
+    assert (full["tiles"], full["dp_tiles"], full["sk_tiles"], full["half_tiles"]) == (76, 76, 0, 0)
+    many = gp.gemm_plan(4096, 4096 + 2048, 1024, "i8", "row_col", 0, "pipelined", **kw)
+    # 384 tiles leave 4 for a last wave: 8 half tiles
+    assert (many["tiles"], many["dp_tiles"], many["half_tiles"]) == (384, 380, 4)
+    over = gp.gemm_plan(4096, 4096 + 4096 + 2048, 1024, "i8", "row_col", 0, "pipelined", **kw)
+    # 640 tiles leave 32 (at most 38) for a last wave
+    assert (over["tiles"], over["half_tiles"]) == (640, 32)
+    wide = gp.gemm_plan(4096, 4096 + 7 * 256, 1024, "i8", "row_col", 0, "pipelined", **kw)
+    # 368 tiles leave 64 (more than half a wave): whole tiles only
+    assert (wide["tiles"], wide["half_tiles"], wide["sk_tiles"]) == (368, 0, 0)
+    f32 = gp.gemm_plan(1024, 1024, 1024, "f32", "row_row", 0, "pipelined", **kw)
+    # 64 tiles: each K-loop shared by two CTAs (128 CTAs), two partial slots per CTA
+    assert (f32["tiles"], f32["k_splits"], f32["grid"]) == (64, 2, 128)
+    assert f32["workspace_bytes"] == 2 * 128 * 128 * 128 * 4
+    f32_big = gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 0, "pipelined", **kw)
+    assert (f32_big["k_splits"], f32_big["grid"], f32_big["workspace_bytes"]) == (1, 1024, 0)
+    k256 = gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 0, "pipelined", **kw)
+    # K <= 256: one CTA per 128 x 256 tile, persistent over the 152 SMs, whole tiles
+    assert (k256["kernel"], k256["cta_pair"], k256["bn"], k256["stages"]) == ("umma_ring", 0, 256, 4)
+    assert (k256["tiles"], k256["grid"], k256["sk_tiles"]) == (2048, 152, 0)
+    assert gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined")["grid"] == 0   # no device queried
+    with pytest.raises(gp.GemmError):
+        gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", plan_sms=-1)
