@@ -164,6 +164,12 @@ typedef struct gp_options {
     int32_t plan_sms;            /* gemm_plan_ex only: plan for a device with this many SMs instead of the
                                     current one, all of them available (0 = query the current device); a
                                     launch always plans for the device it runs on */
+    int32_t inputs_ready;        /* 1: the caller guarantees that no work still in flight on the stream writes A
+                                    or B (they were in place before the previous call on this stream was made).
+                                    INT8 on tcgen05 (two-pass engine) then converts them while the previous
+                                    call's GEMM is still running, into the other of two FP16 copy buffers
+                                    (pipelining successive calls); the result is the same.  A promise the
+                                    library cannot check: if it is false, A and B may be read too early */
 } gp_options;
 
 /*

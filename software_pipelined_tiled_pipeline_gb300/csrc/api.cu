@@ -92,6 +92,8 @@ struct Workspace {
   uint32_t epoch = 0;
   void* conv = nullptr;       // INT8 on tcgen05: FP16 copies of the operands
   size_t conv_bytes = 0;
+  size_t conv_off = 0;        // region [conv_off, conv_off + conv_len) the last INT8 call on this stream used
+  size_t conv_len = 0;
   uint32_t* ov_ctrs = nullptr;   // INT8 overlap engine: two counter sets of ov_kcap + 1 words
   int32_t ov_kcap = 0;
   uint32_t ov_launches = 0;
@@ -142,8 +144,13 @@ cudaError_t get_workspace(int dev, cudaStream_t stream, size_t bytes, size_t nfl
   return cudaSuccess;
 }
 
-// FP16 operand buffer of the INT8 tcgen05 path, per device and stream.
-cudaError_t get_conv_workspace(int dev, cudaStream_t stream, size_t bytes, void** conv) {
+// FP16 operand buffer of the INT8 tcgen05 path, per device and stream.  With
+// alternate = true the call's copies must not overlap the region the previous
+// call on this stream used (its conversion may run while that call's GEMM
+// still reads them): they go below that region if they fit there, else above
+// it, else the buffer is regrown (after the stream has drained).  Otherwise
+// (conversion ordered after all earlier work) they start at offset 0.
+cudaError_t get_conv_workspace(int dev, cudaStream_t stream, size_t bytes, void** conv, bool alternate = false) {
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace* w = nullptr;
   for (auto& x : g_ws)
@@ -155,18 +162,34 @@ cudaError_t get_conv_workspace(int dev, cudaStream_t stream, size_t bytes, void*
     w->dev = dev;
     w->stream = stream;
   }
-  if (w->conv_bytes < bytes) {
+  constexpr size_t kAlign = 256;
+  const size_t above = (w->conv_off + w->conv_len + kAlign - 1) / kAlign * kAlign;
+  size_t off = 0;
+  bool grow = w->conv_bytes < bytes;
+  if (alternate && !grow) {
+    if (w->conv_len == 0 || bytes <= w->conv_off)
+      off = 0;
+    else if (above + bytes <= w->conv_bytes)
+      off = above;
+    else
+      grow = true;
+  }
+  if (grow) {
     cudaError_t e;
     if (w->conv) {
-      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;   // nothing reads the old buffer now
       cudaFree(w->conv);
       w->conv = nullptr;
       w->conv_bytes = 0;
     }
-    if ((e = cudaMalloc(&w->conv, bytes)) != cudaSuccess) return e;
-    w->conv_bytes = bytes;
+    const size_t cap = alternate ? 2 * (bytes + kAlign) : bytes;
+    if ((e = cudaMalloc(&w->conv, cap)) != cudaSuccess) return e;
+    w->conv_bytes = cap;
+    off = 0;
   }
-  *conv = w->conv;
+  w->conv_off = off;
+  w->conv_len = bytes;
+  *conv = static_cast<unsigned char*>(w->conv) + off;
   return cudaSuccess;
 }
 
@@ -694,7 +717,7 @@ using namespace gp;
 
 extern "C" {
 
-int gemm_abi_version(void) { return 10200; }
+int gemm_abi_version(void) { return 10300; }
 
 const char* gemm_strerror(int code) {
   switch (code) {
@@ -816,7 +839,8 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
       }
       if (i8_tc && !i8_overlap) apply_i8_halves(&plan, pairs);
       if (i8_tc) {
-        e = get_conv_workspace(dev, st, static_cast<size_t>(conv_bytes), &conv);
+        e = get_conv_workspace(dev, st, static_cast<size_t>(conv_bytes), &conv,
+                               !i8_overlap && opts && opts->inputs_ready);
         if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
       }
       if (i8_overlap) {
@@ -861,6 +885,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.ffma_tn = (opts && opts->ffma_tn) ? opts->ffma_tn : 8;
     a.conv = conv;
     a.i8_overlap = i8_overlap;
+    a.conv_early = !i8_overlap && opts && opts->inputs_ready;
     a.conv_ctrs = conv_ctrs;
     a.conv_kcap = conv_kcap;
     a.conv_parity = conv_parity;
@@ -1014,6 +1039,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.ffma_tm = a.ffma_tn = 8;
     a.conv = nullptr;
     a.i8_overlap = false;
+    a.conv_early = false;
     a.conv_ctrs = nullptr;
     a.conv_kcap = 0;
     a.conv_parity = 0;

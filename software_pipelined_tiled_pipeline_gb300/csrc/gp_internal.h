@@ -128,6 +128,7 @@ struct LaunchArgs {
   int32_t ffma_tm, ffma_tn; // FFMA ring: thread tile
   void* conv;               // INT8 on tcgen05: FP16 copies of A then B, (M + N) * K halves
   bool i8_overlap;          // INT8 on tcgen05: the GEMM kernel writes the FP16 copies itself
+  bool conv_early;          // INT8 two-pass: convert while the previous GEMM runs (inputs_ready)
   uint32_t* conv_ctrs;      // ... its two counter sets: {batch counter, conv_kcap K-step counters}
   int32_t conv_kcap;
   uint32_t conv_parity;     // ... the set this launch uses (it zeroes the other)

@@ -732,6 +732,43 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict
   if (i < total) i8x16_store_f16(__ldcs(src(i)), dst(i));
 }
 
+// The same conversion launched early: a programmatic dependent of the
+// previous call's GEMM (when the caller promised that this call's inputs were
+// final before that call), so that it runs beside that GEMM's CTAs.  Measured
+// on GB300 beside the INT8 pair kernel (10 warps x 168 registers and all but
+// 2 KB of shared memory per SM): one more block of at most two warps starts
+// on each SM (a four-warp block does not), and a finished block is not
+// replaced there until the GEMM ends.  So the grid is one persistent two-warp
+// block per SM, with eight 16-byte loads in flight per thread.  Only the last
+// block waits for the previous GEMM before it exits, so that this grid, and
+// what waits for it, completes after that GEMM.
+constexpr int kEarlyConvThreads = 64;
+constexpr int kEarlyConvDepth = 8;
+__global__ void __launch_bounds__(kEarlyConvThreads) i8_to_f16_early_kernel(
+    const int8_t* __restrict__ a, __half* __restrict__ a16, int64_t na16, const int8_t* __restrict__ b,
+    __half* __restrict__ b16, int64_t nb16) {
+  const int64_t total = na16 + nb16;   // 16-element groups
+  pdl_launch_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  auto src = [&](int64_t i) {
+    return i < na16 ? reinterpret_cast<const uint4*>(a) + i : reinterpret_cast<const uint4*>(b) + (i - na16);
+  };
+  auto dst = [&](int64_t i) {
+    return i < na16 ? reinterpret_cast<uint4*>(a16) + 2 * i : reinterpret_cast<uint4*>(b16) + 2 * (i - na16);
+  };
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += kEarlyConvDepth * stride) {
+    uint4 r[kEarlyConvDepth];
+#pragma unroll
+    for (int d = 0; d < kEarlyConvDepth; ++d)
+      if (i + d * stride < total) r[d] = __ldcs(src(i + d * stride));
+#pragma unroll
+    for (int d = 0; d < kEarlyConvDepth; ++d)
+      if (i + d * stride < total) i8x16_store_f16(r[d], dst(i + d * stride));
+  }
+  if (blockIdx.x == gridDim.x - 1) pdl_wait();
+}
+
 // Store one 32-row x 32-column INT32 chunk through a 4 KB swizzled staging
 // buffer and a TMA store (lane t holds row t).
 __device__ __forceinline__ void stage_and_store_i32(const uint32_t* v, uint8_t* buf, int lane, const CUtensorMap* tmap_c,
@@ -848,8 +885,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   tc_fence_before();
   if (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after();
-  pdl_launch_dependents();
   pdl_wait();   // the FP16 copies are written by the conversion kernel launched just before
+  // Only now may a dependent (an early conversion for the next call) start:
+  // the copy buffer it writes is free once the GEMM before this one is done.
+  pdl_launch_dependents();
   const uint32_t tmem = bar->tmem_base;
   CtaCtl* cta = &bar->ctl;
   int issued = 0;
@@ -1731,11 +1770,30 @@ cudaError_t launch_i8(LaunchArgs& a, const void** kernel) {
   __half* b16 = a16 + M * K;
   const int64_t na16 = static_cast<int64_t>(M * K / 16), nb16 = static_cast<int64_t>(N * K / 16);
   int64_t blocks = (na16 + nb16 + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(a.sm_count) * 16;
-  if (blocks > cap) blocks = cap;
-  i8_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, a.stream>>>(static_cast<const int8_t*>(a.A), a16, na16,
-                                                                    static_cast<const int8_t*>(a.B), b16, nb16);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (a.conv_early) {
+    // A programmatic dependent of the previous GEMM: one persistent block
+    // per SM, beside that GEMM's CTAs.
+    blocks = (na16 + nb16 + kEarlyConvThreads - 1) / kEarlyConvThreads;
+    if (blocks > a.sm_count) blocks = a.sm_count;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kEarlyConvThreads);
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, i8_to_f16_early_kernel, static_cast<const int8_t*>(a.A), a16, na16,
+                           static_cast<const int8_t*>(a.B), b16, nb16);
+  } else {
+    const int64_t cap = static_cast<int64_t>(a.sm_count) * 16;
+    if (blocks > cap) blocks = cap;
+    i8_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, a.stream>>>(static_cast<const int8_t*>(a.A), a16, na16,
+                                                                      static_cast<const int8_t*>(a.B), b16, nb16);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   CUtensorMap tmA, tmB, tmC;
   if ((e = make_tmap_2d(&tmC, a.C, CU_TENSOR_MAP_DATA_TYPE_INT32, N, M, N * 4, 32, kUmmaEpiRows,

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_function(gp):
 
 
 def test_version_and_strerror(gp):
-    assert gp.abi_version() == 10200
+    assert gp.abi_version() == 10300
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert gp.strerror(code) and "unknown" not in gp.strerror(code)
     assert "unknown" in gp.strerror(-99)

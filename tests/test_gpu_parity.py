@@ -319,6 +319,32 @@ def test_int8_half_tiles_in_the_last_wave(M, N, K):
     assert torch.equal(C, C2)
 
 
+def test_int8_inputs_ready_pipelines_successive_calls():
+    # with the promise that A and B are in place, each call converts its operands while the
+    # previous call's GEMM still runs, alternating between two copy buffers; ordinary calls,
+    # changes of shape and an FP16 GEMM in between must not disturb it
+    shapes = [(1024, 768, 2048), (520, 260, 3088), (2048, 2048, 1024), (256, 4096, 64), (1024, 768, 2048)] * 2
+    ready = [True, True, False, True, True, True, True, False, True, True]
+    ops = [operands("i8", "row_col", M, N, K, seed=100 + i) for i, (M, N, K) in enumerate(shapes)]
+    tens = [(to_dev(A, "i8"), to_dev(B, "i8")) for A, B in ops]
+    outs = [torch.empty(M * N, dtype=torch.int32, device="cuda") for M, N, K in shapes]
+    Mf, Nf, Kf = 1024, 1024, 2048
+    Af, Bf = operands("f16", "row_col", Mf, Nf, Kf, seed=99)
+    tAf, tBf = to_dev(Af, "f16"), to_dev(Bf, "f16")
+    Cf = torch.empty(Mf * Nf, dtype=torch.float16, device="cuda")
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for i, ((M, N, K), (tA, tB), C, r) in enumerate(zip(shapes, tens, outs, ready)):
+        if i == 5:
+            gp.gemm_pipelined(tAf, tBf, Cf, Mf, Nf, Kf, "f16", "row_col", 0, "pipelined", stream)
+        gp.gemm_pipelined(tA, tB, C, M, N, K, "i8", "row_col", 0, "pipelined", stream, inputs_ready=r)
+    st = gp.gemm_stats(sync=True)
+    assert st["status"] == 0 and st["device_status"] == 0
+    for (M, N, K), (A, B), C in zip(shapes, ops, outs):
+        check_full("i8", "row_col", A, B, C.view(M, N).cpu(), K)
+    check_sampled("f16", "row_col", Af, Bf, Cf.view(Mf, Nf).cpu(), Kf, rows=[0, 511, Mf - 1], npts=2000, seed=7)
+
+
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (1000, 3000, 2000), (256, 256, 16), (4104, 264, 1040)])
 def test_int8_overlapped_conversion_matches_two_pass(M, N, K):
     # the same FP16 MMAs in the same order on the same exact values: identical int32 results
