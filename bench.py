@@ -5,9 +5,10 @@ One step = one GEMM over the workload (all steps of the K-loop hot path:
 tile decomposition, prologue, steady-state ring, drain, output epilogue).
 Default workload: FP16 GEMM M=N=K=4096, A row-major, B column-major, FP32
 accumulate, FP16 out, TMA-ring tcgen05 kernel on CTA pairs at the library's
-default depth (6 stages).  Prints ONE JSON
+default depth (5 stages at this shape).  Prints ONE JSON
 line (rank 0).  The INT8 4096^3 result, the stage sweep and the FP32
-ping-pong-vs-async comparison ride along as sub-objects.
+ping-pong-vs-async comparison ride along as sub-objects, and the vendor
+library's time on the same shape and buffers as context.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--stages S] [--no-sweep] [--no-sweep-bf16]
@@ -201,6 +202,43 @@ def isolated_launch_ms(torch, gp, gemm, n, stream):
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
+def library_same_shape(torch, w, bufs, stream, n):
+    """The vendor library on the same shape, buffers and back-to-back timing, for context only
+    (it is not on the product path): torch.matmul (cuBLAS; FP32 with TF32 off) for FP16/BF16/FP32,
+    torch._int_mm (cuBLASLt, INT8 -> INT32) for INT8.  Returns (ms per call, how) or (None, why)."""
+    def call(i):
+        a, b, c = bufs[i % len(bufs)]
+        a2 = a.view(w.M, w.K)
+        c2 = c.view(w.M, w.N)
+        if w.dtype == "i8":
+            torch._int_mm(a2, b.view(w.N, w.K).t(), out=c2)
+        elif w.layout == "row_col":
+            torch.matmul(a2, b.view(w.N, w.K).t(), out=c2)
+        else:
+            torch.matmul(a2, b.view(w.K, w.N), out=c2)
+    how = "torch._int_mm (cuBLASLt)" if w.dtype == "i8" else "torch.matmul (cuBLAS%s)" % (
+        ", TF32 off" if w.dtype == "f32" else "")
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                call(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            stream.synchronize()
+            e0.record(stream)
+            for i in range(n):
+                call(i)
+            e1.record(stream)
+            stream.synchronize()
+        return e0.elapsed_time(e1) / n, how
+    except (RuntimeError, TypeError, AttributeError) as e:
+        return None, "%s unavailable: %s" % (how, str(e).splitlines()[0][:160])
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+
+
 def max_over_ranks(torch, dist, x, device):
     """The largest x over all ranks (the slowest rank's time); x itself on one process."""
     if dist is None:
@@ -284,6 +322,9 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
         if w.dtype in ("f16", "bf16"):
             # the same ring on one CTA per 128-row tile, whole tiles only (no pairs, no stream-K)
             cases += [("pipelined", S, {"no_cta_pair": True, "no_stream_k": True}) for S in (4, 6)]
+            # two CTA pairs per cluster of four on a 256 x 512 tile, A shared by TMA multicast
+            if w.K > 256 and w.N > 256:
+                cases += [("pipelined", S, {"bn": 512}) for S in (5, 6)]
         if w.dtype == "i8":
             # the TMA ring feeding warp-level IMMA (the ping-pong and no-overlap rows use IMMA too)
             cases += [("pipelined", S, {"i8_engine": "imma"}) for S in w.stages]
@@ -499,6 +540,7 @@ def main():
             raise RuntimeError("timed region failed: status %d" % st["status"])
         total_ms = t_start.elapsed_time(t_end)
         iso_ms = isolated_launch_ms(torch, gp, gemm, min(args.steps, 50), stream)
+    lib_ms, lib_how = library_same_shape(torch, w, bufs, stream, max(10, min(args.steps, 50)))
 
     total_ms = max_over_ranks(torch, pg, total_ms, dev)
     ms_per_step = total_ms / args.steps
@@ -643,6 +685,10 @@ def main():
                 "how": "copies of step i+1 in and step i-1 out overlap step i's GEMM (3 streams, 2 buffer sets); "
                        "host link ~180 GB/s each way"},
         "gpu_launches": args.steps * (2 if plan["kernel"] == "umma_i8_pair_ring" else 1),
+        "library_same_shape": ({"value": round(w.ops / (lib_ms * 1e-3) / 1e12, 2), "unit": unit,
+                                "ms_per_call": round(lib_ms, 5), "how": lib_how + ", same buffers, back to back",
+                                "ours_over_library": round(lib_ms / ms_per_step, 3)}
+                               if lib_ms else {"unavailable": lib_how}),
         "sustained": sustained,
         "clocks": ClockSampler.summarize(clock_rows, wall0, wall1),
     }

@@ -307,6 +307,7 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
   constexpr int64_t kMinIdleSteps = 16;
   constexpr int64_t kMinStepsPerWorker = 4;
   const int64_t T = p->tiles, G = workers;
+  const int64_t part_bn = p->cta_pair == 2 ? p->bn / 2 : p->bn;   // columns of one CTA's partial tile
   p->dp_tiles = static_cast<int32_t>(T);
   p->sk_tiles = 0;
   p->workspace_bytes = 0;
@@ -320,7 +321,7 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
   p->dp_tiles = static_cast<int32_t>(dp);
   p->sk_tiles = static_cast<int32_t>(skt);
   p->grid = static_cast<int32_t>(ctas_per_worker * G);
-  p->workspace_bytes = static_cast<int64_t>(p->grid) * 2 * 128 * p->bn * 4;   // two 128 x BN FP32 slots per CTA
+  p->workspace_bytes = static_cast<int64_t>(p->grid) * 2 * 128 * part_bn * 4;   // two 128-row FP32 slots per CTA
 }
 
 // INT8 on tcgen05 (two-pass engine), whole tiles over W workers: when the last
@@ -339,7 +340,7 @@ void apply_i8_halves(gp_plan* p, int64_t workers) {
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
               int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, int i8_engine = 0,
-              int ffma_tm = 0, int ffma_tn = 0) {
+              int ffma_tm = 0, int ffma_tn = 0, bool no_mc = false) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
@@ -470,7 +471,14 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     return ring_smem_total(S * (kUmmaBM + pbn / 2) * kUmmaBK * 2, kUmmaEpiBytes) <= kSmemPerCtaMax;
   };
   const bool pair_base = fam == 2 && ring && !no_pair && K > kShortK;
-  const bool pair256 = pair_base && (bn_req == 0 || bn_req == 256) && N > 128 && pair_fits(256);
+  const bool pair256 = pair_base && (bn_req == 0 || bn_req == 256 || bn_req == 512) && N > 128 && pair_fits(256);
+  // bn = 512 asks for two pairs per cluster of four, side by side along N,
+  // sharing the A rows through TMA multicast (a 256 x 512 tile: a quarter
+  // fewer bytes read from L2 per MMA, the same bytes into each SM).  Measured
+  // at FP16 4096^3 and BF16 8192^2 x 4096 it is no faster than single pairs
+  // (36 clusters of four fit, 144 of 152 SMs), so it is not the default.
+  const bool mc = pair256 && !no_mc && (sm_count == 0 || sm_count >= 8) && bn_req == 512;
+  if (bn_req == 512 && !mc) return GP_ERR_UNSUPPORTED;
   const bool pair128 = pair_base && !pair256 && bn_req == 0 && N > 64 && M > 128 && pair_fits(128);
   const bool pair_ok = pair256 || pair128;
   const int pair_bn = pair256 ? 256 : 128;
@@ -519,11 +527,18 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     if (p->smem_bytes < kSmemPerCtaMax / 2 + 1024) p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
     p->tmem_cols = 2 * pair_bn;
     p->kernel = "umma_pair_ring";
+    if (mc) {
+      p->cta_pair = 2;
+      p->bn = 512;   // the cluster's tile; each pair computes 256 x 256 of it
+      p->kernel = "umma_pair_mc_ring";
+    }
   }
   p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
   p->k_tiles = ceil_div(K, p->bk);
   if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
-  if (p->cta_pair)
+  if (p->cta_pair == 2)
+    p->grid = sm_count > 3 ? static_cast<int32_t>(4 * (p->tiles < sm_count / 4 ? p->tiles : sm_count / 4)) : 0;
+  else if (p->cta_pair)
     p->grid = sm_count > 1 ? static_cast<int32_t>(2 * (p->tiles < sm_count / 2 ? p->tiles : sm_count / 2)) : 0;
   else if (p->persistent)
     p->grid = sm_count > 0 ? static_cast<int32_t>(p->tiles < sm_count ? p->tiles : sm_count) : 0;
@@ -550,14 +565,18 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     }
   }
   if (fam == 2 && ring && sm_count > 0) {
-    if (p->cta_pair)
+    if (p->cta_pair == 2)
+      apply_stream_k(p, sm_count / 4, 4, !no_stream_k);
+    else if (p->cta_pair)
       apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
     else
       apply_stream_k(p, sm_count, 1, !no_stream_k);
   }
   const double e = in_elem_bytes(dtype);
   p->compute_load_ratio = 2.0 * p->bm * p->bn * p->bk / ((static_cast<double>(p->bm) * p->bk + p->bk * p->bn) * e);
-  if (p->cta_pair)   // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B
+  if (p->cta_pair == 2)   // per CTA: 128 x 256 outputs from 64 rows of A fetched (64 multicast in) and 128 of B
+    p->compute_load_ratio = 2.0 * 128 * 256 * p->bk / ((64.0 + 128.0) * p->bk * e);
+  else if (p->cta_pair)   // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B
     p->compute_load_ratio = 2.0 * (p->bm / 2) * p->bn * p->bk / ((p->bm / 2 + p->bn / 2) * p->bk * e);
   return GP_OK;
 }
@@ -717,7 +736,7 @@ using namespace gp;
 
 extern "C" {
 
-int gemm_abi_version(void) { return 10300; }
+int gemm_abi_version(void) { return 10400; }
 
 const char* gemm_strerror(int code) {
   switch (code) {
@@ -820,6 +839,15 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
                    opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
     if (rc != GP_OK) { record(rc, 0); return rc; }
+    if (plan.cta_pair == 2) {
+      // clusters of four sit on two TPCs of one GPC each: fewer than SMs / 4
+      // may be resident (36 on a 152-SM GB300); stream-K over those
+      int clusters = 0;
+      e = umma_mc_capacity(dtype, plan.smem_bytes, &clusters);
+      if (e == cudaSuccess && clusters < 1) e = cudaErrorLaunchOutOfResources;
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (clusters < sms / 4) apply_stream_k(&plan, clusters, 4, !(opts && opts->no_stream_k));
+    }
     void* conv = nullptr;
     const bool i8_overlap = plan.cta_pair && dtype == GP_I8_I32 && plan.kernel == kI8OverlapKernelName;
     const bool i8_tc = plan.cta_pair && dtype == GP_I8_I32;   // both engines keep FP16 copies
@@ -827,7 +855,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     uint32_t* conv_ctrs = nullptr;
     int32_t conv_kcap = 0;
     uint32_t conv_parity = 0;
-    if (plan.cta_pair) {
+    if (plan.cta_pair == 1) {
       // pairs must sit on one TPC each: the resident count may be below SMs / 2
       int pairs = 0;
       e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs, i8_overlap);
@@ -850,7 +878,8 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     }
     SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, 0};
     if (plan.sk_tiles > 0) {
-      const size_t counter_words = static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair ? 2 : 1) * 2;
+      const size_t counter_words =
+          static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair == 2 ? 4 : plan.cta_pair ? 2 : 1) * 2;
       e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes - conv_bytes), counter_words, &sk.workspace,
                         &sk.flags, &sk.epoch);
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
@@ -975,7 +1004,8 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     return GP_ERR_UNSUPPORTED;
   }
   gp_plan plan;
-  int rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, 0, &plan);
+  // (plain CTA pairs: the fixed scratch is sized for them)
+  int rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, 0, &plan, false, false, 0, 0, 0, true);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }
@@ -998,7 +1028,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
   if (K == 0) {
     e = launch_zero_fill(C, M * N * out_elem_bytes(dtype), st);
   } else {
-    rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, sms, &plan);
+    rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, sms, &plan, false, false, 0, 0, 0, true);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     if (plan.cta_pair) {
       int pairs = 0;

@@ -315,6 +315,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// The same load multicast: the box lands at the same shared-memory offset in
+// every CTA of cta_mask, and each destination's arrival is counted on the
+// barrier at bar_cluster_addr's offset in the even CTA of that destination's
+// pair (the address names this CTA's pair leader).
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
+                                                    int32_t x, int32_t y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask)
+      : "memory");
+}
+
 // TMEM management for a CTA pair: one warp of EACH CTA executes these together.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)

@@ -332,7 +332,7 @@ struct RingShape {
   static_assert(EPI_BUFS >= 1 && WARP_CHUNKS >= 1, "epilogue split");
 };
 
-template <int BN, bool BF16, bool PAIR>
+template <int BN, bool BF16, bool PAIR, bool MC>
 __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     umma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl,
@@ -349,19 +349,30 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  // MC: a cluster of two CTA pairs computes a 256 x 2BN tile, pair p its
+  // columns p*BN .. +BN.  Both pairs read the same 256 rows of A: each CTA
+  // receives its 128 rows half from its own multicast load and half from the
+  // one of the CTA with the same rank in the other pair (see the producer).
+  constexpr int CL = MC ? 4 : (PAIR ? 2 : 1);                 // CTAs per worker (one cluster)
+  static_assert(!MC || PAIR, "multicast runs on CTA pairs");
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;      // rank in the cluster
+  const uint32_t rank = crank & 1u;                           // rank in the CTA pair
+  const int pidx = MC ? static_cast<int>(crank >> 1) : 0;     // pair within the cluster
   const bool leader = rank == 0;
-  const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const uint32_t lead_rank = crank & ~1u;                     // this pair's even CTA
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead_rank);
+  const int worker = static_cast<int>(blockIdx.x) / CL;
+  const int workers = static_cast<int>(gridDim.x) / CL;
+  constexpr int UNIT_N = MC ? 2 * BN : BN;                    // output columns of one work item
   const int m_blocks = (M + Sh::TILE_M - 1) / Sh::TILE_M;
-  const int n_blocks = (N + BN - 1) / BN;
+  const int n_blocks = (N + UNIT_N - 1) / UNIT_N;
   const int tiles = m_blocks * n_blocks;
   const int kt = (K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&bar->full[s], 1);
-      mbar_init(&bar->empty[s], 1);
+      mbar_init(&bar->empty[s], MC ? 2 : 1);   // MC: released by both pairs' MMAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->acc_full[a], 1);
@@ -413,14 +424,23 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
         int mb, nb;
         tile_coords(tile, m_blocks, n_blocks, mb, nb);
         const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
-        const int n_row = nb * BN + rank * Sh::B_ROWS;
+        const int n_row = (nb * (MC ? 2 : 1) + pidx) * BN + rank * Sh::B_ROWS;
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto producer_done;
           uint8_t* slot = ring + s * STAGE;
           if (PAIR) {
             if (leader) mbar_arrive_expect_tx(&bar->full[s], 2 * STAGE);
-            const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), 0);
-            tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
+            const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), lead_rank);
+            if (MC) {
+              // rows pidx*64 .. +64 of this CTA's 128 rows of A, to this CTA
+              // and to the CTA of the same pair rank in the other pair (both
+              // slots are free: empty[s] counts both pairs' MMAs)
+              constexpr int HALF = Sh::A_ROWS / 2;
+              tma_load_2d_pair_mc(smem_u32(slot) + pidx * HALF * BK * 2, &tmA, full_leader, kb * BK,
+                                  m_row + pidx * HALF, static_cast<uint16_t>(0x5u << rank));
+            } else {
+              tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
+            }
             tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
             ++issued;
           } else if (!(ctl.inject_lost_load && tile == tiles - 1 && kb == kt - 1)) {
@@ -462,16 +482,16 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
               umma_f16(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
           }
           // slot s is free (in every CTA that loaded into it) once these MMAs have read it
-          if (PAIR) umma_commit_pair(&bar->empty[s], 0x3); else umma_commit(&bar->empty[s]);
+          if (PAIR) umma_commit_pair(&bar->empty[s], MC ? 0xF : 0x3); else umma_commit(&bar->empty[s]);
           ++consumed;
           if (++s == stages) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        if (PAIR) umma_commit_pair(&bar->acc_full[a], 0x3); else umma_commit(&bar->acc_full[a]);
+        if (PAIR) umma_commit_pair(&bar->acc_full[a], pair_mask); else umma_commit(&bar->acc_full[a]);
       }
       bar->consumed_hi = consumed;
       // every MMA issued by this thread has completed once drain fires
-      if (PAIR) umma_commit_pair(&bar->drain, 0x1); else umma_commit(&bar->drain);
+      if (PAIR) umma_commit_pair(&bar->drain, static_cast<uint16_t>(1u << lead_rank)); else umma_commit(&bar->drain);
       CtaCtl never_abort{0};
       mbar_wait(&bar->drain, 0, ctl, &never_abort, kSiteDrain);
     }
@@ -492,7 +512,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       // segment that completes last sums all of them in K order and writes C.
       const bool split = (k0 > 0) || (k1 < kt);
       SplitTile sp;
-      if (split) sp.init(tile, kt, sk, workers, Sh::CTAS, rank);
+      if (split) sp.init(tile, kt, sk, workers, CL, crank);
       uint32_t ok = 1;
       if (lane == 0) ok = mbar_wait(&bar->acc_full[a], (t >> 1) & 1, ctl, cta, kSiteEpilogueAccFull) ? 1u : 0u;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -511,6 +531,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       tc_fence_after();
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
       const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
+      const int x0 = (nb * (MC ? 2 : 1) + pidx) * BN;   // first column of this pair's tile
       if (!split) {
         // Whole tile: the TMEM load of chunk c + 1 is in flight while chunk c
         // is converted, staged and stored (chunks unrolled, so no register
@@ -532,14 +553,14 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
             __syncwarp();
             if (lane == 0) {
               if (PAIR)
-                mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), 0));
+                mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), lead_rank));
               else
                 mbar_arrive(&bar->acc_empty[a]);
             }
           }
           if (lane == 0) bulk_wait_read<Sh::EPI_BUFS - 1>();
           __syncwarp();
-          const int x = nb * BN + c * kUmmaEpiCols;
+          const int x = x0 + c * kUmmaEpiCols;
           store_packed(pk, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
           if (++sb == Sh::EPI_BUFS) sb = 0;
         }
@@ -555,7 +576,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             if (PAIR)
-              mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), 0));
+              mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), lead_rank));
             else
               mbar_arrive(&bar->acc_empty[a]);
           }
@@ -565,7 +586,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
           for (int w = sp.w_first + 1; w <= sp.w_last; ++w) {
             if (!sp.has_segment(w)) continue;
             const float4* src = reinterpret_cast<const float4*>(sk.workspace) +
-                                partial_at<BN>(sp.slot(w, Sh::CTAS, rank), c, 0, row);
+                                partial_at<BN>(sp.slot(w, CL, crank), c, 0, row);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float4 p = __ldcg(src + i * Sh::A_ROWS);
@@ -576,7 +597,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
             }
           }
         } else if (split) {
-          float4* dst = reinterpret_cast<float4*>(sk.workspace) + partial_at<BN>(sp.slot(worker, Sh::CTAS, rank), c, 0, row);
+          float4* dst = reinterpret_cast<float4*>(sk.workspace) + partial_at<BN>(sp.slot(worker, CL, crank), c, 0, row);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             __stcg(dst + i * Sh::A_ROWS, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
@@ -585,7 +606,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
         }
         if (lane == 0) bulk_wait_read<Sh::EPI_BUFS - 1>();
         __syncwarp();
-        const int x = nb * BN + c * kUmmaEpiCols;
+        const int x = x0 + c * kUmmaEpiCols;
         stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
         if (++sb == Sh::EPI_BUFS) sb = 0;
       }
@@ -608,7 +629,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
         for (int w = sp.w_first; w <= sp.w_last; ++w) {
           if (!sp.has_segment(w)) continue;
           const float4* src = reinterpret_cast<const float4*>(sk.workspace) +
-                              partial_at<BN>(sp.slot(w, Sh::CTAS, rank), c, 0, row);
+                              partial_at<BN>(sp.slot(w, CL, crank), c, 0, row);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float4 p = __ldcg(src + i * Sh::A_ROWS);
@@ -628,7 +649,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
         }
         if (lane == 0) bulk_wait_read<Sh::EPI_BUFS - 1>();
         __syncwarp();
-        const int x = nb * BN + c * kUmmaEpiCols;
+        const int x = x0 + c * kUmmaEpiCols;
         stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
         if (++sb == Sh::EPI_BUFS) sb = 0;
       }
@@ -1703,7 +1724,7 @@ __global__ void __launch_bounds__(kPPThreads, 1)
   }
 }
 
-template <int BN, bool BF16, bool PAIR>
+template <int BN, bool BF16, bool PAIR, bool MC = false>
 cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   using Sh = RingShape<BN, PAIR>;
   const gp_plan& p = a.plan;
@@ -1714,11 +1735,13 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   if ((e = make_tmap_2d(&tmC, a.C, dt, N, M, N * 2, kUmmaEpiCols, kUmmaEpiRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       cudaSuccess)
     return e;
-  if ((e = make_tmap_2d(&tmA, a.A, dt, K, M, K * 2, BK, Sh::A_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  // MC: each multicast load carries half of a CTA's rows of A
+  if ((e = make_tmap_2d(&tmA, a.A, dt, K, M, K * 2, BK, MC ? Sh::A_ROWS / 2 : Sh::A_ROWS,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   if ((e = make_tmap_2d(&tmB, a.B, dt, K, N, K * 2, BK, Sh::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
-  auto k = umma_ring_kernel<BN, BF16, PAIR>;
+  auto k = umma_ring_kernel<BN, BF16, PAIR, MC>;
   *kernel = reinterpret_cast<const void*>(k);
   if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1730,7 +1753,7 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   int n = 0;
   if (PAIR) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.x = MC ? 4 : 2;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -1893,29 +1916,35 @@ cudaError_t launch_i8_overlap(LaunchArgs& a, const void** kernel) {
 
 // Largest number of CTA pairs of a pair kernel that can be resident at once.
 // kind: 0 FP16 ring, 1 BF16 ring, 2 INT8 two-pass, 3 INT8 with the conversion overlapped.
-cudaError_t max_pairs(int kind, int smem_bytes, int* pairs) {
+// Clusters of `size` CTAs (2: one pair; 4: two pairs sharing A, kinds 0-1)
+// resident at once at this shared-memory size.
+cudaError_t max_clusters(int kind, int smem_bytes, int size, int* clusters) {
+  const bool mc = size == 4;
   const void* k = kind == 3   ? reinterpret_cast<const void*>(umma_i8_overlap_kernel)
                   : kind == 2 ? reinterpret_cast<const void*>(umma_i8_kernel<true>)
-                  : kind == 1 ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true>)
-                              : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true>);
+                  : kind == 1 ? (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, true>)
+                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, false>))
+                              : (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, true>)
+                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, false>));
   cudaError_t e = ensure_smem_attr(k, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
+  cfg.gridDim = dim3(size);
   cfg.blockDim = dim3(kind == 3 ? kOvThreads : kind == 2 ? kI8Threads : RingShape<256, true>::THREADS);
   cfg.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = size;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(pairs, k, &cfg);
+  return cudaOccupancyMaxActiveClusters(clusters, k, &cfg);
 }
 
 template <bool BF16>
 cudaError_t launch_dtype(LaunchArgs& a, const void** kernel) {
+  if (a.plan.cta_pair == 2) return launch_ring<256, BF16, true, true>(a, kernel);
   if (a.plan.cta_pair)
     return a.plan.bn == 128 ? launch_ring<128, BF16, true>(a, kernel) : launch_ring<256, BF16, true>(a, kernel);
   switch (a.plan.bn) {
@@ -1934,7 +1963,11 @@ cudaError_t launch_umma(LaunchArgs& a, const void** kernel) {
 
 cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs, bool i8_overlap) {
   const int kind = dtype == GP_I8_I32 ? (i8_overlap ? 3 : 2) : (dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0);
-  return max_pairs(kind, smem_bytes, pairs);
+  return max_clusters(kind, smem_bytes, 2, pairs);
+}
+
+cudaError_t umma_mc_capacity(int dtype, int smem_bytes, int* clusters) {
+  return max_clusters(dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0, smem_bytes, 4, clusters);
 }
 
 cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel) {
