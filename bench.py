@@ -714,7 +714,7 @@ def main():
             tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
             line["int8"] = {
                 "workload": "i8_4096", "value": best["TOPS"], "unit": "TOPS", "stages": best["stages"],
-                "kernel": best["kernel"],
+                "kernel": best["kernel"], "options": best.get("options", {}),
                 "peak": tpeak, "frac": round(best["TOPS"] / tpeak, 4),
                 "peak_source": peaks["_source"] + ": dense 16-bit tcgen05 rate (the INT8 products run as exact "
                                                   "FP16 MMAs; includes the FP16 conversion pass)",
