@@ -34,8 +34,11 @@ namespace gp {
 namespace {
 
 constexpr int BM = kFfmaBM, BN = kFfmaBN, BK = kFfmaBK;
-constexpr int A_FLOATS = BM * BK;          // 1024
+constexpr int A_FLOATS = BM * BK;          // 1024 (register-staged kernels)
 constexpr int STAGE = kFfmaStageBytes;     // 8192
+constexpr int RBK = kFfmaRingBK;           // the TMA ring's K steps per slot
+constexpr int RA_FLOATS = BM * RBK;
+constexpr int RSTAGE = kFfmaRingStageBytes;
 
 struct FfmaBarriers {
   uint64_t full[kMaxStages];
@@ -98,16 +101,17 @@ __device__ __forceinline__ void fma2(float& c0, float& c1, float a, float b0, fl
       : "f"(a), "f"(b0), "f"(b1));
 }
 
-template <int TM, int TN>
+// One slot of KB K steps: A as BM rows of KB, B as KB rows of BN.
+template <int TM, int TN, int KB = BK>
 __device__ __forceinline__ void ffma_kblock(const float* __restrict__ As, const float* __restrict__ Bs, int tx,
                                             int ty, Acc<TM, TN>& acc) {
   using T = Tile<TM, TN>;
 #pragma unroll
-  for (int kh = 0; kh < BK; kh += 4) {
+  for (int kh = 0; kh < KB; kh += 4) {
     float a[TM][4];
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
-      const float4 v = *reinterpret_cast<const float4*>(As + (ty + T::TY * i) * BK + kh);
+      const float4 v = *reinterpret_cast<const float4*>(As + (ty + T::TY * i) * KB + kh);
       a[i][0] = v.x; a[i][1] = v.y; a[i][2] = v.z; a[i][3] = v.w;
     }
 #pragma unroll
@@ -275,11 +279,11 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
   using T = Tile<TM, TN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align1024(smem_raw);
-  FfmaBarriers* bar = reinterpret_cast<FfmaBarriers*>(ring + stages * STAGE);
+  FfmaBarriers* bar = reinterpret_cast<FfmaBarriers*>(ring + stages * RSTAGE);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
-  const int kt = (K + BK - 1) / BK;
+  const int kt = (K + RBK - 1) / RBK;
   const int tiles = m_blocks * n_blocks;
 
   if (threadIdx.x == 0) {
@@ -311,10 +315,10 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) { ok = false; break; }
           if (!(ctl.inject_lost_load && last_cta && wk.u >= wk.u_end && kb == k1 - 1)) {
-            uint8_t* slot = ring + s * STAGE;
-            mbar_arrive_expect_tx(&bar->full[s], STAGE);
-            tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, mb * BM);
-            tma_load_2d(smem_u32(slot + A_FLOATS * 4), &tmB, &bar->full[s], nb * BN, kb * BK);
+            uint8_t* slot = ring + s * RSTAGE;
+            mbar_arrive_expect_tx(&bar->full[s], RSTAGE);
+            tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * RBK, mb * BM);
+            tma_load_2d(smem_u32(slot + RA_FLOATS * 4), &tmB, &bar->full[s], nb * BN, kb * RBK);
             ++issued;
           }
           if (++s == stages) { s = 0; ph ^= 1u; }
@@ -335,8 +339,8 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
       for (int kb = k0; kb < k1; ++kb) {
         const bool w = mbar_wait(&bar->full[s], ph, ctl, cta, kSiteConsumerFull);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        const float* As = reinterpret_cast<const float*>(ring + s * STAGE);
-        ffma_kblock<TM, TN>(As, As + A_FLOATS, tx, ty, acc);
+        const float* As = reinterpret_cast<const float*>(ring + s * RSTAGE);
+        ffma_kblock<TM, TN, RBK>(As, As + RA_FLOATS, tx, ty, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar->empty[s]);
         ++consumed;
@@ -401,12 +405,17 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
   const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
   const int kt = (K + BK - 1) / BK;
   const int tx = threadIdx.x % T::TX, ty = threadIdx.x / T::TX;
-  FfmaWork wk(m_blocks * n_blocks, kt);
-  int tile, k0, k1, seg;
-  while (wk.next(tile, k0, k1, seg)) {
+  // A K-loop shared by several CTAs is cut at the ring's K steps (RBK), so
+  // every variant adds the same partial sums: each unit is RBK / BK tiles here.
+  constexpr int R = RBK / BK;
+  static_assert(RBK % BK == 0, "ring K step");
+  FfmaWork wk(m_blocks * n_blocks, (K + RBK - 1) / RBK);
+  int tile, u0, u1, seg;
+  while (wk.next(tile, u0, u1, seg)) {
     int mb, nb;
     tile_coords(tile, m_blocks, n_blocks, mb, nb);
     const int m0 = mb * BM, n0 = nb * BN;
+    const int k0 = u0 * R, k1 = min(u1 * R, kt);
     Acc<8, 8> acc;
     acc.zero();
     RegStage rs;
@@ -464,10 +473,10 @@ cudaError_t launch_ffma(LaunchArgs& a, const void** kernel) {
   if (a.variant == GP_PIPELINED) {
     CUtensorMap tmA, tmB;
     const uint64_t M = a.M, N = a.N, K = a.K;
-    if ((e = make_tmap_2d(&tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, K, M, K * 4, BK, BM,
+    if ((e = make_tmap_2d(&tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, K, M, K * 4, RBK, BM,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
       return e;
-    if ((e = make_tmap_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, K, N * 4, BN, BK,
+    if ((e = make_tmap_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, K, N * 4, BN, RBK,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
       return e;
     switch (a.ffma_tm * 100 + a.ffma_tn) {
