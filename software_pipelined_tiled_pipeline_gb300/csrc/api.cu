@@ -433,7 +433,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   int extra = 0;
   if (fam == 0) {
     p->bm = kFfmaBM;
-    p->bk = ring ? kFfmaRingBK : kFfmaBK;
+    p->bk = ring ? ffma_ring_bk(S) : kFfmaBK;
     cands[ncand++] = kFfmaBN;
     // thread tile of the ring (the register-staged variants build the pages' 8 x 8 only)
     const int tm = ffma_tm ? ffma_tm : 8, tn = ffma_tn ? ffma_tn : 8;
@@ -459,7 +459,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     p->kernel = ring ? "umma_ring" : (variant == GP_PINGPONG ? "umma_pingpong" : "umma_nopipe");
   }
   auto stage_bytes = [&](int bn) {
-    if (fam == 0) return ring ? kFfmaRingStageBytes : kFfmaStageBytes;
+    if (fam == 0) return ring ? ffma_ring_stage_bytes(S) : kFfmaStageBytes;
     if (fam == 1) return imma_stage_bytes(bn);
     return umma_stage_bytes(bn);
   };
@@ -554,9 +554,10 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     // number of CTAs per tile keeps one segment per CTA: measured at FP32
     // 1024^3, 2 per tile (128 CTAs) ran 34.6 TFLOP/s, one range per SM (152
     // CTAs, up to 4 per tile, two segments for most CTAs) 28.3.
-    constexpr int64_t kFfmaMaxSplits = 4, kFfmaMinSplitSteps = 16;
-    // (counted in the ring's K steps for every variant: all cut the K-loop at the same places)
-    const int64_t split_steps = ceil_div(K, kFfmaRingBK);
+    constexpr int64_t kFfmaMaxSplits = 4, kFfmaMinSplitSteps = 256 / kFfmaSplitK;
+    // (counted in units of kFfmaSplitK K steps for every variant: all cut the K-loop at the same
+    // places; kFfmaMinSplitSteps units are 256 K steps)
+    const int64_t split_steps = ceil_div(K, kFfmaSplitK);
     int64_t splits = sm_count / p->tiles;
     if (splits > kFfmaMaxSplits) splits = kFfmaMaxSplits;
     if (splits > split_steps / kFfmaMinSplitSteps) splits = split_steps / kFfmaMinSplitSteps;

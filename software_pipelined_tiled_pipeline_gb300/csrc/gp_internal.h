@@ -74,11 +74,17 @@ constexpr int kMaxStages = 8;
 // FFMA (FP32) family: CTA tile 128 x 128 x 8, 8 compute warps, 8x8 outputs per thread.
 constexpr int kFfmaBM = 128, kFfmaBN = 128, kFfmaBK = 8;
 constexpr int kFfmaStageBytes = (kFfmaBM * kFfmaBK + kFfmaBK * kFfmaBN) * 4;
-// The TMA ring takes 16 K steps per slot (half the slot hand-offs per FMA of
-// 8; measured +9 % at FP32 1024^3, +12 % at 4096^3); the register-staged
-// baselines keep the 8 their thread-to-element mapping is built for.
-constexpr int kFfmaRingBK = 16;
-constexpr int kFfmaRingStageBytes = (kFfmaBM * kFfmaRingBK + kFfmaRingBK * kFfmaBN) * 4;
+// The TMA ring takes 32 K steps per slot up to 6 slots and 16 for 7-8 (so
+// that 8 slots still fit): fewer slot hand-offs per FMA than 8 (measured at
+// FP32 1024^3: 35.6 TFLOP/s with 8, 38.6 with 16, 40.1 with 32).  The
+// register-staged baselines keep the 8 their thread-to-element mapping is
+// built for.  A K-loop shared by several CTAs is cut every kFfmaSplitK K
+// steps in every variant, so all of them add the same partial sums.
+constexpr int kFfmaSplitK = 32;
+constexpr int ffma_ring_bk(int stages) { return stages <= 6 ? 32 : 16; }
+constexpr int ffma_ring_stage_bytes(int stages) {
+  return (kFfmaBM * ffma_ring_bk(stages) + ffma_ring_bk(stages) * kFfmaBN) * 4;
+}
 
 // IMMA (INT8) family: CTA tile 128 x BN x 128, BN in {128, 64}; 8 compute warps (2 x 4).
 constexpr int kImmaBM = 128, kImmaBK = 128;

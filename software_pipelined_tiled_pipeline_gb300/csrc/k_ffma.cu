@@ -36,9 +36,7 @@ namespace {
 constexpr int BM = kFfmaBM, BN = kFfmaBN, BK = kFfmaBK;
 constexpr int A_FLOATS = BM * BK;          // 1024 (register-staged kernels)
 constexpr int STAGE = kFfmaStageBytes;     // 8192
-constexpr int RBK = kFfmaRingBK;           // the TMA ring's K steps per slot
-constexpr int RA_FLOATS = BM * RBK;
-constexpr int RSTAGE = kFfmaRingStageBytes;
+constexpr int SPLIT_K = kFfmaSplitK;       // K steps of one unit of a split K-loop
 
 struct FfmaBarriers {
   uint64_t full[kMaxStages];
@@ -101,7 +99,10 @@ __device__ __forceinline__ void fma2(float& c0, float& c1, float a, float b0, fl
       : "f"(a), "f"(b0), "f"(b1));
 }
 
-// One slot of KB K steps: A as BM rows of KB, B as KB rows of BN.
+// One slot of KB K steps: A as BM rows of KB, B as KB rows of BN.  (At
+// KB = 32 the two A rows a warp reads at once share banks; a 128-byte TMA
+// swizzle of A removed that conflict but measured 4 % slower at FP32 4096^3:
+// the per-load address arithmetic costs more issue slots than it saves.)
 template <int TM, int TN, int KB = BK>
 __device__ __forceinline__ void ffma_kblock(const float* __restrict__ As, const float* __restrict__ Bs, int tx,
                                             int ty, Acc<TM, TN>& acc) {
@@ -272,11 +273,15 @@ __device__ __forceinline__ void ffma_finish(float* C, int M, int N, int m0, int 
 // SPLIT: some tile's K-loop is shared by several CTAs (else each CTA runs one
 // whole tile and stores it directly; a separate instantiation keeps the
 // fix-up code out of that kernel).
-template <int TM, int TN, bool SPLIT>
+template <int TM, int TN, bool SPLIT, int RBK>
 __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
     ffma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      float* __restrict__ C, int M, int N, int K, int stages, KernelCtl ctl, FfmaSplit ks) {
   using T = Tile<TM, TN>;
+  constexpr int RA_FLOATS = BM * RBK;
+  constexpr int RSTAGE = (BM * RBK + RBK * BN) * 4;
+  constexpr int R = SPLIT_K / RBK;   // slots per unit of a split K-loop
+  static_assert(SPLIT_K % RBK == 0, "split unit");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align1024(smem_raw);
   FfmaBarriers* bar = reinterpret_cast<FfmaBarriers*>(ring + stages * RSTAGE);
@@ -298,8 +303,8 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
   __syncthreads();
   CtaCtl* cta = &bar->ctl;
   int issued = 0;
-  FfmaWork wk(tiles, kt);
-  int tile, k0, k1, seg;
+  FfmaWork wk(tiles, (K + SPLIT_K - 1) / SPLIT_K);
+  int tile, u0, u1, seg;
 
   if (warp == T::WARPS) {
     if (lane == 0) {
@@ -309,9 +314,10 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
       uint32_t ph = 0;
       const bool last_cta = blockIdx.x == gridDim.x - 1;
       bool ok = true;
-      while (ok && wk.next(tile, k0, k1, seg)) {
+      while (ok && wk.next(tile, u0, u1, seg)) {
         int mb, nb;
         tile_coords(tile, m_blocks, n_blocks, mb, nb);
+        const int k0 = u0 * R, k1 = min(u1 * R, kt);
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) { ok = false; break; }
           if (!(ctl.inject_lost_load && last_cta && wk.u >= wk.u_end && kb == k1 - 1)) {
@@ -331,9 +337,10 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
     uint32_t ph = 0;
     bool ok = true;
     int consumed = 0;
-    while (ok && wk.next(tile, k0, k1, seg)) {
+    while (ok && wk.next(tile, u0, u1, seg)) {
       int mb, nb;
       tile_coords(tile, m_blocks, n_blocks, mb, nb);
+      const int k0 = u0 * R, k1 = min(u1 * R, kt);
       Acc<TM, TN> acc;
       acc.zero();
       for (int kb = k0; kb < k1; ++kb) {
@@ -405,11 +412,11 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
   const int m_blocks = (M + BM - 1) / BM, n_blocks = (N + BN - 1) / BN;
   const int kt = (K + BK - 1) / BK;
   const int tx = threadIdx.x % T::TX, ty = threadIdx.x / T::TX;
-  // A K-loop shared by several CTAs is cut at the ring's K steps (RBK), so
-  // every variant adds the same partial sums: each unit is RBK / BK tiles here.
-  constexpr int R = RBK / BK;
-  static_assert(RBK % BK == 0, "ring K step");
-  FfmaWork wk(m_blocks * n_blocks, (K + RBK - 1) / RBK);
+  // A K-loop shared by several CTAs is cut every SPLIT_K K steps, as in the
+  // ring, so every variant adds the same partial sums: a unit is R tiles here.
+  constexpr int R = SPLIT_K / BK;
+  static_assert(SPLIT_K % BK == 0, "split unit");
+  FfmaWork wk(m_blocks * n_blocks, (K + SPLIT_K - 1) / SPLIT_K);
   int tile, u0, u1, seg;
   while (wk.next(tile, u0, u1, seg)) {
     int mb, nb;
@@ -448,7 +455,8 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
 template <int TM, int TN>
 cudaError_t launch_ring_tile(LaunchArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB, const void** kernel) {
   const gp_plan& p = a.plan;
-  auto k = p.k_splits > 1 ? ffma_ring_kernel<TM, TN, true> : ffma_ring_kernel<TM, TN, false>;
+  auto k = p.bk == 32 ? (p.k_splits > 1 ? ffma_ring_kernel<TM, TN, true, 32> : ffma_ring_kernel<TM, TN, false, 32>)
+                      : (p.k_splits > 1 ? ffma_ring_kernel<TM, TN, true, 16> : ffma_ring_kernel<TM, TN, false, 16>);
   *kernel = reinterpret_cast<const void*>(k);
   cudaError_t e = ensure_smem_attr(*kernel, p.smem_bytes);
   if (e != cudaSuccess) return e;
@@ -473,10 +481,12 @@ cudaError_t launch_ffma(LaunchArgs& a, const void** kernel) {
   if (a.variant == GP_PIPELINED) {
     CUtensorMap tmA, tmB;
     const uint64_t M = a.M, N = a.N, K = a.K;
-    if ((e = make_tmap_2d(&tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, K, M, K * 4, RBK, BM,
+    const int rbk = p.bk;   // K steps per ring slot: 32, or 16 for 7-8 slots
+    if (rbk != 32 && rbk != 16) return cudaErrorInvalidValue;
+    if ((e = make_tmap_2d(&tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, K, M, K * 4, rbk, BM,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
       return e;
-    if ((e = make_tmap_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, K, N * 4, BN, RBK,
+    if ((e = make_tmap_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, N, K, N * 4, BN, rbk,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
       return e;
     switch (a.ffma_tm * 100 + a.ffma_tn) {

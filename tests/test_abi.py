@@ -142,8 +142,13 @@ def test_ffma_thread_tiles(gp):
     # the register-tile sweep: outputs per thread TM x TN of the 128 x 128 CTA tile, plus a producer warp
     for (tm, tn) in ((4, 8), (8, 4), (8, 8), (8, 16), (16, 8), (16, 16)):
         p = gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 3, "pipelined", ffma_tile=(tm, tn))
-        assert p["threads"] == (128 // tm) * (128 // tn) + 32 and (p["bm"], p["bn"], p["bk"]) == (128, 128, 16)
-        assert p["stage_bytes"] == (128 * 16 + 16 * 128) * 4
+        assert p["threads"] == (128 // tm) * (128 // tn) + 32 and (p["bm"], p["bn"], p["bk"]) == (128, 128, 32)
+        assert p["stage_bytes"] == (128 * 32 + 32 * 128) * 4
+    # the ring takes 32 K steps per slot up to 6 slots, 16 at 7-8 (eight 32 KB slots would not fit)
+    for S, bk in ((1, 32), (6, 32), (7, 16), (8, 16)):
+        p = gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", S, "pipelined")
+        assert (p["bk"], p["stage_bytes"], p["ring_bytes"]) == (bk, (128 * bk + bk * 128) * 4, S * (128 * bk + bk * 128) * 4)
+        assert p["smem_bytes"] <= 232448
     # the register-staged baselines keep 8 K steps per tile (their thread-to-element mapping)
     for v in ("pingpong", "nopipe"):
         q = gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 0, v)
@@ -299,9 +304,9 @@ def test_ffma_tile_matches_published_kernel_table(gp):
     kb = g["static_smem_per_block_kb"]
     assert round(nop["ring_bytes"] / 1000, 2) == kb["baseline"]
     assert round(pp["ring_bytes"] / 1000, 2) == kb["ping_pong"]
-    # the TMA ring takes 16 K steps per slot where the pages' kernels take 8: per 8 K steps its two
+    # the TMA ring takes 32 K steps per slot where the pages' kernels take 8: per 8 K steps its two
     # slots hold what the pages' two-stage buffer holds
-    assert ring2["bk"] == 2 * t["bk"]
+    assert ring2["bk"] == 4 * t["bk"]
     assert round(ring2["ring_bytes"] * t["bk"] / ring2["bk"] / 1000, 2) == kb["cp_async_2stage"]
 
 
