@@ -178,6 +178,11 @@ typedef struct gp_options {
                                     call's GEMM is still running, into the other of two FP16 copy buffers
                                     (pipelining successive calls); the result is the same.  A promise the
                                     library cannot check: if it is false, A and B may be read too early */
+    int32_t pair_k_split;        /* FP16/BF16 on 256 x 128 CTA-pair tiles (N <= 128): 1 = run each tile on a cluster
+                                    of two pairs that split its K-loop in two halves, the second pair's FP32
+                                    accumulator added by the first through distributed shared memory (at most
+                                    5 stages; plan.cta_pair = 3; GP_ERR_UNSUPPORTED where it does not apply);
+                                    0 = the planner's choice; -1 = never */
 } gp_options;
 
 /*

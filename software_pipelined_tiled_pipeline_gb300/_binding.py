@@ -77,7 +77,7 @@ class GpOptions(ctypes.Structure):
         ("bn", ctypes.c_int32), ("time_kernel", ctypes.c_int32), ("timeout_ns", ctypes.c_uint64),
         ("inject_lost_load", ctypes.c_int32), ("no_stream_k", ctypes.c_int32), ("no_cta_pair", ctypes.c_int32),
         ("i8_engine", ctypes.c_int32), ("ffma_tm", ctypes.c_int32), ("ffma_tn", ctypes.c_int32),
-        ("plan_sms", ctypes.c_int32), ("inputs_ready", ctypes.c_int32),
+        ("plan_sms", ctypes.c_int32), ("inputs_ready", ctypes.c_int32), ("pair_k_split", ctypes.c_int32),
     ]
 
 
@@ -149,7 +149,7 @@ I8_ENGINES = {"default": 0, "imma": 1, "tcgen05_2pass": 2, "tcgen05_overlap": 3}
 
 
 def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-             ffma_tile=None, i8_engine=0, plan_sms=0, inputs_ready=False):
+             ffma_tile=None, i8_engine=0, plan_sms=0, inputs_ready=False, pair_k_split=0):
     opts = GpOptions()
     opts.bn = int(bn)
     opts.time_kernel = 1 if time_kernel else 0
@@ -162,21 +162,23 @@ def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_s
         opts.ffma_tm, opts.ffma_tn = int(ffma_tile[0]), int(ffma_tile[1])
     opts.plan_sms = int(plan_sms)
     opts.inputs_ready = 1 if inputs_ready else 0
+    opts.pair_k_split = int(pair_k_split)
     return opts
 
 
 def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
                    time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-                   ffma_tile=None, i8_engine=0, inputs_ready=False, check=True) -> int:
+                   ffma_tile=None, i8_engine=0, inputs_ready=False, pair_k_split=0, check=True) -> int:
     """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
     stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0.
     ffma_tile: (rows, columns) of outputs per thread of the FP32 ring (default 8 x 8).
     i8_engine: INT8 ring engine, a name of I8_ENGINES or its number ("default" lets the planner pick).
     inputs_ready: promise that no work still in flight on the stream writes A or B (see gp_options).
-    bn=512 (FP16/BF16): two CTA pairs per cluster of four sharing A by TMA multicast."""
+    bn=512 (FP16/BF16): two CTA pairs per cluster of four sharing A by TMA multicast.
+    pair_k_split: 1 = split 256 x 128 tiles' K-loops over two CTA pairs (see gp_options), -1 = never."""
     s = getattr(stream, "cuda_stream", stream)
     opts = _options(bn, time_kernel, timeout_ns, inject_lost_load, no_stream_k, no_cta_pair, ffma_tile, i8_engine,
-                    inputs_ready=inputs_ready)
+                    inputs_ready=inputs_ready, pair_k_split=pair_k_split)
     rc = lib().gemm_pipelined_ex(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"),
                                  _enum(layout, LAYOUTS, "layout"), int(stages), _enum(variant, VARIANTS, "variant"),
                                  s or None, ctypes.byref(opts))

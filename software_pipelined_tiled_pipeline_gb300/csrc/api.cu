@@ -340,7 +340,7 @@ void apply_i8_halves(gp_plan* p, int64_t workers) {
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
               int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, int i8_engine = 0,
-              int ffma_tm = 0, int ffma_tn = 0, bool no_mc = false) {
+              int ffma_tm = 0, int ffma_tn = 0, bool no_mc = false, int pair_k_split = 0) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
@@ -383,6 +383,8 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   const bool ring = variant == GP_PIPELINED;
 
   if (i8_engine < 0 || i8_engine > 3) return GP_ERR_ARG;
+  if (pair_k_split < -1 || pair_k_split > 1) return GP_ERR_ARG;
+  if (pair_k_split == 1 && (fam != 2 || !ring)) return GP_ERR_UNSUPPORTED;   // FP16/BF16 ring only
   const int i8_tc_stages = stages == 0 ? 6 : S;
   if (fam == 1 && ring && i8_engine != 1 && !no_pair && (bn_req == 0 || bn_req == 256) &&
       ring_smem_total(i8_tc_stages * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax) {
@@ -480,6 +482,27 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   const bool mc = pair256 && !no_mc && (sm_count == 0 || sm_count >= 8) && bn_req == 512;
   if (bn_req == 512 && !mc) return GP_ERR_UNSUPPORTED;
   const bool pair128 = pair_base && !pair256 && bn_req == 0 && N > 64 && M > 128 && pair_fits(128);
+  // pair_k_split: a cluster of two pairs splits each 256 x 128 tile's K-loop
+  // in two halves and adds them through distributed shared memory (for few
+  // tiles and long K-loops, instead of stream-K partial tiles in L2); its
+  // 64 KB receive buffer leaves room for at most 5 stages.
+  const int kx_S = stages == 0 ? 5 : S;
+  const bool kx_able = pair128 && ceil_div(K, kUmmaBK) >= 2 && (sm_count == 0 || sm_count >= 8) &&
+                       ring_smem_total(kx_S * (kUmmaBM + 64) * kUmmaBK * 2, kUmmaEpiBytes + kUmmaKxBytes) <=
+                           kSmemPerCtaMax;
+  if (pair_k_split == 1 && !kx_able) return GP_ERR_UNSUPPORTED;
+  // By default where the tiles about fill the clusters of four (more than
+  // SMs/8, at most SMs/4) and the K-loops are long: measured at BF16 8192 x
+  // 128 x 8192 (32 tiles), 32.3 us against 38.1 us with stream-K over 76
+  // pairs.  Fewer tiles keep stream-K, which spreads them over more SMs.
+  const int64_t kx_tiles = ceil_div(M, 256) * ceil_div(N, 128);
+  const bool kx_default = sm_count > 0 && kx_tiles > sm_count / 8 && kx_tiles <= sm_count / 4 &&
+                          ceil_div(K, kUmmaBK) >= 32;
+  const bool kx = kx_able && (pair_k_split == 1 || (pair_k_split == 0 && kx_default));
+  if (kx) {
+    S = kx_S;
+    p->stages = S;
+  }
   const bool pair_ok = pair256 || pair128;
   const int pair_bn = pair256 ? 256 : 128;
   int bn = 0;
@@ -532,11 +555,16 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
       p->bn = 512;   // the cluster's tile; each pair computes 256 x 256 of it
       p->kernel = "umma_pair_mc_ring";
     }
+    if (kx) {
+      p->cta_pair = 3;
+      p->kernel = "umma_pair_ksplit_ring";
+      p->smem_bytes = ring_smem_total(p->ring_bytes, kUmmaEpiBytes + kUmmaKxBytes);
+    }
   }
   p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
   p->k_tiles = ceil_div(K, p->bk);
   if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
-  if (p->cta_pair == 2)
+  if (p->cta_pair == 2 || p->cta_pair == 3)
     p->grid = sm_count > 3 ? static_cast<int32_t>(4 * (p->tiles < sm_count / 4 ? p->tiles : sm_count / 4)) : 0;
   else if (p->cta_pair)
     p->grid = sm_count > 1 ? static_cast<int32_t>(2 * (p->tiles < sm_count / 2 ? p->tiles : sm_count / 2)) : 0;
@@ -570,6 +598,8 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   if (fam == 2 && ring && sm_count > 0) {
     if (p->cta_pair == 2)
       apply_stream_k(p, sm_count / 4, 4, !no_stream_k);
+    else if (p->cta_pair == 3)
+      ;   // whole tiles, each K-loop split over the cluster's two pairs
     else if (p->cta_pair)
       apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
     else
@@ -739,7 +769,7 @@ using namespace gp;
 
 extern "C" {
 
-int gemm_abi_version(void) { return 10400; }
+int gemm_abi_version(void) { return 10500; }
 
 const char* gemm_strerror(int code) {
   switch (code) {
@@ -785,7 +815,8 @@ int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int sta
   }
   const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
   return plan_impl(M, N, K, dtype, layout, stages, variant, opts ? opts->bn : 0, sms, out, opts && opts->no_stream_k,
-                   no_pair, opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
+                   no_pair, opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, false,
+                   opts ? opts->pair_k_split : 0);
 }
 
 int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
@@ -801,7 +832,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   gp_plan plan;
   int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan, opts && opts->no_stream_k,
                      opts && (opts->no_cta_pair || opts->inject_lost_load), opts ? opts->i8_engine : 0,
-                     opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
+                     opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, false, opts ? opts->pair_k_split : 0);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }   // empty output: nothing read or written
@@ -840,8 +871,16 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   } else {
     const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
     rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
-                   opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0);
+                   opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, false,
+                   opts ? opts->pair_k_split : 0);
     if (rc != GP_OK) { record(rc, 0); return rc; }
+    if (plan.cta_pair == 3) {
+      int clusters = 0;
+      e = umma_kx_capacity(dtype, plan.smem_bytes, &clusters);
+      if (e == cudaSuccess && clusters < 1) e = cudaErrorLaunchOutOfResources;
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (4 * clusters < plan.grid) plan.grid = 4 * clusters;
+    }
     if (plan.cta_pair == 2) {
       // clusters of four sit on two TPCs of one GPC each: fewer than SMs / 4
       // may be resident (36 on a 152-SM GB300); stream-K over those

@@ -123,6 +123,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// The same wait with cluster-scope acquire: writes that other CTAs of the
+// cluster made before a release-arrive on `bar` are visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t parity, const KernelCtl& ctl,
+                                                      CtaCtl* cta, uint32_t site) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_acq_cluster(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_acq_cluster(a, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (cta->abort) return false;
+      if (global_timer_ns() - t0 > ctl.timeout_ns) {
+        report_error(ctl.status, kDevErrTimeout, site);
+        cta->abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Registers per thread of the executing warpgroup (all four warps must run it).
 template <int N>
 __device__ __forceinline__ void regs_increase() {
@@ -326,6 +358,13 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensor
       "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask)
       : "memory");
+}
+
+// Store 16 bytes into another CTA's shared memory (cluster-window address).
+__device__ __forceinline__ void st_cluster_f4(uint32_t cluster_addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
 }
 
 // TMEM management for a CTA pair: one warp of EACH CTA executes these together.

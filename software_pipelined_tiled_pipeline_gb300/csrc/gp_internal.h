@@ -25,6 +25,7 @@ enum WaitSite : uint32_t {
   kSiteDrain = 6,
   kSiteConvReady = 7,     // INT8 overlap engine: producer waiting for a K step's FP16 copies
   kSiteConvRing = 8,      // INT8 overlap engine: converter / signaller hand-off
+  kSiteKSplitXfer = 9,    // K split over two pairs: accumulator hand-off between the pairs
 };
 
 struct KernelCtl {
@@ -97,6 +98,9 @@ constexpr int kUmmaEpiRows = 32;         // rows per epilogue warp (one TMEM lan
 constexpr int kUmmaEpiCols = 64;         // 16-bit columns per staged chunk (128 bytes)
 constexpr int kUmmaEpiBufBytes = kUmmaEpiRows * kUmmaEpiCols * 2;
 constexpr int kUmmaEpiBytes = kUmmaEpiWarps * 2 * kUmmaEpiBufBytes;   // double-buffered per warp
+// K split over the two pairs of a cluster (256 x 128 tiles): one CTA's 128 x 128 FP32 half of the
+// other pair's accumulator, received through distributed shared memory.
+constexpr int kUmmaKxBytes = 128 * 128 * 4;
 // CTA-pair kernel: 256 x 256 output tile per pair, 128 rows of A and of B per CTA.
 constexpr int kUmmaPairStageBytes = 2 * 128 * kUmmaBK * 2;             // per CTA per K step
 __host__ __device__ constexpr int umma_stage_bytes(int bn) { return (kUmmaBM + bn) * kUmmaBK * 2; }
@@ -158,6 +162,8 @@ cudaError_t launch_umma(LaunchArgs& a, const void** kernel);
 cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs, bool i8_overlap = false);
 // Clusters of four CTAs (two pairs sharing A by multicast) resident at once.
 cudaError_t umma_mc_capacity(int dtype, int smem_bytes, int* clusters);
+// Clusters of four CTAs (two pairs splitting each 256 x 128 tile's K-loop) resident at once.
+cudaError_t umma_kx_capacity(int dtype, int smem_bytes, int* clusters);
 // INT8 x INT8 -> INT32 on tcgen05 (FP16 operands, accumulator restarted every 1024 K).
 cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel);
 cudaError_t launch_zero_fill(void* C, int64_t bytes, cudaStream_t stream);

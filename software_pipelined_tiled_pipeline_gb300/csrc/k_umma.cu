@@ -49,6 +49,7 @@ struct UmmaBarriers {
   uint64_t acc_empty[2];
   uint64_t mma_done[2];
   uint64_t drain;
+  uint64_t xfull, xempty;     // K split over two pairs: the other pair's accumulator half is in xbuf / xbuf is free
   uint32_t tmem_base;
   int32_t consumed_hi;        // k-blocks consumed by the MMA thread (low 31 bits)
   CtaCtl ctl;
@@ -332,7 +333,7 @@ struct RingShape {
   static_assert(EPI_BUFS >= 1 && WARP_CHUNKS >= 1, "epilogue split");
 };
 
-template <int BN, bool BF16, bool PAIR, bool MC>
+template <int BN, bool BF16, bool PAIR, bool MC, bool KX>
 __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     umma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl,
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
   uint8_t* ring = smem;
   uint8_t* epi = smem + stages * STAGE;
   UmmaBarriers* bar = reinterpret_cast<UmmaBarriers*>(epi + kUmmaEpiBytes);
+  float4* xbuf = reinterpret_cast<float4*>(epi + kUmmaEpiBytes + kBarrierRegion);   // KX only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -353,11 +355,15 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
   // columns p*BN .. +BN.  Both pairs read the same 256 rows of A: each CTA
   // receives its 128 rows half from its own multicast load and half from the
   // one of the CTA with the same rank in the other pair (see the producer).
-  constexpr int CL = MC ? 4 : (PAIR ? 2 : 1);                 // CTAs per worker (one cluster)
+  // KX: a cluster of two CTA pairs computes one 256 x BN tile, pair p the
+  // K steps p*ceil(kt/2) .. of it; pair 1 sends its FP32 accumulator through
+  // distributed shared memory to pair 0, which adds it and writes C.
+  constexpr int CL = (MC || KX) ? 4 : (PAIR ? 2 : 1);         // CTAs per worker (one cluster)
   static_assert(!MC || PAIR, "multicast runs on CTA pairs");
+  static_assert(!KX || (PAIR && !MC && BN == 128), "K split runs on 256 x 128 pair tiles");
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;      // rank in the cluster
   const uint32_t rank = crank & 1u;                           // rank in the CTA pair
-  const int pidx = MC ? static_cast<int>(crank >> 1) : 0;     // pair within the cluster
+  const int pidx = (MC || KX) ? static_cast<int>(crank >> 1) : 0;   // pair within the cluster
   const bool leader = rank == 0;
   const uint32_t lead_rank = crank & ~1u;                     // this pair's even CTA
   const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead_rank);
@@ -379,6 +385,8 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       mbar_init(&bar->acc_empty[a], Sh::CTAS * Sh::EPI_WARPS);
     }
     mbar_init(&bar->drain, 1);
+    mbar_init(&bar->xfull, Sh::EPI_THREADS);    // every epilogue thread of the sending CTA
+    mbar_init(&bar->xempty, Sh::EPI_THREADS);   // every epilogue thread of the receiving CTA
     bar->ctl.abort = 0;
     bar->consumed_hi = 0;
     fence_mbar_init();
@@ -414,17 +422,26 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
   WorkIter it;
   it.init(sk, kt, worker, workers);
   int tile, k0, k1;
+  // the work items of this CTA (KX: this pair's half of each tile's K-loop)
+  auto next_item = [&](int& t_, int& a_, int& b_) {
+    if (!it.next(t_, a_, b_)) return false;
+    if (KX) {
+      const int h = (kt + 1) / 2;
+      if (pidx == 0) b_ = h; else a_ = h;
+    }
+    return true;
+  };
 
   if (warp == 0) {
     // ---------------- producer (every CTA) ----------------
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      while (!cta->abort && it.next(tile, k0, k1)) {
+      while (!cta->abort && next_item(tile, k0, k1)) {
         int mb, nb;
         tile_coords(tile, m_blocks, n_blocks, mb, nb);
         const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
-        const int n_row = (nb * (MC ? 2 : 1) + pidx) * BN + rank * Sh::B_ROWS;
+        const int n_row = (nb * (MC ? 2 : 1) + (MC ? pidx : 0)) * BN + rank * Sh::B_ROWS;
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto producer_done;
           uint8_t* slot = ring + s * STAGE;
@@ -460,7 +477,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       int consumed = 0;
-      for (int t = 0; it.next(tile, k0, k1); ++t) {
+      for (int t = 0; next_item(tile, k0, k1); ++t) {
         const int a = t & 1;
         if (!mbar_wait(&bar->acc_empty[a], ((t >> 1) & 1) ^ 1u, ctl, cta, kSiteMmaAccEmpty)) break;
         tc_fence_after();
@@ -482,7 +499,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
               umma_f16(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
           }
           // slot s is free (in every CTA that loaded into it) once these MMAs have read it
-          if (PAIR) umma_commit_pair(&bar->empty[s], MC ? 0xF : 0x3); else umma_commit(&bar->empty[s]);
+          if (PAIR) umma_commit_pair(&bar->empty[s], MC ? 0xF : pair_mask); else umma_commit(&bar->empty[s]);
           ++consumed;
           if (++s == stages) { s = 0; ph ^= 1u; }
         }
@@ -504,13 +521,13 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     const int c_end = c_begin + Sh::WARP_CHUNKS;
     uint8_t* my_stage = epi + e * Sh::EPI_BUFS * kUmmaEpiBufBytes;
     int sb = 0;
-    for (int t = 0; it.next(tile, k0, k1); ++t) {
+    for (int t = 0; next_item(tile, k0, k1); ++t) {
       int mb, nb;
       tile_coords(tile, m_blocks, n_blocks, mb, nb);
       const int a = t & 1;
       // A split tile (stream-K): every segment stores its FP32 partial; the
       // segment that completes last sums all of them in K order and writes C.
-      const bool split = (k0 > 0) || (k1 < kt);
+      const bool split = !KX && ((k0 > 0) || (k1 < kt));
       SplitTile sp;
       if (split) sp.init(tile, kt, sk, workers, CL, crank);
       uint32_t ok = 1;
@@ -531,7 +548,56 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       tc_fence_after();
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
       const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
-      const int x0 = (nb * (MC ? 2 : 1) + pidx) * BN;   // first column of this pair's tile
+      const int x0 = (nb * (MC ? 2 : 1) + (MC ? pidx : 0)) * BN;   // first column of this pair's tile
+      if (KX) {
+        // K split over the two pairs: pair 1 sends its FP32 half of the
+        // accumulator to the CTA of the same pair rank in pair 0 (row-
+        // innermost float4 groups, conflict-free), which adds it to its own
+        // half and writes C.  xfull / xempty hand the 64 KB buffer back and forth.
+        const uint32_t xph = static_cast<uint32_t>(t & 1);
+        const bool xok = pidx == 1 ? mbar_wait_acq_cluster(&bar->xempty, xph ^ 1u, ctl, cta, kSiteKSplitXfer)
+                                   : mbar_wait_acq_cluster(&bar->xfull, xph, ctl, cta, kSiteKSplitXfer);
+        if (!epi_bar_and<Sh::EPI_THREADS>(xok && !cta->abort)) break;
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; ++c) {
+          uint32_t v[64];
+          load_acc_chunk(trow + c * kUmmaEpiCols, v);
+          if (c == c_end - 1) {
+            // all of accumulator a is in registers: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bar->acc_empty[a]), lead_rank));
+          }
+          float4* xb = xbuf + static_cast<size_t>(c) * 16 * Sh::A_ROWS + row;
+          if (pidx == 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              st_cluster_f4(mapa_shared(smem_u32(xb + i * Sh::A_ROWS), crank - 2u),
+                            make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                        __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+            continue;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 p = xb[i * Sh::A_ROWS];
+            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + p.x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + p.y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + p.z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + p.w);
+          }
+          if (lane == 0) bulk_wait_read<Sh::EPI_BUFS - 1>();
+          __syncwarp();
+          const int x = x0 + c * kUmmaEpiCols;
+          stage_and_store<BF16>(v, my_stage + sb * kUmmaEpiBufBytes, lane, &tmC, x, y, (x < N) && (y < M));
+          if (++sb == Sh::EPI_BUFS) sb = 0;
+        }
+        // release: the sent half is visible to pair 0 / the buffer may be refilled
+        if (pidx == 1)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&bar->xfull), crank - 2u));
+        else
+          mbar_arrive_cluster(mapa_shared(smem_u32(&bar->xempty), crank + 2u));
+        continue;
+      }
       if (!split) {
         // Whole tile: the TMEM load of chunk c + 1 is in flight while chunk c
         // is converted, staged and stored (chunks unrolled, so no register
@@ -1724,7 +1790,7 @@ __global__ void __launch_bounds__(kPPThreads, 1)
   }
 }
 
-template <int BN, bool BF16, bool PAIR, bool MC = false>
+template <int BN, bool BF16, bool PAIR, bool MC = false, bool KX = false>
 cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   using Sh = RingShape<BN, PAIR>;
   const gp_plan& p = a.plan;
@@ -1741,7 +1807,7 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
     return e;
   if ((e = make_tmap_2d(&tmB, a.B, dt, K, N, K * 2, BK, Sh::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
-  auto k = umma_ring_kernel<BN, BF16, PAIR, MC>;
+  auto k = umma_ring_kernel<BN, BF16, PAIR, MC, KX>;
   *kernel = reinterpret_cast<const void*>(k);
   if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1753,7 +1819,7 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   int n = 0;
   if (PAIR) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = MC ? 4 : 2;
+    attr[n].val.clusterDim.x = (MC || KX) ? 4 : 2;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -1916,16 +1982,18 @@ cudaError_t launch_i8_overlap(LaunchArgs& a, const void** kernel) {
 
 // Largest number of CTA pairs of a pair kernel that can be resident at once.
 // kind: 0 FP16 ring, 1 BF16 ring, 2 INT8 two-pass, 3 INT8 with the conversion overlapped.
-// Clusters of `size` CTAs (2: one pair; 4: two pairs sharing A, kinds 0-1)
-// resident at once at this shared-memory size.
-cudaError_t max_clusters(int kind, int smem_bytes, int size, int* clusters) {
-  const bool mc = size == 4;
+// Clusters of `size` CTAs (2: one pair; 4: two pairs, sharing A (kx false)
+// or splitting K (kx true), kinds 0-1) resident at once at this shared-memory size.
+cudaError_t max_clusters(int kind, int smem_bytes, int size, int* clusters, bool kx = false) {
+  const bool mc = size == 4 && !kx;
   const void* k = kind == 3   ? reinterpret_cast<const void*>(umma_i8_overlap_kernel)
                   : kind == 2 ? reinterpret_cast<const void*>(umma_i8_kernel<true>)
-                  : kind == 1 ? (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, true>)
-                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, false>))
-                              : (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, true>)
-                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, false>));
+                  : kx ? (kind == 1 ? reinterpret_cast<const void*>(umma_ring_kernel<128, true, true, false, true>)
+                                    : reinterpret_cast<const void*>(umma_ring_kernel<128, false, true, false, true>))
+                  : kind == 1 ? (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, true, false>)
+                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, false, false>))
+                              : (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, true, false>)
+                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, false, false>));
   cudaError_t e = ensure_smem_attr(k, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1945,6 +2013,7 @@ cudaError_t max_clusters(int kind, int smem_bytes, int size, int* clusters) {
 template <bool BF16>
 cudaError_t launch_dtype(LaunchArgs& a, const void** kernel) {
   if (a.plan.cta_pair == 2) return launch_ring<256, BF16, true, true>(a, kernel);
+  if (a.plan.cta_pair == 3) return launch_ring<128, BF16, true, false, true>(a, kernel);
   if (a.plan.cta_pair)
     return a.plan.bn == 128 ? launch_ring<128, BF16, true>(a, kernel) : launch_ring<256, BF16, true>(a, kernel);
   switch (a.plan.bn) {
@@ -1968,6 +2037,10 @@ cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs, bool i8_ov
 
 cudaError_t umma_mc_capacity(int dtype, int smem_bytes, int* clusters) {
   return max_clusters(dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0, smem_bytes, 4, clusters);
+}
+
+cudaError_t umma_kx_capacity(int dtype, int smem_bytes, int* clusters) {
+  return max_clusters(dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0, smem_bytes, 4, clusters, true);
 }
 
 cudaError_t launch_umma_i8(LaunchArgs& a, const void** kernel) {

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_function(gp):
 
 
 def test_version_and_strerror(gp):
-    assert gp.abi_version() == 10400
+    assert gp.abi_version() == 10500
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert gp.strerror(code) and "unknown" not in gp.strerror(code)
     assert "unknown" in gp.strerror(-99)
@@ -133,8 +133,8 @@ def test_default_depth_follows_k(gp):
     for K, S in ((256, 4), (1024, 6), (2048, 6), (4096, 5), (16384, 5)):
         assert gp.gemm_plan(8192, 8192, K, "bf16", "row_col", 0, "pipelined")["stages"] == S, K
     assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined")["stages"] == 6
-    # 64 < N <= 128 on the 256 x 128 pair tile: the deepest ring
-    p = gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined")
+    # 64 < N <= 128 on the 256 x 128 pair tile: the deepest ring (with the K split: 5, see below)
+    p = gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined", pair_k_split=-1)
     assert (p["stages"], p["cta_pair"], p["bn"]) == (8, 1, 128)
 
 
@@ -344,6 +344,33 @@ def test_multicast_tile_plan(gp):
     for M, N, K, dt, lay in [(4096, 4096, 256, "f16", "row_col"), (4096, 4096, 4096, "f32", "row_row"),
                              (4096, 4096, 4096, "i8", "row_col"), (4096, 128, 4096, "bf16", "row_col")]:
         assert gp.gemm_plan_rc(M, N, K, dt, lay, 0, "pipelined", bn=512) == gp.GP_ERR_UNSUPPORTED
+
+
+def test_pair_k_split_plan(gp):
+    # pair_k_split = 1: each 256 x 128 tile on a cluster of two CTA pairs, each pair half of the
+    # K-loop; no stream-K; at most 5 stages (the 64 KB receive buffer)
+    kw = dict(plan_sms=152, pair_k_split=1)
+    p = gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined", **kw)
+    assert (p["kernel"], p["cta_pair"], p["bm"], p["bn"], p["stages"]) == ("umma_pair_ksplit_ring", 3, 256, 128, 5)
+    assert (p["tiles"], p["grid"], p["dp_tiles"], p["sk_tiles"], p["workspace_bytes"]) == (32, 128, 32, 0, 0)
+    assert p["smem_bytes"] <= 232448
+    # the planner's choice: 32 tiles (more than 152/8, at most 152/4) and 128 K steps -> the K split
+    d = gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined", plan_sms=152)
+    assert (d["cta_pair"], d["stages"]) == (3, 5)
+    assert gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined", plan_sms=152,
+                        pair_k_split=-1)["cta_pair"] == 1
+    # fewer tiles (stream-K over all pairs), short K-loops, or no device: CTA pairs
+    assert gp.gemm_plan(2048, 128, 8192, "bf16", "row_col", 0, "pipelined", plan_sms=152)["cta_pair"] == 1
+    assert gp.gemm_plan(8192, 128, 1024, "bf16", "row_col", 0, "pipelined", plan_sms=152)["cta_pair"] == 1
+    assert gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined")["cta_pair"] == 1
+    with pytest.raises(gp.GemmError):   # 6 stages leave no room for the receive buffer
+        gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 6, "pipelined", **kw)
+    for M, N, K, dt in [(4096, 4096, 4096, "f16"), (8192, 128, 256, "bf16"), (4096, 128, 4096, "i8")]:
+        assert gp.gemm_plan_rc(M, N, K, dt, "row_col", 0, "pipelined") == 0
+        with pytest.raises(gp.GemmError):
+            gp.gemm_plan(M, N, K, dt, "row_col", 0, "pipelined", pair_k_split=1)
+    with pytest.raises(gp.GemmError):
+        gp.gemm_plan(8192, 128, 8192, "bf16", "row_col", 0, "pipelined", pair_k_split=2)
 
 
 def test_planner_for_a_152_sm_gb300(gp):

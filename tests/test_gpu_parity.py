@@ -267,6 +267,36 @@ def test_multicast_pair_kernel(dtype, M, N, K, S):
     assert torch.equal(Cd.view(torch.int16), C2.view(torch.int16))
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K,S", [(1000, 120, 2056, 5), (520, 128, 1032, 4), (256, 72, 264, 3), (2056, 104, 4104, 5)])
+def test_pair_k_split_kernel(dtype, M, N, K, S):
+    # each 256 x 128 tile on two CTA pairs, one per half of the K-loop, the halves added through
+    # distributed shared memory; ragged in M, N and K (odd numbers of K steps included)
+    lay = "row_col"
+    A, B = operands(dtype, lay, M, N, K, seed=M + 5 * N + K)
+    C, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, pair_k_split=1)
+    p = st["plan"]
+    assert p["cta_pair"] == 3 and p["kernel"] == "umma_pair_ksplit_ring" and p["grid"] % 4 == 0
+    check_full(dtype, lay, A, B, C, K)
+
+
+def test_pair_k_split_full_skinny_and_repeats():
+    # the skinny BF16 workload (8192 x 128 x 8192) at full size, sampled, then repeated launches
+    M, N, K = 8192, 128, 8192
+    A, B = operands("bf16", "row_col", M, N, K, seed=5)
+    tA, tB = to_dev(A, "bf16"), to_dev(B, "bf16")
+    outs = [torch.empty(M * N, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for C in outs:
+        gp.gemm_pipelined(tA, tB, C, M, N, K, "bf16", "row_col", 0, "pipelined", torch.cuda.current_stream(),
+                          pair_k_split=1)
+    st = gp.gemm_stats(sync=True)
+    assert st["status"] == 0 and st["device_status"] == 0 and st["plan"]["cta_pair"] == 3
+    check_sampled("bf16", "row_col", A, B, outs[0].view(M, N).cpu(), K, rows=[0, 1, 255, 256, 4095, M - 1],
+                  npts=2000, seed=3)
+    for C in outs[1:]:
+        assert torch.equal(C, outs[0])
+
+
 def test_multicast_pair_repeated_launches():
     # back-to-back launches (programmatic dependent launch, stream-K workspace reused) stay exact
     M, N, K = 1024, 2048, 2048
