@@ -325,6 +325,9 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
             # two CTA pairs per cluster of four on a 256 x 512 tile, A shared by TMA multicast
             if w.K > 256 and w.N > 256:
                 cases += [("pipelined", S, {"bn": 512}) for S in (5, 6)]
+            # the caller's promise that the inputs are in place: each launch's loads and MMAs
+            # start while the previous launch finishes (only its stores wait)
+            cases += [("pipelined", 5, {"inputs_ready": True})]
         if w.dtype == "i8":
             # the TMA ring feeding warp-level IMMA (the ping-pong and no-overlap rows use IMMA too)
             cases += [("pipelined", S, {"i8_engine": "imma"}) for S in w.stages]

@@ -176,8 +176,10 @@ typedef struct gp_options {
                                     or B (they were in place before the previous call on this stream was made).
                                     INT8 on tcgen05 (two-pass engine) then converts them while the previous
                                     call's GEMM is still running, into the other of two FP16 copy buffers
-                                    (pipelining successive calls); the result is the same.  A promise the
-                                    library cannot check: if it is false, A and B may be read too early */
+                                    (pipelining successive calls); FP16/BF16 on tcgen05 then starts its loads
+                                    and MMAs while the previous kernel on the stream is still finishing (only
+                                    its stores wait).  The result is the same.  A promise the library cannot
+                                    check: if it is false, A and B may be read too early */
     int32_t pair_k_split;        /* FP16/BF16 on 256 x 128 CTA-pair tiles (N <= 128): 1 = run each tile on a cluster
                                     of two pairs that split its K-loop in two halves, the second pair's FP32
                                     accumulator added by the first through distributed shared memory (at most

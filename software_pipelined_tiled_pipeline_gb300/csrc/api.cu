@@ -949,6 +949,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.ctl.status = status;
     a.ctl.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     a.ctl.inject_lost_load = opts ? opts->inject_lost_load : 0;
+    a.ctl.inputs_ready = (opts && opts->inputs_ready) ? 1 : 0;
     a.sm_count = sms;
     a.sk = sk;
     a.ks = ks;
@@ -1105,6 +1106,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.ctl.status = status;
     a.ctl.timeout_ns = kDefaultTimeoutNs;
     a.ctl.inject_lost_load = 0;
+    a.ctl.inputs_ready = 0;
     a.sm_count = sms;
     a.sk = sk;
     a.ks = FfmaSplit{1, nullptr, nullptr, 0};

@@ -32,6 +32,8 @@ struct KernelCtl {
   uint32_t* status;         // device word, 0 = clean
   uint64_t timeout_ns;      // limit of every bounded wait
   int32_t inject_lost_load; // test hook: producer skips the final tile load
+  int32_t inputs_ready;     // FP16/BF16 ring: the caller promised that nothing in flight writes A or B,
+                            // so loads and MMAs may start before the previous kernel has completed
 };
 
 // Stream-K split of a persistent launch over W workers (CTAs, or CTA pairs):

@@ -415,7 +415,10 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
   // of the previous kernel; from here on the operands, C and the stream-K
   // workspace may be touched only once that kernel has completed.
   pdl_launch_dependents();
-  pdl_wait();
+  // With the caller's promise that nothing in flight writes A or B, the
+  // producer and the MMA issuer start while the previous kernel is still
+  // finishing; only the epilogue (C, the stream-K workspace) waits for it.
+  if (!ctl.inputs_ready) pdl_wait();
   const uint32_t tmem = bar->tmem_base;
   CtaCtl* cta = &bar->ctl;
   int issued = 0;  // producer only
@@ -514,6 +517,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     }
   } else {
     // ---------------- epilogue (warps 2..5 of every CTA) ----------------
+    if (ctl.inputs_ready) pdl_wait();
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int e = warp - 2;
     const int row = q * 32 + lane;      // accumulator row of this CTA that this thread holds

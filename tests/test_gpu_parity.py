@@ -297,6 +297,26 @@ def test_pair_k_split_full_skinny_and_repeats():
         assert torch.equal(C, outs[0])
 
 
+@pytest.mark.parametrize("dtype,M,N,K", [("f16", 4096, 4096, 4096), ("bf16", 1000, 1800, 1040), ("f16", 8192, 128, 8192)])
+def test_inputs_ready_fp16_bf16_back_to_back(dtype, M, N, K):
+    # with the promise, each launch's loads and MMAs start while the previous launch finishes and
+    # only its stores wait: results identical to ordinary launches (stream-K and K-split shapes too)
+    A, B = operands(dtype, "row_col", M, N, K, seed=M + N + K)
+    tA, tB = to_dev(A, dtype), to_dev(B, dtype)
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
+    ref = torch.empty(M * N, dtype=tdt, device="cuda")
+    stream = torch.cuda.current_stream()
+    gp.gemm_pipelined(tA, tB, ref, M, N, K, dtype, "row_col", 0, "pipelined", stream)
+    outs = [torch.empty(M * N, dtype=tdt, device="cuda") for _ in range(4)]
+    for C in outs:
+        gp.gemm_pipelined(tA, tB, C, M, N, K, dtype, "row_col", 0, "pipelined", stream, inputs_ready=True)
+    st = gp.gemm_stats(sync=True)
+    assert st["status"] == 0 and st["device_status"] == 0
+    for C in outs:
+        assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    check_sampled(dtype, "row_col", A, B, ref.view(M, N).cpu(), K, rows=[0, 255, 256, M - 1], npts=1500, seed=1)
+
+
 def test_multicast_pair_repeated_launches():
     # back-to-back launches (programmatic dependent launch, stream-K workspace reused) stay exact
     M, N, K = 1024, 2048, 2048
