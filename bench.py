@@ -328,6 +328,10 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
             # the caller's promise that the inputs are in place: each launch's loads and MMAs
             # start while the previous launch finishes (only its stores wait)
             cases += [("pipelined", 5, {"inputs_ready": True})]
+        if w.dtype == "f32":
+            # the caller's promise that the inputs are in place: each launch's loads and FMAs
+            # start while the previous launch finishes (only its stores wait)
+            cases += [("pipelined", 3, {"inputs_ready": True})]
         if w.dtype == "i8":
             # the TMA ring feeding warp-level IMMA (the ping-pong and no-overlap rows use IMMA too)
             cases += [("pipelined", S, {"i8_engine": "imma"}) for S in w.stages]

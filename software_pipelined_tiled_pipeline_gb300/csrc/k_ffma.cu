@@ -301,6 +301,12 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  // Launched as a programmatic dependent: the set-up above overlaps the
+  // previous kernel's tail.  The producer reads A and B only after that
+  // kernel has completed (or at once, when the caller promised that nothing
+  // in flight writes them); the compute warps write C and the split
+  // workspace only after it has completed.
+  pdl_launch_dependents();
   CtaCtl* cta = &bar->ctl;
   int issued = 0;
   FfmaWork wk(tiles, (K + SPLIT_K - 1) / SPLIT_K);
@@ -313,6 +319,7 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
       int s = 0;
       uint32_t ph = 0;
       const bool last_cta = blockIdx.x == gridDim.x - 1;
+      if (!ctl.inputs_ready) pdl_wait();
       bool ok = true;
       while (ok && wk.next(tile, u0, u1, seg)) {
         int mb, nb;
@@ -337,6 +344,7 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
     uint32_t ph = 0;
     bool ok = true;
     int consumed = 0;
+    bool waited = false;
     while (ok && wk.next(tile, u0, u1, seg)) {
       int mb, nb;
       tile_coords(tile, m_blocks, n_blocks, mb, nb);
@@ -355,6 +363,10 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
       }
       // one decision for all compute warps: a timed-out warp must not leave the others at a barrier
       ok = compute_bar_and<T::THREADS>(ok);
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
       if (ok) {
         if (SPLIT)
           ffma_finish<TM, TN>(C, M, N, mb * BM, nb * BN, wk, tile, seg, ks, tx, ty, threadIdx.x, acc, &bar->last);
@@ -460,9 +472,17 @@ cudaError_t launch_ring_tile(LaunchArgs& a, const CUtensorMap& tmA, const CUtens
   *kernel = reinterpret_cast<const void*>(k);
   cudaError_t e = ensure_smem_attr(*kernel, p.smem_bytes);
   if (e != cudaSuccess) return e;
-  k<<<p.grid, Tile<TM, TN>::THREADS + 32, p.smem_bytes, a.stream>>>(tmA, tmB, static_cast<float*>(a.C), a.M, a.N,
-                                                                      a.K, p.stages, a.ctl, a.ks);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(Tile<TM, TN>::THREADS + 32);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait() in the kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, tmA, tmB, static_cast<float*>(a.C), a.M, a.N, a.K, p.stages, a.ctl, a.ks);
 }
 
 }  // namespace
