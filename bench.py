@@ -322,9 +322,6 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
         if w.dtype in ("f16", "bf16"):
             # the same ring on one CTA per 128-row tile, whole tiles only (no pairs, no stream-K)
             cases += [("pipelined", S, {"no_cta_pair": True, "no_stream_k": True}) for S in (4, 6)]
-            # two CTA pairs per cluster of four on a 256 x 512 tile, A shared by TMA multicast
-            if w.K > 256 and w.N > 256:
-                cases += [("pipelined", S, {"bn": 512}) for S in (5, 6)]
             # the caller's promise that the inputs are in place: each launch's loads and MMAs
             # start while the previous launch finishes (only its stores wait)
             cases += [("pipelined", 5, {"inputs_ready": True})]

@@ -124,11 +124,8 @@ typedef struct gp_plan {
                                     partial tiles of split K-loops; for INT8 on tcgen05 also the FP16 copies */
     int32_t cta_pair;            /* 1: two CTAs (a cluster on one TPC) share each BM x BN tile, each holding
                                     BM/2 rows of A and BN/2 rows of B; stage_bytes and smem_bytes are per CTA.
-                                    2 (gp_options.bn = 512): a cluster of four CTAs (two such pairs) shares
-                                    each 256 x 512 tile, pair p computing its columns p*256 .. +255; both
-                                    pairs need the same A rows, which each CTA loads half of by TMA multicast
-                                    to itself and to the CTA of the same pair rank in the other pair (tiles,
-                                    dp_tiles and sk_tiles count 256 x 512 tiles) */
+                                    3 (gp_options.pair_k_split): a cluster of four CTAs (two such pairs)
+                                    shares each 256 x 128 tile, splitting its K-loop in two halves */
     int32_t k_splits;            /* FP32 FFMA path: CTAs that share each tile's K-loop, when the tiles alone
                                     leave SMs idle (each writes a partial tile; the last to finish adds them in
                                     split order, so results do not depend on timing); 1 = whole K-loops */
@@ -152,10 +149,9 @@ typedef struct gp_stats {
 
 /* Per-call options for gemm_pipelined_ex.  Zero-initialise and set what you need. */
 typedef struct gp_options {
-    int32_t bn;                  /* force the CTA tile width BN (0 = automatic); must be one the variant builds.
-                                    FP16/BF16 ring: 512 runs two CTA pairs per cluster of four on a 256 x 512
-                                    tile, sharing A by TMA multicast (plan.cta_pair = 2; GP_ERR_UNSUPPORTED
-                                    where CTA pairs do not apply) */
+    int32_t bn;                  /* force the CTA tile width BN (0 = automatic); must be one the variant builds
+                                    (FP16/BF16: 256, 128, 64; INT8: 256 on tcgen05, 128 or 64 on IMMA; FP32:
+                                    128), else GP_ERR_UNSUPPORTED */
     int32_t time_kernel;         /* 1: record CUDA events around the launch; gemm_stats(sync=1) reports last_ms */
     uint64_t timeout_ns;         /* limit of every bounded wait inside the kernel (0 = 1 s) */
     int32_t inject_lost_load;    /* test hook: the TMA producer skips the last tile load of the problem, so a

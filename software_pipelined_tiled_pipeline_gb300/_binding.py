@@ -174,7 +174,6 @@ def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined
     ffma_tile: (rows, columns) of outputs per thread of the FP32 ring (default 8 x 8).
     i8_engine: INT8 ring engine, a name of I8_ENGINES or its number ("default" lets the planner pick).
     inputs_ready: promise that no work still in flight on the stream writes A or B (see gp_options).
-    bn=512 (FP16/BF16): two CTA pairs per cluster of four sharing A by TMA multicast.
     pair_k_split: 1 = split 256 x 128 tiles' K-loops over two CTA pairs (see gp_options), -1 = never."""
     s = getattr(stream, "cuda_stream", stream)
     opts = _options(bn, time_kernel, timeout_ns, inject_lost_load, no_stream_k, no_cta_pair, ffma_tile, i8_engine,

@@ -307,7 +307,6 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
   constexpr int64_t kMinIdleSteps = 16;
   constexpr int64_t kMinStepsPerWorker = 4;
   const int64_t T = p->tiles, G = workers;
-  const int64_t part_bn = p->cta_pair == 2 ? p->bn / 2 : p->bn;   // columns of one CTA's partial tile
   p->dp_tiles = static_cast<int32_t>(T);
   p->sk_tiles = 0;
   p->workspace_bytes = 0;
@@ -321,7 +320,7 @@ void apply_stream_k(gp_plan* p, int64_t workers, int ctas_per_worker, bool allow
   p->dp_tiles = static_cast<int32_t>(dp);
   p->sk_tiles = static_cast<int32_t>(skt);
   p->grid = static_cast<int32_t>(ctas_per_worker * G);
-  p->workspace_bytes = static_cast<int64_t>(p->grid) * 2 * 128 * part_bn * 4;   // two 128-row FP32 slots per CTA
+  p->workspace_bytes = static_cast<int64_t>(p->grid) * 2 * 128 * p->bn * 4;   // two 128-row FP32 slots per CTA
 }
 
 // INT8 on tcgen05 (two-pass engine), whole tiles over W workers: when the last
@@ -340,7 +339,7 @@ void apply_i8_halves(gp_plan* p, int64_t workers) {
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
               int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, int i8_engine = 0,
-              int ffma_tm = 0, int ffma_tn = 0, bool no_mc = false, int pair_k_split = 0) {
+              int ffma_tm = 0, int ffma_tn = 0, int pair_k_split = 0) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
@@ -473,14 +472,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     return ring_smem_total(S * (kUmmaBM + pbn / 2) * kUmmaBK * 2, kUmmaEpiBytes) <= kSmemPerCtaMax;
   };
   const bool pair_base = fam == 2 && ring && !no_pair && K > kShortK;
-  const bool pair256 = pair_base && (bn_req == 0 || bn_req == 256 || bn_req == 512) && N > 128 && pair_fits(256);
-  // bn = 512 asks for two pairs per cluster of four, side by side along N,
-  // sharing the A rows through TMA multicast (a 256 x 512 tile: a quarter
-  // fewer bytes read from L2 per MMA, the same bytes into each SM).  Measured
-  // at FP16 4096^3 and BF16 8192^2 x 4096 it is no faster than single pairs
-  // (36 clusters of four fit, 144 of 152 SMs), so it is not the default.
-  const bool mc = pair256 && !no_mc && (sm_count == 0 || sm_count >= 8) && bn_req == 512;
-  if (bn_req == 512 && !mc) return GP_ERR_UNSUPPORTED;
+  const bool pair256 = pair_base && (bn_req == 0 || bn_req == 256) && N > 128 && pair_fits(256);
   const bool pair128 = pair_base && !pair256 && bn_req == 0 && N > 64 && M > 128 && pair_fits(128);
   // pair_k_split: a cluster of two pairs splits each 256 x 128 tile's K-loop
   // in two halves and adds them through distributed shared memory (for few
@@ -550,11 +542,6 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     if (p->smem_bytes < kSmemPerCtaMax / 2 + 1024) p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
     p->tmem_cols = 2 * pair_bn;
     p->kernel = "umma_pair_ring";
-    if (mc) {
-      p->cta_pair = 2;
-      p->bn = 512;   // the cluster's tile; each pair computes 256 x 256 of it
-      p->kernel = "umma_pair_mc_ring";
-    }
     if (kx) {
       p->cta_pair = 3;
       p->kernel = "umma_pair_ksplit_ring";
@@ -564,7 +551,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
   p->k_tiles = ceil_div(K, p->bk);
   if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
-  if (p->cta_pair == 2 || p->cta_pair == 3)
+  if (p->cta_pair == 3)
     p->grid = sm_count > 3 ? static_cast<int32_t>(4 * (p->tiles < sm_count / 4 ? p->tiles : sm_count / 4)) : 0;
   else if (p->cta_pair)
     p->grid = sm_count > 1 ? static_cast<int32_t>(2 * (p->tiles < sm_count / 2 ? p->tiles : sm_count / 2)) : 0;
@@ -596,9 +583,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     }
   }
   if (fam == 2 && ring && sm_count > 0) {
-    if (p->cta_pair == 2)
-      apply_stream_k(p, sm_count / 4, 4, !no_stream_k);
-    else if (p->cta_pair == 3)
+    if (p->cta_pair == 3)
       ;   // whole tiles, each K-loop split over the cluster's two pairs
     else if (p->cta_pair)
       apply_stream_k(p, sm_count / 2, 2, !no_stream_k);
@@ -607,9 +592,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   }
   const double e = in_elem_bytes(dtype);
   p->compute_load_ratio = 2.0 * p->bm * p->bn * p->bk / ((static_cast<double>(p->bm) * p->bk + p->bk * p->bn) * e);
-  if (p->cta_pair == 2)   // per CTA: 128 x 256 outputs from 64 rows of A fetched (64 multicast in) and 128 of B
-    p->compute_load_ratio = 2.0 * 128 * 256 * p->bk / ((64.0 + 128.0) * p->bk * e);
-  else if (p->cta_pair)   // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B
+  if (p->cta_pair)   // per CTA: 128 x 256 outputs from 128 rows of A and 128 rows of B
     p->compute_load_ratio = 2.0 * (p->bm / 2) * p->bn * p->bk / ((p->bm / 2 + p->bn / 2) * p->bk * e);
   return GP_OK;
 }
@@ -815,7 +798,7 @@ int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int sta
   }
   const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
   return plan_impl(M, N, K, dtype, layout, stages, variant, opts ? opts->bn : 0, sms, out, opts && opts->no_stream_k,
-                   no_pair, opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, false,
+                   no_pair, opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0,
                    opts ? opts->pair_k_split : 0);
 }
 
@@ -832,7 +815,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   gp_plan plan;
   int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan, opts && opts->no_stream_k,
                      opts && (opts->no_cta_pair || opts->inject_lost_load), opts ? opts->i8_engine : 0,
-                     opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, false, opts ? opts->pair_k_split : 0);
+                     opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, opts ? opts->pair_k_split : 0);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }   // empty output: nothing read or written
@@ -871,7 +854,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   } else {
     const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
     rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
-                   opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, false,
+                   opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0,
                    opts ? opts->pair_k_split : 0);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     if (plan.cta_pair == 3) {
@@ -880,15 +863,6 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
       if (e == cudaSuccess && clusters < 1) e = cudaErrorLaunchOutOfResources;
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
       if (4 * clusters < plan.grid) plan.grid = 4 * clusters;
-    }
-    if (plan.cta_pair == 2) {
-      // clusters of four sit on two TPCs of one GPC each: fewer than SMs / 4
-      // may be resident (36 on a 152-SM GB300); stream-K over those
-      int clusters = 0;
-      e = umma_mc_capacity(dtype, plan.smem_bytes, &clusters);
-      if (e == cudaSuccess && clusters < 1) e = cudaErrorLaunchOutOfResources;
-      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
-      if (clusters < sms / 4) apply_stream_k(&plan, clusters, 4, !(opts && opts->no_stream_k));
     }
     void* conv = nullptr;
     const bool i8_overlap = plan.cta_pair && dtype == GP_I8_I32 && plan.kernel == kI8OverlapKernelName;
@@ -921,7 +895,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, 0};
     if (plan.sk_tiles > 0) {
       const size_t counter_words =
-          static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair == 2 ? 4 : plan.cta_pair ? 2 : 1) * 2;
+          static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair ? 2 : 1) * 2;
       e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes - conv_bytes), counter_words, &sk.workspace,
                         &sk.flags, &sk.epoch);
       if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
@@ -1048,7 +1022,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
   }
   gp_plan plan;
   // (plain CTA pairs: the fixed scratch is sized for them)
-  int rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, 0, &plan, false, false, 0, 0, 0, true);
+  int rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, 0, &plan, false, false, 0, 0, 0, 0);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }
@@ -1071,7 +1045,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
   if (K == 0) {
     e = launch_zero_fill(C, M * N * out_elem_bytes(dtype), st);
   } else {
-    rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, sms, &plan, false, false, 0, 0, 0, true);
+    rc = plan_impl(M, N, K, dtype, GP_A_ROW_B_COL, stages, GP_PIPELINED, 0, sms, &plan, false, false, 0, 0, 0, 0);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     if (plan.cta_pair) {
       int pairs = 0;

@@ -347,19 +347,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// The same load multicast: the box lands at the same shared-memory offset in
-// every CTA of cta_mask, and each destination's arrival is counted on the
-// barrier at bar_cluster_addr's offset in the even CTA of that destination's
-// pair (the address names this CTA's pair leader).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
-                                                    int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 // Store 16 bytes into another CTA's shared memory (cluster-window address).
 __device__ __forceinline__ void st_cluster_f4(uint32_t cluster_addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x), "f"(v.y), "f"(v.z),

@@ -162,8 +162,6 @@ cudaError_t launch_umma(LaunchArgs& a, const void** kernel);
 // CTA pairs of the pair kernel for dtype (FP16/BF16 ring, or INT8 on tcgen05: two-pass or
 // conversion overlapped in the kernel) that fit at once.
 cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs, bool i8_overlap = false);
-// Clusters of four CTAs (two pairs sharing A by multicast) resident at once.
-cudaError_t umma_mc_capacity(int dtype, int smem_bytes, int* clusters);
 // Clusters of four CTAs (two pairs splitting each 256 x 128 tile's K-loop) resident at once.
 cudaError_t umma_kx_capacity(int dtype, int smem_bytes, int* clusters);
 // INT8 x INT8 -> INT32 on tcgen05 (FP16 operands, accumulator restarted every 1024 K).

@@ -333,7 +333,7 @@ struct RingShape {
   static_assert(EPI_BUFS >= 1 && WARP_CHUNKS >= 1, "epilogue split");
 };
 
-template <int BN, bool BF16, bool PAIR, bool MC, bool KX>
+template <int BN, bool BF16, bool PAIR, bool KX>
 __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     umma_ring_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int stages, KernelCtl ctl,
@@ -351,34 +351,28 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // MC: a cluster of two CTA pairs computes a 256 x 2BN tile, pair p its
-  // columns p*BN .. +BN.  Both pairs read the same 256 rows of A: each CTA
-  // receives its 128 rows half from its own multicast load and half from the
-  // one of the CTA with the same rank in the other pair (see the producer).
   // KX: a cluster of two CTA pairs computes one 256 x BN tile, pair p the
   // K steps p*ceil(kt/2) .. of it; pair 1 sends its FP32 accumulator through
   // distributed shared memory to pair 0, which adds it and writes C.
-  constexpr int CL = (MC || KX) ? 4 : (PAIR ? 2 : 1);         // CTAs per worker (one cluster)
-  static_assert(!MC || PAIR, "multicast runs on CTA pairs");
-  static_assert(!KX || (PAIR && !MC && BN == 128), "K split runs on 256 x 128 pair tiles");
+  constexpr int CL = KX ? 4 : (PAIR ? 2 : 1);                 // CTAs per worker (one cluster)
+  static_assert(!KX || (PAIR && BN == 128), "K split runs on 256 x 128 pair tiles");
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;      // rank in the cluster
   const uint32_t rank = crank & 1u;                           // rank in the CTA pair
-  const int pidx = (MC || KX) ? static_cast<int>(crank >> 1) : 0;   // pair within the cluster
+  const int pidx = KX ? static_cast<int>(crank >> 1) : 0;   // pair within the cluster
   const bool leader = rank == 0;
   const uint32_t lead_rank = crank & ~1u;                     // this pair's even CTA
   const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead_rank);
   const int worker = static_cast<int>(blockIdx.x) / CL;
   const int workers = static_cast<int>(gridDim.x) / CL;
-  constexpr int UNIT_N = MC ? 2 * BN : BN;                    // output columns of one work item
   const int m_blocks = (M + Sh::TILE_M - 1) / Sh::TILE_M;
-  const int n_blocks = (N + UNIT_N - 1) / UNIT_N;
+  const int n_blocks = (N + BN - 1) / BN;
   const int tiles = m_blocks * n_blocks;
   const int kt = (K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&bar->full[s], 1);
-      mbar_init(&bar->empty[s], MC ? 2 : 1);   // MC: released by both pairs' MMAs
+      mbar_init(&bar->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bar->acc_full[a], 1);
@@ -444,23 +438,14 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
         int mb, nb;
         tile_coords(tile, m_blocks, n_blocks, mb, nb);
         const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
-        const int n_row = (nb * (MC ? 2 : 1) + (MC ? pidx : 0)) * BN + rank * Sh::B_ROWS;
+        const int n_row = nb * BN + rank * Sh::B_ROWS;
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto producer_done;
           uint8_t* slot = ring + s * STAGE;
           if (PAIR) {
             if (leader) mbar_arrive_expect_tx(&bar->full[s], 2 * STAGE);
             const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), lead_rank);
-            if (MC) {
-              // rows pidx*64 .. +64 of this CTA's 128 rows of A, to this CTA
-              // and to the CTA of the same pair rank in the other pair (both
-              // slots are free: empty[s] counts both pairs' MMAs)
-              constexpr int HALF = Sh::A_ROWS / 2;
-              tma_load_2d_pair_mc(smem_u32(slot) + pidx * HALF * BK * 2, &tmA, full_leader, kb * BK,
-                                  m_row + pidx * HALF, static_cast<uint16_t>(0x5u << rank));
-            } else {
-              tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
-            }
+            tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
             tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
             ++issued;
           } else if (!(ctl.inject_lost_load && tile == tiles - 1 && kb == kt - 1)) {
@@ -502,7 +487,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
               umma_f16(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
           }
           // slot s is free (in every CTA that loaded into it) once these MMAs have read it
-          if (PAIR) umma_commit_pair(&bar->empty[s], MC ? 0xF : pair_mask); else umma_commit(&bar->empty[s]);
+          if (PAIR) umma_commit_pair(&bar->empty[s], pair_mask); else umma_commit(&bar->empty[s]);
           ++consumed;
           if (++s == stages) { s = 0; ph ^= 1u; }
         }
@@ -552,7 +537,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       tc_fence_after();
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
       const int y = mb * Sh::TILE_M + rank * Sh::A_ROWS + q * 32;
-      const int x0 = (nb * (MC ? 2 : 1) + (MC ? pidx : 0)) * BN;   // first column of this pair's tile
+      const int x0 = nb * BN;   // first column of this pair's tile
       if (KX) {
         // K split over the two pairs: pair 1 sends its FP32 half of the
         // accumulator to the CTA of the same pair rank in pair 0 (row-
@@ -1794,7 +1779,7 @@ __global__ void __launch_bounds__(kPPThreads, 1)
   }
 }
 
-template <int BN, bool BF16, bool PAIR, bool MC = false, bool KX = false>
+template <int BN, bool BF16, bool PAIR, bool KX = false>
 cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   using Sh = RingShape<BN, PAIR>;
   const gp_plan& p = a.plan;
@@ -1805,13 +1790,11 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   if ((e = make_tmap_2d(&tmC, a.C, dt, N, M, N * 2, kUmmaEpiCols, kUmmaEpiRows, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       cudaSuccess)
     return e;
-  // MC: each multicast load carries half of a CTA's rows of A
-  if ((e = make_tmap_2d(&tmA, a.A, dt, K, M, K * 2, BK, MC ? Sh::A_ROWS / 2 : Sh::A_ROWS,
-                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  if ((e = make_tmap_2d(&tmA, a.A, dt, K, M, K * 2, BK, Sh::A_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   if ((e = make_tmap_2d(&tmB, a.B, dt, K, N, K * 2, BK, Sh::B_ROWS, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
-  auto k = umma_ring_kernel<BN, BF16, PAIR, MC, KX>;
+  auto k = umma_ring_kernel<BN, BF16, PAIR, KX>;
   *kernel = reinterpret_cast<const void*>(k);
   if ((e = ensure_smem_attr(*kernel, p.smem_bytes)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1823,7 +1806,7 @@ cudaError_t launch_ring(LaunchArgs& a, const void** kernel) {
   int n = 0;
   if (PAIR) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (MC || KX) ? 4 : 2;
+    attr[n].val.clusterDim.x = KX ? 4 : 2;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -1984,20 +1967,16 @@ cudaError_t launch_i8_overlap(LaunchArgs& a, const void** kernel) {
                             a.M, a.N, a.K, p.stages, stg_slots, a.ctl);
 }
 
-// Largest number of CTA pairs of a pair kernel that can be resident at once.
+// Largest number of clusters of a pair kernel that can be resident at once.
 // kind: 0 FP16 ring, 1 BF16 ring, 2 INT8 two-pass, 3 INT8 with the conversion overlapped.
-// Clusters of `size` CTAs (2: one pair; 4: two pairs, sharing A (kx false)
-// or splitting K (kx true), kinds 0-1) resident at once at this shared-memory size.
+// size 2: one CTA pair; size 4 (kinds 0-1, kx): two pairs splitting each 256 x 128 tile's K-loop.
 cudaError_t max_clusters(int kind, int smem_bytes, int size, int* clusters, bool kx = false) {
-  const bool mc = size == 4 && !kx;
   const void* k = kind == 3   ? reinterpret_cast<const void*>(umma_i8_overlap_kernel)
                   : kind == 2 ? reinterpret_cast<const void*>(umma_i8_kernel<true>)
-                  : kx ? (kind == 1 ? reinterpret_cast<const void*>(umma_ring_kernel<128, true, true, false, true>)
-                                    : reinterpret_cast<const void*>(umma_ring_kernel<128, false, true, false, true>))
-                  : kind == 1 ? (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, true, false>)
-                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, false, false>))
-                              : (mc ? reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, true, false>)
-                                    : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, false, false>));
+                  : kx ? (kind == 1 ? reinterpret_cast<const void*>(umma_ring_kernel<128, true, true, true>)
+                                    : reinterpret_cast<const void*>(umma_ring_kernel<128, false, true, true>))
+                  : kind == 1 ? reinterpret_cast<const void*>(umma_ring_kernel<256, true, true, false>)
+                              : reinterpret_cast<const void*>(umma_ring_kernel<256, false, true, false>);
   cudaError_t e = ensure_smem_attr(k, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -2016,8 +1995,7 @@ cudaError_t max_clusters(int kind, int smem_bytes, int size, int* clusters, bool
 
 template <bool BF16>
 cudaError_t launch_dtype(LaunchArgs& a, const void** kernel) {
-  if (a.plan.cta_pair == 2) return launch_ring<256, BF16, true, true>(a, kernel);
-  if (a.plan.cta_pair == 3) return launch_ring<128, BF16, true, false, true>(a, kernel);
+  if (a.plan.cta_pair == 3) return launch_ring<128, BF16, true, true>(a, kernel);
   if (a.plan.cta_pair)
     return a.plan.bn == 128 ? launch_ring<128, BF16, true>(a, kernel) : launch_ring<256, BF16, true>(a, kernel);
   switch (a.plan.bn) {
@@ -2037,10 +2015,6 @@ cudaError_t launch_umma(LaunchArgs& a, const void** kernel) {
 cudaError_t umma_pair_capacity(int dtype, int smem_bytes, int* pairs, bool i8_overlap) {
   const int kind = dtype == GP_I8_I32 ? (i8_overlap ? 3 : 2) : (dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0);
   return max_clusters(kind, smem_bytes, 2, pairs);
-}
-
-cudaError_t umma_mc_capacity(int dtype, int smem_bytes, int* clusters) {
-  return max_clusters(dtype == GP_BF16_F32ACC_BF16OUT ? 1 : 0, smem_bytes, 4, clusters);
 }
 
 cudaError_t umma_kx_capacity(int dtype, int smem_bytes, int* clusters) {

@@ -328,20 +328,10 @@ def test_double_buffer_rule_matches_published_example():
     assert 2 * g["single_buffer_kb"] == g["double_buffer_kb"]
 
 
-def test_multicast_tile_plan(gp):
-    # bn = 512: two CTA pairs per cluster of four on a 256 x 512 tile, A shared by TMA multicast;
-    # tiles and the stream-K split count 256 x 512 tiles, partial slots stay 128 x 256 per CTA
-    kw = dict(plan_sms=152, bn=512)
-    p = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", **kw)
-    assert (p["kernel"], p["cta_pair"], p["bm"], p["bn"], p["stages"]) == ("umma_pair_mc_ring", 2, 256, 512, 5)
-    # 128 tiles on 38 clusters: two whole waves, the last 52 tiles' K-loops split
-    assert (p["tiles"], p["grid"], p["dp_tiles"], p["sk_tiles"]) == (128, 152, 76, 52)
-    assert p["workspace_bytes"] == 152 * 2 * 128 * 256 * 4
-    assert p["stage_bytes"] == (128 + 128) * 64 * 2   # per CTA: its 128 rows of A (half multicast in) and of B
-    r = gp.gemm_plan(1000, 1800, 1000, "bf16", "row_col", 0, "pipelined", **kw)
-    assert (r["tiles"], r["grid"], r["sk_tiles"]) == (4 * 4, 64, 0)
-    assert gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined")["cta_pair"] == 1   # not the default
-    for M, N, K, dt, lay in [(4096, 4096, 256, "f16", "row_col"), (4096, 4096, 4096, "f32", "row_row"),
+def test_no_512_wide_tile(gp):
+    # no tile is 512 columns wide: every dtype and layout refuses bn = 512
+    for M, N, K, dt, lay in [(4096, 4096, 4096, "f16", "row_col"), (4096, 4096, 4096, "bf16", "row_col"),
+                             (4096, 4096, 256, "f16", "row_col"), (4096, 4096, 4096, "f32", "row_row"),
                              (4096, 4096, 4096, "i8", "row_col"), (4096, 128, 4096, "bf16", "row_col")]:
         assert gp.gemm_plan_rc(M, N, K, dt, lay, 0, "pipelined", bn=512) == gp.GP_ERR_UNSUPPORTED
 

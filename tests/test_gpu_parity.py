@@ -248,26 +248,6 @@ def test_cta_pair_kernel(dtype, M, N, K, S):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("M,N,K,S", [(256, 512, 320, 5), (1000, 1800, 1000, 6), (768, 1536, 2048, 4),
-                                     (2304, 2560, 640, 6), (520, 264, 1032, 3)])
-def test_multicast_pair_kernel(dtype, M, N, K, S):
-    # bn = 512: two CTA pairs per cluster of four, each CTA's A rows half from its own multicast load
-    # and half from the other pair's; ragged in M, N (a last pair wholly past N), K; stream-K splits
-    lay = "row_col"
-    A, B = operands(dtype, lay, M, N, K, seed=M * 3 + N + K)
-    C, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, bn=512)
-    p = st["plan"]
-    assert p["cta_pair"] == 2 and p["kernel"] == "umma_pair_mc_ring" and p["grid"] % 4 == 0
-    assert p["tiles"] == -(-M // 256) * -(-N // 512)
-    check_full(dtype, lay, A, B, C, K)
-    # whole tiles: each pair runs the MMAs of a 256 x 256 pair tile in the same order, bit for bit
-    Cd, std = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, bn=512, no_stream_k=True)
-    C2, st2 = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, no_stream_k=True)
-    assert std["plan"]["cta_pair"] == 2 and st2["plan"]["cta_pair"] == 1
-    assert torch.equal(Cd.view(torch.int16), C2.view(torch.int16))
-
-
-@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("M,N,K,S", [(1000, 120, 2056, 5), (520, 128, 1032, 4), (256, 72, 264, 3), (2056, 104, 4104, 5)])
 def test_pair_k_split_kernel(dtype, M, N, K, S):
     # each 256 x 128 tile on two CTA pairs, one per half of the K-loop, the halves added through
@@ -315,21 +295,6 @@ def test_inputs_ready_fp16_bf16_back_to_back(dtype, M, N, K):
     for C in outs:
         assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
     check_sampled(dtype, "row_col", A, B, ref.view(M, N).cpu(), K, rows=[0, 255, 256, M - 1], npts=1500, seed=1)
-
-
-def test_multicast_pair_repeated_launches():
-    # back-to-back launches (programmatic dependent launch, stream-K workspace reused) stay exact
-    M, N, K = 1024, 2048, 2048
-    A, B = operands("f16", "row_col", M, N, K, seed=11)
-    tA, tB = to_dev(A, "f16"), to_dev(B, "f16")
-    outs = [torch.empty(M * N, dtype=torch.float16, device="cuda") for _ in range(4)]
-    for C in outs:
-        gp.gemm_pipelined(tA, tB, C, M, N, K, "f16", "row_col", 0, "pipelined", torch.cuda.current_stream(), bn=512)
-    st = gp.gemm_stats(sync=True)
-    assert st["status"] == 0 and st["device_status"] == 0 and st["plan"]["cta_pair"] == 2
-    check_full("f16", "row_col", A, B, outs[0].view(M, N).cpu(), K)
-    for C in outs[1:]:
-        assert torch.equal(C, outs[0])
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
