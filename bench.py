@@ -5,10 +5,15 @@ One step = one GEMM over the workload (all steps of the K-loop hot path:
 tile decomposition, prologue, steady-state ring, drain, output epilogue).
 Default workload: FP16 GEMM M=N=K=4096, A row-major, B column-major, FP32
 accumulate, FP16 out, TMA-ring tcgen05 kernel on CTA pairs at the library's
-default depth (5 stages at this shape).  Prints ONE JSON
-line (rank 0).  The INT8 4096^3 result, the stage sweep and the FP32
-ping-pong-vs-async comparison ride along as sub-objects, and the vendor
-library's time on the same shape and buffers as context.
+default depth (5 stages at this shape).  The last line on stdout (rank 0)
+is one compact JSON object (under 2 KB): the headline, its roofline, the
+end-to-end rate through the C ABI with host buffers, the CPU oracle baseline,
+the clocks, and a few scalars of the other configurations (INT8 4096^3 per
+call at the library's default, FP32 1024^3, the like-for-like pipelining
+gain).  The full sweeps (stage depth per configuration, the BF16
+compute/load-ratio sweep, the FFMA register-tile sweep) go to a JSON file
+(--sweep-out, default gpurun_out/bench_sweep.json) and, one short line per
+configuration, to stdout before the final line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--stages S] [--no-sweep] [--no-sweep-bf16]
@@ -53,6 +58,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sustained-s", type=float, default=3.0,
                     help="seconds of back-to-back steps for the sustained figure (0 = skip)")
+    ap.add_argument("--sweep-out", default=os.path.join(ROOT, "gpurun_out", "bench_sweep.json"),
+                    help="file the full sweep results are written to")
     return ap.parse_args()
 
 
@@ -322,6 +329,10 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
         if w.dtype in ("f16", "bf16"):
             # the same ring on one CTA per 128-row tile, whole tiles only (no pairs, no stream-K)
             cases += [("pipelined", S, {"no_cta_pair": True, "no_stream_k": True}) for S in (4, 6)]
+            if w.name == "f16_4096":
+                # like for like: the ring on the ping-pong kernel's launch shape (one CTA per
+                # 128 x 256 tile, grid = tiles, same smem layout, MMA sequence and epilogue)
+                cases += [("pipelined", S, {"one_tile_per_cta": True}) for S in (1, 2, 3, 4)]
             # the caller's promise that the inputs are in place: each launch's loads and MMAs
             # start while the previous launch finishes (only its stores wait)
             cases += [("pipelined", 5, {"inputs_ready": True})]
@@ -332,6 +343,8 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
         if w.dtype == "i8":
             # the TMA ring feeding warp-level IMMA (the ping-pong and no-overlap rows use IMMA too)
             cases += [("pipelined", S, {"i8_engine": "imma"}) for S in w.stages]
+            # like for like: the IMMA ring on the ping-pong kernel's launch shape (one CTA per tile)
+            cases += [("pipelined", S, {"one_tile_per_cta": True}) for S in (2, 4)]
             # tcgen05 with the int8 -> FP16 conversion overlapped inside the GEMM kernel (one launch)
             cases += [("pipelined", S, {"i8_engine": "tcgen05_overlap"}) for S in (4, 5)]
             # the two-pass engine with successive calls pipelined (the caller promises the inputs are
@@ -356,6 +369,8 @@ def sweep(torch, gp, dev, stream, names, steps, peaks, imma_peak, rw=None):
         base = next(r for r in rows if r["variant"] == "pingpong")[unit]
         for r in rows:
             r["vs_pingpong"] = round(r[unit] / base, 3) if base else None
+            if r.get("options", {}).get("one_tile_per_cta"):
+                r["like_for_like"] = True   # same tile, grid and occupancy as the ping-pong row
         out[name] = {"unit": unit, "rows": rows}
         del bufs
         torch.cuda.empty_cache()
@@ -380,6 +395,36 @@ def ffma_tile_sweep(torch, gp, dev, stream, steps=10):
     del bufs
     torch.cuda.empty_cache()
     return {"workload": "f32_4096", "stages": 3, "rows": rows}
+
+
+def int8_default(torch, gp, dev, stream, steps):
+    """INT8 4096^3 through the library's default call (stages = 0: the planner's engine and depth),
+    back to back on rotating buffers; every call is a full GEMM (its conversion pass included)."""
+    from software_pipelined_tiled_pipeline_gb300 import synth
+    from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
+    w = WORKLOADS["i8_4096"]
+    A, B = synth.operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    bufs = device_sets(torch, w, A, B, dev, ROTATE)
+    time_kernel(torch, gp, w, bufs, "pipelined", 0, 5, stream)
+    ms, _, st = time_kernel(torch, gp, w, bufs, "pipelined", 0, steps, stream)
+    del bufs
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "ms": round(ms, 5), "TOPS": round(w.ops / (ms * 1e-3) / 1e12, 2),
+            "stages": st["plan"]["stages"], "kernel": st["plan"]["kernel"], "steps": steps}
+
+
+def compact_line(line, limit=2000):
+    """Drop optional keys (last added first) until the JSON line is under `limit` bytes: the
+    driver keeps only the tail of stdout."""
+    required = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks",
+                "cpu_baseline", "impl"}
+    for key in reversed(list(line)):
+        if len(json.dumps(line)) < limit:
+            break
+        if key not in required:
+            del line[key]
+    return line
 
 
 def _code_only(text):
@@ -645,9 +690,7 @@ def main():
     kernel_key = "%s@%s" % (plan["kernel"], w.name)
     imma_peak = gp.probe_peak("imma_s8", stream) / 1e12 if plan["kernel"].startswith("imma") else None
     bound, _ = roofline_row(w, plan["kernel"], kavg, peaks, imma_peak)
-    roofline = {"kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5),
-                "kernel_avg_how": "timed-region CUDA events / steps (launches back to back)",
-                "launch_isolated_ms": round(iso_ms, 5),
+    roofline = {"kernel": plan["kernel"], "kernel_avg_ms": round(kavg, 5), "launch_isolated_ms": round(iso_ms, 5),
                 "traffic": traffic_for(kernel_key, kernel_src)}
     if bound == "hbm":
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -655,49 +698,50 @@ def main():
         rw = hbm_probe(torch, dev)
         roofline.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "algorithmic_bytes": w.algorithmic_bytes,
-                         "peak_source": peaks["_source"] + ": STREAM-style copy",
-                         "rw_probe": rw, "rw_roof_frac": round(rw_roof_us(w, rw) / (kavg * 1e3), 4)})
+                         "peak_source": peaks["_source"] + ": copy",
+                         "rw_roof_frac": round(rw_roof_us(w, rw) / (kavg * 1e3), 4)})
     else:
         peak = compute_peak(plan["kernel"], peaks, imma_peak)
         roofline.update({"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
                          "unit": "TOPS" if w.dtype == "i8" else "TFLOP/s", "frac": round(achieved / peak, 4)})
         if plan["kernel"].startswith("umma") and w.dtype == "i8":
-            roofline.update({"peak_source": peaks["_source"] + ": dense 16-bit tcgen05 rate (exact FP16 MMAs)",
-                             "note": "launch time includes the int8->FP16 conversion kernel"})
+            roofline["peak_source"] = peaks["_source"] + ": dense 16-bit burst (exact FP16 MMAs, conversion included)"
         elif plan["kernel"].startswith("umma"):
-            roofline["peak_source"] = peaks["_source"] + ": dense bf16 burst (FP16 runs at the same tcgen05 rate)"
+            roofline["peak_source"] = peaks["_source"] + ": dense bf16 burst (FP16 at the same rate)"
         elif plan["kernel"].startswith("imma"):
             roofline["peak_source"] = "measured IMMA mma.sync s8 probe (gemm_probe_peak)"
         else:
             roofline["peak_source"] = "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz"
 
+    clocks = ClockSampler.summarize(clock_rows, wall0, wall1)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description, "M": w.M, "N": w.N, "K": w.K,
-                   "layout": w.layout, "variant": args.variant, "stages": plan["stages"], "bm": plan["bm"],
-                   "bn": plan["bn"], "bk": plan["bk"], "grid": plan["grid"], "smem_bytes": plan["smem_bytes"],
-                   "regs_per_thread": st["regs_per_thread"],
-                   "l2": "operands and output rotated over %d buffer sets (%.0f MiB > 129 MB L2)" % (
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "variant": args.variant,
+                   "stages": plan["stages"], "kernel": plan["kernel"], "tile": "%dx%dx%d" % (
+                       plan["bm"], plan["bn"], plan["bk"]), "grid": plan["grid"],
+                   "l2": "inputs and output rotated over %d buffer sets (%.0f MiB > 129 MB L2)" % (
                        ROTATE, ROTATE * (A.nbytes + B.nbytes + w.M * w.N * (4 if w.dtype in ("i8", "f32") else 2))
                        / 2 ** 20),
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
-                "d2h_bytes_per_step": int(hC[0].numel() * hC[0].element_size()), "steps": e2e_steps,
-                "how": "copies of step i+1 in and step i-1 out overlap step i's GEMM (3 streams, 2 buffer sets); "
-                       "host link ~180 GB/s each way"},
+                "d2h_bytes_per_step": int(hC[0].numel() * hC[0].element_size())},
         "gpu_launches": args.steps * (2 if plan["kernel"] == "umma_i8_pair_ring" else 1),
-        "library_same_shape": ({"value": round(w.ops / (lib_ms * 1e-3) / 1e12, 2), "unit": unit,
-                                "ms_per_call": round(lib_ms, 5), "how": lib_how + ", same buffers, back to back",
-                                "ours_over_library": round(lib_ms / ms_per_step, 3)}
-                               if lib_ms else {"unavailable": lib_how}),
-        "sustained": sustained,
-        "clocks": ClockSampler.summarize(clock_rows, wall0, wall1),
+        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                   "reasons": clocks.get("reasons"), "samples": clocks.get("samples")},
     }
+    if lib_ms:
+        line["library_same_shape"] = {"value": round(w.ops / (lib_ms * 1e-3) / 1e12, 1),
+                                      "ours_over_library": round(lib_ms / ms_per_step, 3)}
+    if sustained:
+        line["sustained"] = {k: sustained.get(k) for k in ("value", "frac", "seconds")}
+        line["sustained"]["sm_mhz"] = sustained["clocks"].get("sm_mhz")
 
     extra_steps = max(10, min(args.steps, 50))
+    full = {"headline": {"roofline": roofline, "sustained": sustained, "clocks": clocks,
+                         "library_same_shape": {"ms_per_call": lib_ms, "how": lib_how}}}
     if not args.no_sweep:
         names = ["f16_4096", "i8_4096", "f32_1024"]
         if args.sweep_bf16:
@@ -707,39 +751,68 @@ def main():
         imma_peak = gp.probe_peak("imma_s8", stream) / 1e12
         rw = hbm_probe(torch, dev) if args.sweep_bf16 else None
         sw = sweep(torch, gp, dev, stream, names, extra_steps, peaks, imma_peak, rw)
-        if rw:
-            line["hbm_probe"] = rw
-        line["sweep"] = sw
+        full["hbm_probe"] = rw
+        full["sweep"] = sw
+        tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         i8 = sw.get("i8_4096")
         if i8:
-            best = max((r for r in i8["rows"] if r["variant"] == "pipelined"), key=lambda r: r["TOPS"])
+            # the INT8 headline: the library's default call (stages = 0), timed on its own
+            i8d = int8_default(torch, gp, dev, stream, max(20, extra_steps))
             imma = max((r for r in i8["rows"] if r["kernel"] == "imma_ring"), key=lambda r: r["TOPS"])
-            ipeak = imma_peak
-            tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-            line["int8"] = {
-                "workload": "i8_4096", "value": best["TOPS"], "unit": "TOPS", "stages": best["stages"],
-                "kernel": best["kernel"], "options": best.get("options", {}),
-                "peak": tpeak, "frac": round(best["TOPS"] / tpeak, 4),
-                "peak_source": peaks["_source"] + ": dense 16-bit tcgen05 rate (the INT8 products run as exact "
-                                                  "FP16 MMAs; includes the FP16 conversion pass)",
-                "imma_ceiling": round(ipeak, 1),
-                "imma_ceiling_source": "measured mma.sync s8 probe (gemm_probe_peak)",
-                "imma_ring": {"TOPS": imma["TOPS"], "stages": imma["stages"], "frac_of_imma_ceiling":
-                              round(imma["TOPS"] / ipeak, 4)},
-                "vs_pingpong": best["vs_pingpong"]}
+            promised = [r for r in i8["rows"] if r.get("options", {}).get("inputs_ready")]
+            line["int8_4096"] = {"TOPS": i8d["TOPS"], "frac": round(i8d["TOPS"] / tpeak, 4),
+                                 "stages": i8d["stages"], "kernel": i8d["kernel"], "launches_per_call": 2,
+                                 "imma_ring_TOPS": imma["TOPS"], "imma_ceiling": round(imma_peak, 1)}
+            if promised:
+                line["int8_4096_inputs_ready"] = {"TOPS": promised[0]["TOPS"],
+                                                  "frac": round(promised[0]["TOPS"] / tpeak, 4),
+                                                  "caller_promise": True}
+            full["int8_default"] = i8d
         f16 = sw.get("f16_4096")
         if f16:
-            best = max((r for r in f16["rows"] if r["variant"] == "pipelined"), key=lambda r: r["TFLOPS"])
-            line["fp16_best_stage"] = {"stages": best["stages"], "TFLOPS": best["TFLOPS"],
-                                       "frac": round(best["TFLOPS"] / peaks.get("bf16_tflops", 1920.0), 4)}
-        line["ffma_peak_probe_tflops"] = round(gp.probe_peak("ffma_f32", stream) / 1e12, 2)
-        line["ffma_thread_tile_sweep"] = ffma_tile_sweep(torch, gp, dev, stream)
+            rows = {(r["variant"], r["stages"], json.dumps(r.get("options", {}), sort_keys=True)): r
+                    for r in f16["rows"]}
+            pp = rows[("pingpong", 2, "{}")]
+            lfl = rows.get(("pipelined", 2, json.dumps({"one_tile_per_cta": True})))
+            best = max((r for r in f16["rows"] if r["variant"] == "pipelined" and not r.get("options")),
+                       key=lambda r: r["TFLOPS"])
+            line["f16_stages"] = {str(r["stages"]): r["TFLOPS"] for r in f16["rows"]
+                                  if r["variant"] == "pipelined" and not r.get("options")}
+            line["f16_stages"]["pingpong"] = pp["TFLOPS"]
+            line["f16_best_stage"] = best["stages"]
+            if lfl:
+                # the pages' comparison: same tile, grid and occupancy, only the data path differs
+                line["pipelining_gain_like_for_like"] = {"f16_ring_s2_over_pingpong": round(
+                    lfl["TFLOPS"] / pp["TFLOPS"], 3)}
+        f32 = sw.get("f32_1024")
+        if f32:
+            pf = {r["stages"]: r for r in f32["rows"] if r["variant"] == "pipelined" and not r.get("options")}
+            pp32 = next(r for r in f32["rows"] if r["variant"] == "pingpong")
+            line["fp32_1024"] = {"TFLOPS": pf[2]["TFLOPS"] if 2 in pf else None,
+                                 "frac_alu": pf[2]["roofline_frac"] if 2 in pf else None,
+                                 "s2_over_pingpong": pf[2]["vs_pingpong"] if 2 in pf else None,
+                                 "pingpong_TFLOPS": pp32["TFLOPS"]}
+        full["ffma_peak_probe_tflops"] = round(gp.probe_peak("ffma_f32", stream) / 1e12, 2)
+        full["ffma_thread_tile_sweep"] = ffma_tile_sweep(torch, gp, dev, stream)
+        for name, d in sw.items():
+            short = {"sweep": name, "unit": d["unit"],
+                     "rows": [[r["variant"][:4], r["stages"], r[d["unit"]], r["roofline_frac"]] +
+                              ([r["options"]] if r.get("options") else []) for r in d["rows"]]}
+            print(json.dumps(short), flush=True)
 
     if not args.no_cpu_baseline and world == 1:
         v, R, t, cores = oracle_sample(w, A, B, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": unit, "cores": cores, "kind": "oracle",
-                                "sample": "first %d of %d rows of C (%d x %d x %d MACs) in %.1f s" % (
-                                    R, w.M, R, w.N, w.K, t)}
+                                "sample": "first %d of %d rows of C in %.1f s" % (R, w.M, t)}
+    if args.sweep_out:
+        try:
+            os.makedirs(os.path.dirname(os.path.abspath(args.sweep_out)), exist_ok=True)
+            with open(args.sweep_out, "w") as f:
+                json.dump(dict(full, line=line), f, indent=1)
+            line["sweep_file"] = os.path.relpath(os.path.abspath(args.sweep_out), ROOT)
+        except OSError as e:
+            line["sweep_file"] = "not written: %s" % e
+    line = compact_line(line)
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

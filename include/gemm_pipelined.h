@@ -35,14 +35,25 @@
  *  - Device workspace: split K-loops (stream-K tails of the tcgen05 kernels,
  *    split FFMA K-loops) and the FP16 copies of INT8 operands live in a
  *    workspace the library allocates per (device, stream) on first need,
- *    grows when a larger plan needs it and keeps (gp_plan.workspace_bytes is
- *    the size a call uses).  Growing it synchronises that stream once.
- *    gemm_pipelined_noalloc uses a fixed static array instead.
+ *    grows when a larger plan needs it and keeps until gemm_release
+ *    (gp_plan.workspace_bytes is the size a call uses).  Growing it
+ *    synchronises that stream and frees and allocates device memory
+ *    (cudaFree / cudaMalloc, which may synchronise the device).  The library
+ *    tracks up to 64 streams at once; a call on a 65th stream takes over the
+ *    least recently used stream's workspace after a device-wide
+ *    synchronisation.  gemm_pipelined_noalloc uses a fixed static array
+ *    instead.
+ *  - Status: each call has its own status record, tagged with the call, in a
+ *    static per-device ring of 4096 slots; gemm_stats(sync=1) reads it on the
+ *    call's stream only.  A call's record can be lost only if 4096 later calls
+ *    on the device are made before it is read and the one sharing its slot
+ *    also fails.
  *  - Return value: GP_OK (0) or a negative GP_ERR_* code.  Argument errors are
  *    detected on the host before anything is launched; the output is then
  *    untouched.  gemm_strerror() names every code.
  *  - Thread safety: the per-thread "last call" record read by gemm_stats() is
- *    thread-local; everything else may be called from several host threads.
+ *    thread-local; everything else may be called from several host threads
+ *    (calls on different streams report their own errors).
  */
 #ifndef GEMM_PIPELINED_H
 #define GEMM_PIPELINED_H
@@ -143,7 +154,8 @@ typedef struct gp_stats {
     int32_t local_bytes;         /* cudaFuncAttributes.localSizeBytes (register spills) */
     int32_t blocks_per_sm;       /* cudaOccupancyMaxActiveBlocksPerMultiprocessor at plan.smem_bytes */
     int32_t sm_count;            /* multiprocessors of the device used */
-    uint32_t device_status;      /* kernel status word (0 = clean); valid after gemm_stats(sync=1) */
+    uint32_t device_status;      /* the call's status record: 0 = clean, else code | wait site << 8;
+                                    valid after gemm_stats(sync=1) */
     float last_ms;               /* kernel time from CUDA events if timing was requested, else -1 */
 } gp_stats;
 
@@ -181,6 +193,12 @@ typedef struct gp_options {
                                     accumulator added by the first through distributed shared memory (at most
                                     5 stages; plan.cta_pair = 3; GP_ERR_UNSUPPORTED where it does not apply);
                                     0 = the planner's choice; -1 = never */
+    int32_t one_tile_per_cta;    /* GP_PIPELINED, FP16/BF16 and INT8: 1 = launch one CTA per BM x BN output tile
+                                    (grid = tiles), each computing its tile whole and exiting -- no CTA pairs, no
+                                    persistent loop, no stream-K (INT8 then runs on the IMMA ring).  This is the
+                                    launch shape of the ping-pong and no-overlap variants, so that the three data
+                                    paths can be compared with nothing else changed ("CUDA Kernel Study:
+                                    Pipelining", Benchmark Results).  0 = the planner's choice */
 } gp_options;
 
 /*
@@ -223,10 +241,10 @@ int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int sta
 
 /*
  * gemm_stats -- copy the calling thread's last-call record into *out.
- *   sync != 0: first synchronise the stream of that call, read and clear the
- *   device status word, and compute last_ms if timing was requested.  If the
- *   kernel reported a timed-out wait, the record's status becomes
- *   GP_ERR_TIMEOUT and so does the return value.
+ *   sync != 0: first read that call's status record on the call's stream and
+ *   synchronise that stream (no other stream), and compute last_ms if timing
+ *   was requested.  If the kernel reported a timed-out wait, the record's
+ *   status becomes GP_ERR_TIMEOUT and so does the return value.
  * Returns GP_OK, GP_ERR_ARG (out == NULL) or the code described above.
  */
 int gemm_stats(gp_stats* out, int sync);
@@ -236,6 +254,16 @@ const char* gemm_strerror(int code);
 
 /* Version of this ABI: major * 10000 + minor * 100 + patch. */
 int gemm_abi_version(void);
+
+/*
+ * gemm_release -- free every device workspace the library holds for
+ * `device` (the stream-K partial tiles, split-K counters and INT8 FP16 copies
+ * of all streams that called it).  Synchronises the device first, so nothing
+ * in flight still uses them; later calls allocate afresh.  The fixed array of
+ * gemm_pipelined_noalloc and the status slots are static and not affected.
+ * Returns GP_OK, GP_ERR_ARG (no such device) or GP_ERR_CUDA.
+ */
+int gemm_release(int device);
 
 /*
  * gemm_pipelined_noalloc -- the FP16/BF16 TMA-ring GEMM (GP_PIPELINED,

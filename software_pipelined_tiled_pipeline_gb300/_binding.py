@@ -38,7 +38,7 @@ VARIANTS = {"pingpong": GP_PINGPONG, "pipelined": GP_PIPELINED, "nopipe": GP_NOP
 
 # exported symbols, in header order
 SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_plan_ex", "gemm_stats", "gemm_strerror",
-           "gemm_abi_version", "gemm_pipelined_noalloc", "gemm_probe_peak"]
+           "gemm_abi_version", "gemm_release", "gemm_pipelined_noalloc", "gemm_probe_peak"]
 
 
 class GpPlan(ctypes.Structure):
@@ -78,6 +78,7 @@ class GpOptions(ctypes.Structure):
         ("inject_lost_load", ctypes.c_int32), ("no_stream_k", ctypes.c_int32), ("no_cta_pair", ctypes.c_int32),
         ("i8_engine", ctypes.c_int32), ("ffma_tm", ctypes.c_int32), ("ffma_tn", ctypes.c_int32),
         ("plan_sms", ctypes.c_int32), ("inputs_ready", ctypes.c_int32), ("pair_k_split", ctypes.c_int32),
+        ("one_tile_per_cta", ctypes.c_int32),
     ]
 
 
@@ -113,6 +114,8 @@ def lib():
     L.gemm_strerror.restype = ctypes.c_char_p
     L.gemm_abi_version.argtypes = []
     L.gemm_abi_version.restype = ci
+    L.gemm_release.argtypes = [ci]
+    L.gemm_release.restype = ci
     L.gemm_pipelined_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, vp]
     L.gemm_pipelined_noalloc.restype = ci
     L.gemm_probe_peak.argtypes = [ci, ctypes.POINTER(ctypes.c_double), vp]
@@ -137,6 +140,13 @@ def _enum(val, table, name):
     return int(val)
 
 
+def release(device=0) -> None:
+    """Free the library's device workspaces of `device` (synchronises it)."""
+    rc = lib().gemm_release(int(device))
+    if rc != GP_OK:
+        raise GemmError(rc, "gemm_release")
+
+
 def strerror(code: int) -> str:
     return lib().gemm_strerror(int(code)).decode()
 
@@ -149,7 +159,7 @@ I8_ENGINES = {"default": 0, "imma": 1, "tcgen05_2pass": 2, "tcgen05_overlap": 3}
 
 
 def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-             ffma_tile=None, i8_engine=0, plan_sms=0, inputs_ready=False, pair_k_split=0):
+             ffma_tile=None, i8_engine=0, plan_sms=0, inputs_ready=False, pair_k_split=0, one_tile_per_cta=False):
     opts = GpOptions()
     opts.bn = int(bn)
     opts.time_kernel = 1 if time_kernel else 0
@@ -163,21 +173,24 @@ def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_s
     opts.plan_sms = int(plan_sms)
     opts.inputs_ready = 1 if inputs_ready else 0
     opts.pair_k_split = int(pair_k_split)
+    opts.one_tile_per_cta = 1 if one_tile_per_cta else 0
     return opts
 
 
 def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
                    time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-                   ffma_tile=None, i8_engine=0, inputs_ready=False, pair_k_split=0, check=True) -> int:
+                   ffma_tile=None, i8_engine=0, inputs_ready=False, pair_k_split=0, one_tile_per_cta=False,
+                   check=True) -> int:
     """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
     stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0.
     ffma_tile: (rows, columns) of outputs per thread of the FP32 ring (default 8 x 8).
     i8_engine: INT8 ring engine, a name of I8_ENGINES or its number ("default" lets the planner pick).
     inputs_ready: promise that no work still in flight on the stream writes A or B (see gp_options).
-    pair_k_split: 1 = split 256 x 128 tiles' K-loops over two CTA pairs (see gp_options), -1 = never."""
+    pair_k_split: 1 = split 256 x 128 tiles' K-loops over two CTA pairs (see gp_options), -1 = never.
+    one_tile_per_cta: the ring on the launch shape of the ping-pong kernel (one CTA per tile)."""
     s = getattr(stream, "cuda_stream", stream)
     opts = _options(bn, time_kernel, timeout_ns, inject_lost_load, no_stream_k, no_cta_pair, ffma_tile, i8_engine,
-                    inputs_ready=inputs_ready, pair_k_split=pair_k_split)
+                    inputs_ready=inputs_ready, pair_k_split=pair_k_split, one_tile_per_cta=one_tile_per_cta)
     rc = lib().gemm_pipelined_ex(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"),
                                  _enum(layout, LAYOUTS, "layout"), int(stages), _enum(variant, VARIANTS, "variant"),
                                  s or None, ctypes.byref(opts))

@@ -14,10 +14,10 @@
 
 namespace gp {
 
-// Kernel status word, one per device (every device that loads the library
-// holds its own copy).  Kernels receive its address; gemm_stats(sync=1)
-// reads and clears it.
-__device__ uint32_t g_status_word;
+// Per-call status slots, a ring per device (every device that loads the
+// library holds its own copy: 32 KiB).  Call i on a device records a failed
+// wait in slot i mod kStatusSlots, tagged with its id (see kStatusSlots).
+__device__ unsigned long long g_status_ring[kStatusSlots];
 
 namespace {
 
@@ -28,24 +28,28 @@ constexpr int kMaxDevices = 64;
 // per-device caches
 // ---------------------------------------------------------------------------
 std::mutex g_mu;
-uint32_t* g_status_ptr[kMaxDevices] = {};
+unsigned long long* g_status_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
+uint32_t g_call_id[kMaxDevices] = {};
 
-cudaError_t device_info(int dev, uint32_t** status, int* sms) {
+// SM count of `dev` and, for a new call, its id and status slot.
+cudaError_t device_info(int dev, int* sms, uint32_t* call_id, unsigned long long** slot) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_status_ptr[dev]) {
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_status_ring);
     if (e != cudaSuccess) return e;
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    g_status_ptr[dev] = static_cast<unsigned long long*>(p);
     g_sm_count[dev] = n;
   }
-  *status = g_status_ptr[dev];
+  if (++g_call_id[dev] == 0) g_call_id[dev] = 1;   // 0 would match an untouched slot
   *sms = g_sm_count[dev];
+  *call_id = g_call_id[dev];
+  *slot = g_status_ptr[dev] + (g_call_id[dev] % kStatusSlots);
   return cudaSuccess;
 }
 
@@ -81,10 +85,15 @@ uint64_t g_tmap_clock = 0;
 // ---------------------------------------------------------------------------
 // stream-K workspace: per device and stream, grown on demand, never shrunk.
 // Calls on one stream are ordered, so one workspace per stream is race-free.
+// The table holds kMaxWorkspaces streams; a new stream beyond that takes over
+// the least recently used entry after a device-wide synchronisation (the
+// entry's stream may have been destroyed, so it is not used).  gemm_release
+// frees a device's workspaces.
 // ---------------------------------------------------------------------------
 struct Workspace {
   int dev = -1;
   cudaStream_t stream = nullptr;
+  uint64_t last_use = 0;
   float* partials = nullptr;
   size_t bytes = 0;
   uint32_t* flags = nullptr;
@@ -94,27 +103,63 @@ struct Workspace {
   size_t conv_bytes = 0;
   size_t conv_off = 0;        // region [conv_off, conv_off + conv_len) the last INT8 call on this stream used
   size_t conv_len = 0;
-  uint32_t* ov_ctrs = nullptr;   // INT8 overlap engine: two counter sets of ov_kcap + 1 words
+  uint32_t* ov_ctrs = nullptr;   // INT8 conversion / GEMM hand-off counters: two sets of ov_kcap + 1 words
   int32_t ov_kcap = 0;
   uint32_t ov_launches = 0;
 };
 constexpr int kMaxWorkspaces = 64;
 Workspace g_ws[kMaxWorkspaces];
+uint64_t g_ws_clock = 0;
 
-cudaError_t get_workspace(int dev, cudaStream_t stream, size_t bytes, size_t nflags, float** partials,
-                          uint32_t** flags, uint32_t* epoch) {
-  std::lock_guard<std::mutex> lk(g_mu);
+// Free an entry's buffers (nothing may still use them) and mark it empty.
+void free_workspace(Workspace& w) {
+  if (w.partials) cudaFree(w.partials);
+  if (w.flags) cudaFree(w.flags);
+  if (w.conv) cudaFree(w.conv);
+  if (w.ov_ctrs) cudaFree(w.ov_ctrs);
+  w = Workspace();
+}
+
+// The entry of (dev, stream), created if needed.  Caller holds g_mu; dev is current.
+cudaError_t find_workspace(int dev, cudaStream_t stream, Workspace** out) {
   Workspace* w = nullptr;
   for (auto& x : g_ws)
     if (x.dev == dev && x.stream == stream) { w = &x; break; }
   if (!w) {
     for (auto& x : g_ws)
       if (x.dev < 0) { w = &x; break; }
-    if (!w) return cudaErrorMemoryAllocation;   // more streams than slots
+  }
+  if (!w) {
+    // every entry taken: reclaim the least recently used one
+    Workspace* lru = &g_ws[0];
+    for (auto& x : g_ws)
+      if (x.last_use < lru->last_use) lru = &x;
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    const int owner = lru->dev;
+    if (owner != cur && (e = cudaSetDevice(owner)) != cudaSuccess) return e;
+    e = cudaDeviceSynchronize();   // whatever its stream still had in flight is done
+    if (e == cudaSuccess) free_workspace(*lru);
+    if (owner != cur) cudaSetDevice(cur);
+    if (e != cudaSuccess) return e;
+    w = lru;
+  }
+  if (w->dev < 0) {
     w->dev = dev;
     w->stream = stream;
   }
-  cudaError_t e;
+  w->last_use = ++g_ws_clock;
+  *out = w;
+  return cudaSuccess;
+}
+
+cudaError_t get_workspace(int dev, cudaStream_t stream, size_t bytes, size_t nflags, float** partials,
+                          uint32_t** flags, uint32_t* epoch) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace* w = nullptr;
+  cudaError_t e = find_workspace(dev, stream, &w);
+  if (e != cudaSuccess) return e;
   if (w->bytes < bytes) {
     if (w->partials) {
       if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
@@ -153,15 +198,8 @@ cudaError_t get_workspace(int dev, cudaStream_t stream, size_t bytes, size_t nfl
 cudaError_t get_conv_workspace(int dev, cudaStream_t stream, size_t bytes, void** conv, bool alternate = false) {
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace* w = nullptr;
-  for (auto& x : g_ws)
-    if (x.dev == dev && x.stream == stream) { w = &x; break; }
-  if (!w) {
-    for (auto& x : g_ws)
-      if (x.dev < 0) { w = &x; break; }
-    if (!w) return cudaErrorMemoryAllocation;
-    w->dev = dev;
-    w->stream = stream;
-  }
+  cudaError_t e0 = find_workspace(dev, stream, &w);
+  if (e0 != cudaSuccess) return e0;
   constexpr size_t kAlign = 256;
   const size_t above = (w->conv_off + w->conv_len + kAlign - 1) / kAlign * kAlign;
   size_t off = 0;
@@ -200,16 +238,8 @@ cudaError_t get_overlap_ctrs(int dev, cudaStream_t stream, int64_t k_tiles, uint
                              uint32_t* parity) {
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace* w = nullptr;
-  for (auto& x : g_ws)
-    if (x.dev == dev && x.stream == stream) { w = &x; break; }
-  if (!w) {
-    for (auto& x : g_ws)
-      if (x.dev < 0) { w = &x; break; }
-    if (!w) return cudaErrorMemoryAllocation;
-    w->dev = dev;
-    w->stream = stream;
-  }
-  cudaError_t e;
+  cudaError_t e = find_workspace(dev, stream, &w);
+  if (e != cudaSuccess) return e;
   if (w->ov_kcap < k_tiles) {
     if (w->ov_ctrs) {
       if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
@@ -237,6 +267,8 @@ struct LastCall {
   gp_stats stats;
   int device = -1;
   cudaStream_t stream = nullptr;
+  unsigned long long* status_slot = nullptr;   // the call's status slot and id (see kStatusSlots)
+  uint32_t call_id = 0;
   const void* kernel = nullptr;
   bool timed = false;
   cudaEvent_t ev[2] = {nullptr, nullptr};
@@ -339,7 +371,7 @@ void apply_i8_halves(gp_plan* p, int64_t workers) {
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
               int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, int i8_engine = 0,
-              int ffma_tm = 0, int ffma_tn = 0, int pair_k_split = 0) {
+              int ffma_tm = 0, int ffma_tn = 0, int pair_k_split = 0, bool one_tile = false) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
@@ -385,7 +417,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   if (pair_k_split < -1 || pair_k_split > 1) return GP_ERR_ARG;
   if (pair_k_split == 1 && (fam != 2 || !ring)) return GP_ERR_UNSUPPORTED;   // FP16/BF16 ring only
   const int i8_tc_stages = stages == 0 ? 6 : S;
-  if (fam == 1 && ring && i8_engine != 1 && !no_pair && (bn_req == 0 || bn_req == 256) &&
+  if (fam == 1 && ring && i8_engine != 1 && !no_pair && !one_tile && (bn_req == 0 || bn_req == 256) &&
       ring_smem_total(i8_tc_stages * kUmmaPairStageBytes, kUmmaEpiBytes) <= kSmemPerCtaMax) {
     // INT8 on tcgen05: FP16 operands, CTA pair per 256 x 256 tile.
     // Deeper rings than this tile allows (7, 8 stages) run on the IMMA ring.
@@ -471,7 +503,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   auto pair_fits = [&](int pbn) {
     return ring_smem_total(S * (kUmmaBM + pbn / 2) * kUmmaBK * 2, kUmmaEpiBytes) <= kSmemPerCtaMax;
   };
-  const bool pair_base = fam == 2 && ring && !no_pair && K > kShortK;
+  const bool pair_base = fam == 2 && ring && !no_pair && !one_tile && K > kShortK;
   const bool pair256 = pair_base && (bn_req == 0 || bn_req == 256) && N > 128 && pair_fits(256);
   const bool pair128 = pair_base && !pair256 && bn_req == 0 && N > 64 && M > 128 && pair_fits(128);
   // pair_k_split: a cluster of two pairs splits each 256 x 128 tile's K-loop
@@ -529,7 +561,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
       p->smem_bytes = kSmemPerCtaMax / 2 + 1024;
     }
   }
-  p->persistent = (ring && fam != 0) ? 1 : 0;
+  p->persistent = (ring && fam != 0 && !one_tile) ? 1 : 0;
   // FP16/BF16 ring on CTA pairs: 256 x BN tile per pair; per CTA per K step 128 rows of A and
   // BN/2 rows of B (32 KB for BN 256, 24 KB for BN 128)
   if (pair_ok) {
@@ -562,7 +594,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->dp_tiles = static_cast<int32_t>(p->tiles);
   p->sk_tiles = 0;
   p->workspace_bytes = 0;
-  if (fam == 0 && sm_count > 0 && p->tiles < sm_count && !no_stream_k) {
+  if (fam == 0 && sm_count > 0 && p->tiles < sm_count && !no_stream_k && !one_tile) {
     // FFMA: fewer tiles than SMs -- the tiles' K-loops, laid end to end, are
     // dealt out as equal ranges to k_splits CTAs per tile (at most
     // kFfmaMaxSplits, ranges of at least kFfmaMinSplitSteps K steps).  A whole
@@ -582,7 +614,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
       p->workspace_bytes = 2 * p->tiles * splits * p->bm * p->bn * 4;   // two FP32 partial slots per CTA
     }
   }
-  if (fam == 2 && ring && sm_count > 0) {
+  if (fam == 2 && ring && sm_count > 0 && !one_tile) {
     if (p->cta_pair == 3)
       ;   // whole tiles, each K-loop split over the cluster's two pairs
     else if (p->cta_pair)
@@ -752,7 +784,7 @@ using namespace gp;
 
 extern "C" {
 
-int gemm_abi_version(void) { return 10500; }
+int gemm_abi_version(void) { return 10600; }
 
 const char* gemm_strerror(int code) {
   switch (code) {
@@ -799,12 +831,14 @@ int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int sta
   const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
   return plan_impl(M, N, K, dtype, layout, stages, variant, opts ? opts->bn : 0, sms, out, opts && opts->no_stream_k,
                    no_pair, opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0,
-                   opts ? opts->pair_k_split : 0);
+                   opts ? opts->pair_k_split : 0, opts && opts->one_tile_per_cta);
 }
 
 int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
                       int stages, int variant, void* stream, const gp_options* opts) {
   std::memset(&t_last.stats, 0, sizeof(t_last.stats));
+  t_last.status_slot = nullptr;
+  t_last.call_id = 0;
   t_last.stats.last_ms = -1.f;
   t_last.kernel = nullptr;
   t_last.timed = false;
@@ -815,7 +849,8 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   gp_plan plan;
   int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan, opts && opts->no_stream_k,
                      opts && (opts->no_cta_pair || opts->inject_lost_load), opts ? opts->i8_engine : 0,
-                     opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, opts ? opts->pair_k_split : 0);
+                     opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, opts ? opts->pair_k_split : 0,
+                     opts && opts->one_tile_per_cta);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }   // empty output: nothing read or written
@@ -827,11 +862,14 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  uint32_t* status = nullptr;
+  unsigned long long* status = nullptr;
+  uint32_t call_id = 0;
   int sms = 0;
-  if (e == cudaSuccess) e = device_info(dev, &status, &sms);
+  if (e == cudaSuccess) e = device_info(dev, &sms, &call_id, &status);
   if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
   t_last.device = dev;
+  t_last.status_slot = status;
+  t_last.call_id = call_id;
   t_last.stats.sm_count = sms;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -855,7 +893,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
     rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
                    opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0,
-                   opts ? opts->pair_k_split : 0);
+                   opts ? opts->pair_k_split : 0, opts && opts->one_tile_per_cta);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     if (plan.cta_pair == 3) {
       int clusters = 0;
@@ -921,6 +959,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.plan = plan;
     a.stream = st;
     a.ctl.status = status;
+    a.ctl.call_id = call_id;
     a.ctl.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     a.ctl.inject_lost_load = opts ? opts->inject_lost_load : 0;
     a.ctl.inputs_ready = (opts && opts->inputs_ready) ? 1 : 0;
@@ -935,6 +974,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     a.conv_ctrs = conv_ctrs;
     a.conv_kcap = conv_kcap;
     a.conv_parity = conv_parity;
+    a.one_tile = opts && opts->one_tile_per_cta;
     const void* kernel = nullptr;
     switch (family_of(dtype)) {
       case 0: e = launch_ffma(a, &kernel); break;
@@ -956,6 +996,26 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   return GP_OK;
 }
 
+int gemm_release(int device) {
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+    cudaGetLastError();
+    return GP_ERR_CUDA;
+  }
+  if (device < 0 || device >= ndev || device >= kMaxDevices) return GP_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = 0;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return GP_ERR_CUDA;
+  if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return GP_ERR_CUDA;
+  e = cudaDeviceSynchronize();   // nothing on any stream of the device still uses a workspace
+  if (e == cudaSuccess)
+    for (auto& w : g_ws)
+      if (w.dev == device) free_workspace(w);
+  if (cur != device) cudaSetDevice(cur);
+  return e == cudaSuccess ? GP_OK : GP_ERR_CUDA;
+}
+
 int gemm_pipelined(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
                    int stages, int variant, void* stream) {
   return gemm_pipelined_ex(A, B, C, M, N, K, dtype, layout, stages, variant, stream, nullptr);
@@ -973,16 +1033,16 @@ int gemm_stats(gp_stats* out, int sync) {
     int prev = 0;
     cudaGetDevice(&prev);
     if (prev != t_last.device) cudaSetDevice(t_last.device);
-    cudaError_t e = cudaStreamSynchronize(t_last.stream);
-    if (e == cudaSuccess) {
-      uint32_t word = 0;
-      e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word));
-      if (e == cudaSuccess && word != 0) {
-        const uint32_t zero = 0;
-        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
-        s.device_status = word;
-        s.status = GP_ERR_TIMEOUT;
-      }
+    // the call's status slot, read on the call's own stream (after the call)
+    unsigned long long word = 0;
+    cudaError_t e = cudaSuccess;
+    if (t_last.status_slot)
+      e = cudaMemcpyAsync(&word, t_last.status_slot, sizeof(word), cudaMemcpyDeviceToHost, t_last.stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(t_last.stream);
+    if (e == cudaSuccess && t_last.status_slot && static_cast<uint32_t>(word >> 32) == t_last.call_id &&
+        static_cast<uint32_t>(word) != 0) {
+      s.device_status = static_cast<uint32_t>(word);
+      s.status = GP_ERR_TIMEOUT;
     }
     if (e != cudaSuccess) {
       s.status = GP_ERR_CUDA;
@@ -1012,6 +1072,8 @@ int gemm_stats(gp_stats* out, int sync) {
 int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
                            int stages, void* stream) {
   std::memset(&t_last.stats, 0, sizeof(t_last.stats));
+  t_last.status_slot = nullptr;
+  t_last.call_id = 0;
   t_last.stats.last_ms = -1.f;
   t_last.kernel = nullptr;
   t_last.timed = false;
@@ -1031,14 +1093,17 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  uint32_t* status = nullptr;
+  unsigned long long* status = nullptr;
+  uint32_t call_id = 0;
   int sms = 0;
-  if (e == cudaSuccess) e = device_info(dev, &status, &sms);
+  if (e == cudaSuccess) e = device_info(dev, &sms, &call_id, &status);
   unsigned char* scratch = nullptr;
   uint32_t epoch = 0;
   if (e == cudaSuccess) e = noalloc_setup(dev, &scratch, &epoch);
   if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
   t_last.device = dev;
+  t_last.status_slot = status;
+  t_last.call_id = call_id;
   t_last.stats.sm_count = sms;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -1078,6 +1143,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.plan = plan;
     a.stream = st;
     a.ctl.status = status;
+    a.ctl.call_id = call_id;
     a.ctl.timeout_ns = kDefaultTimeoutNs;
     a.ctl.inject_lost_load = 0;
     a.ctl.inputs_ready = 0;
@@ -1091,6 +1157,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     a.conv_ctrs = nullptr;
     a.conv_kcap = 0;
     a.conv_parity = 0;
+    a.one_tile = false;
     const void* kernel = nullptr;
     e = launch_umma(a, &kernel);
     t_last.stats.plan = a.plan;

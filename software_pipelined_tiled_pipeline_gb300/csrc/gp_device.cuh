@@ -29,9 +29,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Record the first error of a launch: code in the low byte, site above it.
-__device__ __forceinline__ void report_error(uint32_t* status, uint32_t code, uint32_t site) {
-  if (status) atomicCAS(status, 0u, code | (site << 8));
+// Record the first error of this call in its status slot: {call id, code in
+// the low byte, wait site above it}.  A record of another call is replaced.
+__device__ __forceinline__ void report_error(const KernelCtl& ctl, uint32_t code, uint32_t site) {
+  if (!ctl.status) return;
+  const unsigned long long mine = (static_cast<unsigned long long>(ctl.call_id) << 32) | code | (site << 8);
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctl.status);
+  for (;;) {
+    if (static_cast<uint32_t>(old >> 32) == ctl.call_id) return;   // this call has a record already
+    const unsigned long long seen = atomicCAS(ctl.status, old, mine);
+    if (seen == old) return;
+    old = seen;
+  }
 }
 
 // Per-CTA control block kept in shared memory.
@@ -115,7 +124,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if ((i & 31u) == 0) {
       if (cta->abort) return false;
       if (global_timer_ns() - t0 > ctl.timeout_ns) {
-        report_error(ctl.status, kDevErrTimeout, site);
+        report_error(ctl, kDevErrTimeout, site);
         cta->abort = 1;
         return false;
       }
@@ -147,7 +156,7 @@ __device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t pa
     if ((i & 31u) == 0) {
       if (cta->abort) return false;
       if (global_timer_ns() - t0 > ctl.timeout_ns) {
-        report_error(ctl.status, kDevErrTimeout, site);
+        report_error(ctl, kDevErrTimeout, site);
         cta->abort = 1;
         return false;
       }

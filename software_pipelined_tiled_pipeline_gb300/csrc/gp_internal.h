@@ -11,9 +11,17 @@
 namespace gp {
 
 // ---------------------------------------------------------------------------
-// device status word
+// per-call status
 // ---------------------------------------------------------------------------
+// Every call gets a nonzero 32-bit id and one slot of a per-device ring of
+// kStatusSlots 64-bit words (slot = id mod kStatusSlots).  A kernel that gives
+// up a wait stores {id, code | site << 8} there (the first error of the call
+// wins; a record of another call in the slot is overwritten).  The host reads
+// the slot on the call's own stream and takes a record as this call's only if
+// its id matches, so slots never need clearing and concurrent calls on other
+// streams cannot report or clear each other's errors.
 constexpr uint32_t kDevErrTimeout = 1;  // a bounded wait gave up
+constexpr int kStatusSlots = 4096;
 
 // wait-site codes (bits 8.. of the status word) -- which wait gave up
 enum WaitSite : uint32_t {
@@ -29,7 +37,8 @@ enum WaitSite : uint32_t {
 };
 
 struct KernelCtl {
-  uint32_t* status;         // device word, 0 = clean
+  unsigned long long* status;   // this call's status slot (see kStatusSlots)
+  uint32_t call_id;             // tag of this call's records in it
   uint64_t timeout_ns;      // limit of every bounded wait
   int32_t inject_lost_load; // test hook: producer skips the final tile load
   int32_t inputs_ready;     // FP16/BF16 ring: the caller promised that nothing in flight writes A or B,
@@ -149,6 +158,7 @@ struct LaunchArgs {
   uint32_t* conv_ctrs;      // ... its two counter sets: {batch counter, conv_kcap K-step counters}
   int32_t conv_kcap;
   uint32_t conv_parity;     // ... the set this launch uses (it zeroes the other)
+  bool one_tile;            // gp_options.one_tile_per_cta: one output tile per CTA, grid = tiles
   int32_t sm_count;
 };
 

@@ -345,6 +345,13 @@ __global__ void __launch_bounds__(Tile<TM, TN>::THREADS + 32, 1)
     bool ok = true;
     int consumed = 0;
     bool waited = false;
+    if (!ctl.inputs_ready) {
+      // The producer's loads start only after the previous kernel has completed,
+      // so start the bounded waits on full slots only then too: a long-running
+      // predecessor must not use up their time limit.
+      pdl_wait();
+      waited = true;
+    }
     while (ok && wk.next(tile, u0, u1, seg)) {
       int mb, nb;
       tile_coords(tile, m_blocks, n_blocks, mb, nb);

@@ -340,7 +340,7 @@ cudaError_t launch_bn(LaunchArgs& a, const void** kernel) {
     int occ = 1;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, p.threads, p.smem_bytes)) != cudaSuccess) return e;
     if (occ < 1) occ = 1;
-    const int64_t cap = static_cast<int64_t>(a.sm_count) * occ;
+    const int64_t cap = a.one_tile ? p.tiles : static_cast<int64_t>(a.sm_count) * occ;
     p.grid = static_cast<int32_t>(p.tiles < cap ? p.tiles : cap);
     k<<<p.grid, p.threads, p.smem_bytes, a.stream>>>(tmA, tmB, static_cast<int32_t*>(a.C), a.M, a.N, a.K, p.stages,
                                                       a.ctl);

@@ -861,6 +861,13 @@ __device__ __forceinline__ void stage_and_store_i32(const uint32_t* v, uint8_t* 
   if (lane == 0) bulk_commit();
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Threads: warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 epilogue.
 // Epilogue warp w reads TMEM lane quarter w % 4 and column half (w - 2) / 4,
 // so each thread keeps the int32 running sums of 128 accumulator columns.
@@ -1256,13 +1263,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
-}
-
 __global__ void __launch_bounds__(kOvThreads, 1)
     umma_i8_overlap_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA8,
@@ -1477,7 +1477,7 @@ __global__ void __launch_bounds__(kOvThreads, 1)
               if (kb < ready) break;
               if (cta->abort) goto ov_producer_done;
               if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                report_error(ctl.status, kDevErrTimeout, kSiteConvReady);
+                report_error(ctl, kDevErrTimeout, kSiteConvReady);
                 cta->abort = 1;
                 goto ov_producer_done;
               }

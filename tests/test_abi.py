@@ -44,7 +44,7 @@ def test_library_exports_every_declared_function(gp):
 
 
 def test_version_and_strerror(gp):
-    assert gp.abi_version() == 10500
+    assert gp.abi_version() == 10600
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert gp.strerror(code) and "unknown" not in gp.strerror(code)
     assert "unknown" in gp.strerror(-99)
@@ -334,6 +334,23 @@ def test_no_512_wide_tile(gp):
                              (4096, 4096, 256, "f16", "row_col"), (4096, 4096, 4096, "f32", "row_row"),
                              (4096, 4096, 4096, "i8", "row_col"), (4096, 128, 4096, "bf16", "row_col")]:
         assert gp.gemm_plan_rc(M, N, K, dt, lay, 0, "pipelined", bn=512) == gp.GP_ERR_UNSUPPORTED
+
+
+def test_one_tile_per_cta_plan(gp):
+    # the ring on the ping-pong kernel's launch shape: one CTA per 128 x 256 tile, grid = tiles,
+    # not persistent, no pairs, no stream-K; same tile as the register-staged variants
+    for S in (1, 2, 3, 4):
+        r = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined", plan_sms=152, one_tile_per_cta=True)
+        assert (r["kernel"], r["bm"], r["bn"], r["bk"], r["cta_pair"]) == ("umma_ring", 128, 256, 64, 0)
+        assert (r["grid"], r["tiles"], r["persistent"], r["sk_tiles"]) == (512, 512, 0, 0)
+    pp = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 2, "pingpong", plan_sms=152)
+    assert (pp["bm"], pp["bn"], pp["bk"], pp["grid"]) == (128, 256, 64, 512)
+    i = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 4, "pipelined", plan_sms=152, one_tile_per_cta=True)
+    ip = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 2, "pingpong", plan_sms=152)
+    assert (i["kernel"], i["bm"], i["bn"], i["persistent"]) == ("imma_ring", ip["bm"], ip["bn"], 0)
+    assert i["tiles"] == ip["tiles"] == ip["grid"]
+    f = gp.gemm_plan(1024, 1024, 1024, "f32", "row_row", 3, "pipelined", plan_sms=152, one_tile_per_cta=True)
+    assert (f["k_splits"], f["grid"]) == (1, 64)
 
 
 def test_pair_k_split_plan(gp):

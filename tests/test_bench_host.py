@@ -115,3 +115,39 @@ def test_traffic_records_are_well_formed():
         assert rec["dram_bytes_per_launch"] == rec["dram_read"] + rec["dram_write"] > 0, key
         assert len(rec["source_sha"]) == 16 and int(rec["source_sha"], 16) >= 0, key
         assert os.path.exists(os.path.join(os.path.dirname(path), os.path.basename(rec["capture"]))), key
+
+
+def test_final_line_fits_the_driver_tail():
+    # a line as large as the bench builds it stays under 2 KB: optional keys go, required ones stay
+    line = {"metric": bench.METRIC, "value": 1690.12, "unit": "TFLOPS", "n_gpus": 1, "steps": 20, "warmup": 5,
+            "ms_per_step": 0.08134, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "f16_4096", "M": 4096, "N": 4096, "K": 4096, "layout": "row_col",
+                       "variant": "pipelined", "stages": 5, "kernel": "umma_pair_ring", "tile": "256x256x64",
+                       "grid": 152, "l2": "inputs and output rotated over 4 buffer sets (384 MiB > 129 MB L2)",
+                       "parallelism": "single"},
+            "roofline": {"kernel": "umma_pair_ring", "kernel_avg_ms": 0.08134, "launch_isolated_ms": 0.0851,
+                         "traffic": 144812345, "bound": "tensor", "achieved": 1690.12, "peak": 1920.5,
+                         "unit": "TFLOP/s", "frac": 0.88,
+                         "peak_source": "measured (MEASURED_PEAKS.json): dense bf16 burst (FP16 at the same rate)"},
+            "e2e": {"value": 372.1, "unit": "TFLOPS", "h2d_bytes_per_step": 67108864, "d2h_bytes_per_step": 33554432},
+            "gpu_launches": 20, "clocks": {"sm_mhz": 1560.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                                           "samples": 33},
+            "library_same_shape": {"value": 1760.2, "ours_over_library": 0.951},
+            "sustained": {"value": 1455.2, "frac": 0.848, "seconds": 3.01, "sm_mhz": 1540.0},
+            "int8_4096": {"TOPS": 1398.2, "frac": 0.728, "stages": 6, "kernel": "umma_i8_pair_ring",
+                          "launches_per_call": 2, "imma_ring_TOPS": 147.6, "imma_ceiling": 158.2},
+            "int8_4096_inputs_ready": {"TOPS": 1430.1, "frac": 0.745, "caller_promise": True},
+            "f16_stages": {"2": 979.1, "3": 1384.2, "4": 1551.3, "5": 1649.1, "6": 1645.2, "pingpong": 495.1},
+            "f16_best_stage": 5, "pipelining_gain_like_for_like": {"f16_ring_s2_over_pingpong": 1.512},
+            "fp32_1024": {"TFLOPS": 41.8, "frac_alu": 0.5193, "s2_over_pingpong": 1.79, "pingpong_TFLOPS": 23.3},
+            "cpu_baseline": {"value": 0.044698, "unit": "TFLOPS", "cores": 16, "kind": "oracle",
+                             "sample": "first 512 of 4096 rows of C in 10.1 s"},
+            "sweep_file": "gpurun_out/bench_sweep.json"}
+    out = bench.compact_line(dict(line))
+    assert len(json.dumps(out)) < 2000
+    for k in ("metric", "value", "unit", "roofline", "e2e", "cpu_baseline", "clocks", "config", "gpu_launches"):
+        assert k in out
+    big = dict(line, padding="x" * 3000)
+    out = bench.compact_line(big)
+    assert len(json.dumps(out)) < 2000 and "padding" not in out and "roofline" in out

@@ -39,6 +39,11 @@ def test_i8_4096_bit_exact_every_stage_and_variant():
     for S in w.stages:
         C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S, i8_engine="imma")
         assert torch.equal(C, ref)
+    for S in (2, 6):
+        C, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S,
+                    i8_engine="tcgen05_2pass")
+        assert st["plan"]["kernel"] == "umma_i8_pair_ring"
+        assert torch.equal(C, ref)
     for variant in ("pingpong", "nopipe"):
         C, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant=variant)
         assert torch.equal(C, ref)

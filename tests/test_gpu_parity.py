@@ -150,6 +150,11 @@ def test_all_variants_and_depths_bitwise_identical(dtype):
     outs = [run(dtype, lay, A, B, M, N, K, variant="pingpong", no_stream_k=True)[0]]
     for S in range(1, 9):
         outs.append(run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, no_stream_k=True)[0])
+    for S in (1, 2, 4):
+        # the ring on the ping-pong kernel's launch shape (one CTA per tile)
+        o, st1 = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=S, one_tile_per_cta=True)
+        assert st1["plan"]["grid"] == st1["plan"]["tiles"] and st1["plan"]["persistent"] == 0
+        outs.append(o)
     for o in outs:
         assert torch.equal(o.view(torch.int16) if o.dtype in (torch.float16, torch.bfloat16) else o,
                            ref.view(torch.int16) if ref.dtype in (torch.float16, torch.bfloat16) else ref)
@@ -407,6 +412,7 @@ def test_int8_overlapped_conversion_matches_two_pass(M, N, K):
     C3, st3 = run("i8", "row_col", A, B, M, N, K, variant="pipelined", i8_engine="tcgen05_overlap")
     assert st3["plan"]["kernel"] == "umma_i8_overlap_pair_ring" and st3["plan"]["sk_tiles"] == 0
     assert torch.equal(C2, C3)
+
     if M * N * K <= 3e9:
         check_full("i8", "row_col", A, B, C3, K)
     else:

@@ -27,9 +27,9 @@ def _cases(dtype, n, seed):
         S = int(rng.integers(1, 9)) if variant == "pipelined" else 0
         opts = {}
         if dtype in ("f16", "bf16") and variant == "pipelined":
-            opts = [{}, {"no_stream_k": True}, {"no_cta_pair": True}][int(rng.integers(0, 3))]
+            opts = [{}, {"no_stream_k": True}, {"no_cta_pair": True}, {"one_tile_per_cta": True}][int(rng.integers(0, 4))]
         if dtype == "i8" and variant == "pipelined" and rng.integers(0, 2):
-            opts = {"i8_engine": "imma"}
+            opts = [{"i8_engine": "imma"}, {"one_tile_per_cta": True}][int(rng.integers(0, 2))]
         if dtype == "f32" and variant == "pipelined" and rng.integers(0, 2):
             opts = {"ffma_tile": [(4, 8), (8, 4), (8, 16), (16, 8)][int(rng.integers(0, 4))]}
         out.append((M, N, K, variant, S, opts))
