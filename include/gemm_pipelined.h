@@ -111,6 +111,16 @@ typedef enum {
 #define GP_ERR_SIZE (-6)        /* a dimension exceeds what the variant can address (see gemm_pipelined) */
 #define GP_ERR_SCRATCH (-7)     /* gemm_pipelined_noalloc: the plan needs more scratch than its fixed array holds */
 
+/* Step of a call whose CUDA runtime call failed (gp_stats.cuda_error_site; 0 when nothing failed). */
+#define GP_SITE_DEVICE 1        /* device query or the per-device set-up */
+#define GP_SITE_EVENT 2         /* timing events (gp_options.time_kernel) */
+#define GP_SITE_CAPACITY 3      /* occupancy query of a cluster kernel */
+#define GP_SITE_WORKSPACE 4     /* device workspace allocation */
+#define GP_SITE_TENSOR_MAP 5    /* TMA tensor-map encoding */
+#define GP_SITE_SMEM_ATTR 6     /* opting a kernel into its dynamic shared memory */
+#define GP_SITE_LAUNCH 7        /* the kernel launch itself */
+#define GP_SITE_SYNC 8          /* gemm_stats(sync=1): reading the status record or synchronising */
+
 /* Tile, stage and resource choice for one problem ("pipeline-gpu-kernel",
  * Step 1 "shared-memory budget" and Step 2 "compute/load ratio"; "Part 4 --
  * Pipelining and Occupancy", section 4.2). */
@@ -143,6 +153,8 @@ typedef struct gp_plan {
     int32_t half_tiles;          /* INT8 on tcgen05: the last tiles (after dp_tiles whole ones), each run as two
                                     BM x BN/2 halves by two workers, when the whole tiles would leave a last
                                     wave at most half full; 0 = none */
+    int32_t raster_gm;           /* tile order: groups of raster_gm consecutive BM-row blocks, each group swept
+                                    over all N blocks (N block major inside a group), groups in turn */
 } gp_plan;
 
 /* Record of the last gemm_pipelined call made by the calling host thread. */
@@ -157,6 +169,7 @@ typedef struct gp_stats {
     uint32_t device_status;      /* the call's status record: 0 = clean, else code | wait site << 8;
                                     valid after gemm_stats(sync=1) */
     float last_ms;               /* kernel time from CUDA events if timing was requested, else -1 */
+    int32_t cuda_error_site;     /* GP_SITE_* of the failing CUDA call when cuda_error != 0, else 0 */
 } gp_stats;
 
 /* Per-call options for gemm_pipelined_ex.  Zero-initialise and set what you need. */
@@ -199,6 +212,8 @@ typedef struct gp_options {
                                     launch shape of the ping-pong and no-overlap variants, so that the three data
                                     paths can be compared with nothing else changed ("CUDA Kernel Study:
                                     Pipelining", Benchmark Results).  0 = the planner's choice */
+    int32_t raster_gm;           /* persistent tcgen05 rings: M blocks per raster group (gp_plan.raster_gm);
+                                    0 = the planner's choice; negative: GP_ERR_ARG */
 } gp_options;
 
 /*

@@ -31,6 +31,9 @@ GP_ERR_CUDA = -4
 GP_ERR_TIMEOUT = -5
 GP_ERR_SIZE = -6
 GP_ERR_SCRATCH = -7
+# gp_stats.cuda_error_site
+SITES = {1: "device", 2: "event", 3: "capacity", 4: "workspace", 5: "tensor_map", 6: "smem_attr", 7: "launch",
+         8: "sync"}
 
 DTYPES = {"i8": GP_I8_I32, "f16": GP_F16_F32ACC_F16OUT, "bf16": GP_BF16_F32ACC_BF16OUT, "f32": GP_F32}
 LAYOUTS = {"row_col": GP_A_ROW_B_COL, "row_row": GP_A_ROW_B_ROW}
@@ -51,6 +54,7 @@ class GpPlan(ctypes.Structure):
         ("compute_load_ratio", ctypes.c_double), ("kernel", ctypes.c_char_p),
         ("dp_tiles", ctypes.c_int32), ("sk_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
         ("cta_pair", ctypes.c_int32), ("k_splits", ctypes.c_int32), ("half_tiles", ctypes.c_int32),
+        ("raster_gm", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -64,6 +68,7 @@ class GpStats(ctypes.Structure):
         ("plan", GpPlan), ("status", ctypes.c_int32), ("cuda_error", ctypes.c_int32),
         ("regs_per_thread", ctypes.c_int32), ("local_bytes", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
         ("sm_count", ctypes.c_int32), ("device_status", ctypes.c_uint32), ("last_ms", ctypes.c_float),
+        ("cuda_error_site", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -78,7 +83,7 @@ class GpOptions(ctypes.Structure):
         ("inject_lost_load", ctypes.c_int32), ("no_stream_k", ctypes.c_int32), ("no_cta_pair", ctypes.c_int32),
         ("i8_engine", ctypes.c_int32), ("ffma_tm", ctypes.c_int32), ("ffma_tn", ctypes.c_int32),
         ("plan_sms", ctypes.c_int32), ("inputs_ready", ctypes.c_int32), ("pair_k_split", ctypes.c_int32),
-        ("one_tile_per_cta", ctypes.c_int32),
+        ("one_tile_per_cta", ctypes.c_int32), ("raster_gm", ctypes.c_int32),
     ]
 
 
@@ -159,7 +164,8 @@ I8_ENGINES = {"default": 0, "imma": 1, "tcgen05_2pass": 2, "tcgen05_overlap": 3}
 
 
 def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
-             ffma_tile=None, i8_engine=0, plan_sms=0, inputs_ready=False, pair_k_split=0, one_tile_per_cta=False):
+             ffma_tile=None, i8_engine=0, plan_sms=0, inputs_ready=False, pair_k_split=0, one_tile_per_cta=False,
+             raster_gm=0):
     opts = GpOptions()
     opts.bn = int(bn)
     opts.time_kernel = 1 if time_kernel else 0
@@ -174,23 +180,26 @@ def _options(bn=0, time_kernel=False, timeout_ns=0, inject_lost_load=False, no_s
     opts.inputs_ready = 1 if inputs_ready else 0
     opts.pair_k_split = int(pair_k_split)
     opts.one_tile_per_cta = 1 if one_tile_per_cta else 0
+    opts.raster_gm = int(raster_gm)
     return opts
 
 
 def gemm_pipelined(A, B, C, M, N, K, dtype, layout, stages=0, variant="pipelined", stream=0, *, bn=0,
                    time_kernel=False, timeout_ns=0, inject_lost_load=False, no_stream_k=False, no_cta_pair=False,
                    ffma_tile=None, i8_engine=0, inputs_ready=False, pair_k_split=0, one_tile_per_cta=False,
-                   check=True) -> int:
+                   raster_gm=0, check=True) -> int:
     """C = A x B through the C ABI.  A, B, C: device tensors or raw pointers.
     stream: a torch.cuda.Stream, a raw cudaStream_t (int) or 0.
     ffma_tile: (rows, columns) of outputs per thread of the FP32 ring (default 8 x 8).
     i8_engine: INT8 ring engine, a name of I8_ENGINES or its number ("default" lets the planner pick).
     inputs_ready: promise that no work still in flight on the stream writes A or B (see gp_options).
     pair_k_split: 1 = split 256 x 128 tiles' K-loops over two CTA pairs (see gp_options), -1 = never.
-    one_tile_per_cta: the ring on the launch shape of the ping-pong kernel (one CTA per tile)."""
+    one_tile_per_cta: the ring on the launch shape of the ping-pong kernel (one CTA per tile).
+    raster_gm: M blocks per group of the persistent rings' tile raster (0 = the planner's choice)."""
     s = getattr(stream, "cuda_stream", stream)
     opts = _options(bn, time_kernel, timeout_ns, inject_lost_load, no_stream_k, no_cta_pair, ffma_tile, i8_engine,
-                    inputs_ready=inputs_ready, pair_k_split=pair_k_split, one_tile_per_cta=one_tile_per_cta)
+                    inputs_ready=inputs_ready, pair_k_split=pair_k_split, one_tile_per_cta=one_tile_per_cta,
+                    raster_gm=raster_gm)
     rc = lib().gemm_pipelined_ex(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), _enum(dtype, DTYPES, "dtype"),
                                  _enum(layout, LAYOUTS, "layout"), int(stages), _enum(variant, VARIANTS, "variant"),
                                  s or None, ctypes.byref(opts))

@@ -322,6 +322,23 @@ static_assert(i8_overlap_staging_slots(kI8OverlapDefaultStages) >= 2 &&
 // INT8 on tcgen05: bytes of the FP16 copies of A and B.
 int64_t i8_conv_bytes(int64_t M, int64_t N, int64_t K) { return (M + N) * K * 2; }
 
+// M blocks per group of the tile raster of the persistent tcgen05 rings:
+// one group over all of them when there are at most kWholeRasterBlocks and
+// their A panels take at most kWholeRasterBytes (every wave then sweeps the
+// whole of A, which stays in L2, while each B panel is read by one wave's
+// worth of tiles at once: at FP16 4096^3, 124 against 144 MB of DRAM traffic
+// per launch and 2 % less time than groups of 8), else groups of 8 (measured
+// as fast or faster on 8192-row problems: BF16 8192^2 x 16384, 1166 against
+// 1202 us with groups of 4).
+constexpr int kDefaultRasterGM = 8;
+constexpr int64_t kWholeRasterBlocks = 16;
+constexpr int64_t kWholeRasterBytes = int64_t(48) << 20;
+int auto_raster_gm(int64_t M, int64_t K, int bm, int in_bytes) {
+  const int64_t m_blocks = (M + bm - 1) / bm;
+  if (m_blocks <= kWholeRasterBlocks && M * K * in_bytes <= kWholeRasterBytes) return static_cast<int>(m_blocks);
+  return kDefaultRasterGM;
+}
+
 // FP16/BF16 GEMMs with K up to this many elements run one CTA per tile, not CTA pairs.
 constexpr int64_t kShortK = 256;
 // FP16/BF16 GEMMs with K at least this long default to 5 ring stages (6 below).
@@ -371,13 +388,13 @@ void apply_i8_halves(gp_plan* p, int64_t workers) {
 // Tile/stage choice.  sm_count <= 0: no device queried (grid left 0 for persistent kernels).
 int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages, int variant, int bn_req,
               int sm_count, gp_plan* p, bool no_stream_k = false, bool no_pair = false, int i8_engine = 0,
-              int ffma_tm = 0, int ffma_tn = 0, int pair_k_split = 0, bool one_tile = false) {
+              int ffma_tm = 0, int ffma_tn = 0, int pair_k_split = 0, bool one_tile = false, int raster_gm = 0) {
   if (dtype < GP_I8_I32 || dtype > GP_F32) return GP_ERR_ARG;
   if (layout != GP_A_ROW_B_COL && layout != GP_A_ROW_B_ROW) return GP_ERR_ARG;
   if (variant < GP_PINGPONG || variant > GP_NOPIPE) return GP_ERR_ARG;
   if (M < 0 || N < 0 || K < 0) return GP_ERR_ARG;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GP_ERR_SIZE;
-  if (bn_req < 0) return GP_ERR_ARG;
+  if (bn_req < 0 || raster_gm < 0) return GP_ERR_ARG;
   const int fam = family_of(dtype);
   if (fam == 0 && layout != GP_A_ROW_B_ROW) return GP_ERR_UNSUPPORTED;
   if (fam != 0 && layout != GP_A_ROW_B_COL) return GP_ERR_UNSUPPORTED;
@@ -407,6 +424,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
 
   std::memset(p, 0, sizeof(*p));
   p->k_splits = 1;
+  p->raster_gm = raster_gm > 0 ? raster_gm : kDefaultRasterGM;   // (the tcgen05 tiles refine the default below)
   p->dtype = dtype;
   p->layout = layout;
   p->variant = variant;
@@ -445,6 +463,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
     p->k_tiles = ceil_div(K, p->bk);
     if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
+    if (raster_gm <= 0) p->raster_gm = auto_raster_gm(M, K, p->bm, 2);   // the FP16 copies are what is read
     p->grid = sm_count > 1 ? static_cast<int32_t>(2 * (p->tiles < sm_count / 2 ? p->tiles : sm_count / 2)) : 0;
     p->dp_tiles = static_cast<int32_t>(p->tiles);
     p->sk_tiles = 0;
@@ -583,6 +602,7 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->tiles = ceil_div(M, p->bm) * ceil_div(N, p->bn);
   p->k_tiles = ceil_div(K, p->bk);
   if (p->tiles > INT32_MAX) return GP_ERR_SIZE;
+  if (fam == 2 && ring && raster_gm <= 0) p->raster_gm = auto_raster_gm(M, K, p->bm, in_elem_bytes(dtype));
   if (p->cta_pair == 3)
     p->grid = sm_count > 3 ? static_cast<int32_t>(4 * (p->tiles < sm_count / 4 ? p->tiles : sm_count / 4)) : 0;
   else if (p->cta_pair)
@@ -640,9 +660,14 @@ int alignment_ok(const void* A, const void* B, const void* C, int64_t N, int64_t
   }
 }
 
-void record(int status, int cuda_err) {
+// Step of the call whose CUDA call failed (a GP_SITE_* code); helpers that run
+// inside the kernel-family launchers set it when they fail.
+thread_local int t_fail_site = 0;
+
+void record(int status, int cuda_err, int site = 0) {
   t_last.stats.status = status;
   t_last.stats.cuda_error = cuda_err;
+  t_last.stats.cuda_error_site = cuda_err ? site : 0;
   t_last.valid = true;
 }
 
@@ -671,8 +696,22 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
     e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+      t_fail_site = GP_SITE_TENSOR_MAP;
+      return e != cudaSuccess ? e : cudaErrorNotSupported;
+    }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // The encode is a driver call: it needs the device's context current in this
+  // host thread, which a thread that has only queried the device may not have
+  // yet (cudaSetDevice makes the primary context current).
+  thread_local int ctx_dev = -1;
+  if (ctx_dev != dev) {
+    if ((e = cudaSetDevice(dev)) != cudaSuccess) {
+      t_fail_site = GP_SITE_TENSOR_MAP;
+      return e;
+    }
+    ctx_dev = dev;
   }
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
@@ -682,7 +721,10 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
   const CUresult r = g_encode(&m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) {
+    t_fail_site = GP_SITE_TENSOR_MAP;
+    return cudaErrorInvalidValue;
+  }
   TmapEntry* victim = &g_tmaps[0];
   for (auto& t : g_tmaps) {
     if (!t.used) { victim = &t; break; }
@@ -708,11 +750,13 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
   // the opt-in limit covers static and dynamic shared memory together
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kernel);
-  if (e != cudaSuccess) return e;
   const int max_dynamic = kSmemPerCtaMax - static_cast<int>(fa.sharedSizeBytes);
-  if (bytes > max_dynamic) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
-  if (e != cudaSuccess) return e;
+  if (e == cudaSuccess && bytes > max_dynamic) e = cudaErrorInvalidValue;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic);
+  if (e != cudaSuccess) {
+    t_fail_site = GP_SITE_SMEM_ATTR;
+    return e;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   done.insert({dev, kernel});
   return cudaSuccess;
@@ -784,7 +828,7 @@ using namespace gp;
 
 extern "C" {
 
-int gemm_abi_version(void) { return 10600; }
+int gemm_abi_version(void) { return 10700; }
 
 const char* gemm_strerror(int code) {
   switch (code) {
@@ -831,7 +875,7 @@ int gemm_plan_ex(int64_t M, int64_t N, int64_t K, int dtype, int layout, int sta
   const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
   return plan_impl(M, N, K, dtype, layout, stages, variant, opts ? opts->bn : 0, sms, out, opts && opts->no_stream_k,
                    no_pair, opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0,
-                   opts ? opts->pair_k_split : 0, opts && opts->one_tile_per_cta);
+                   opts ? opts->pair_k_split : 0, opts && opts->one_tile_per_cta, opts ? opts->raster_gm : 0);
 }
 
 int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int layout,
@@ -839,6 +883,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   std::memset(&t_last.stats, 0, sizeof(t_last.stats));
   t_last.status_slot = nullptr;
   t_last.call_id = 0;
+  t_fail_site = 0;
   t_last.stats.last_ms = -1.f;
   t_last.kernel = nullptr;
   t_last.timed = false;
@@ -850,7 +895,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   int rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, 0, &plan, opts && opts->no_stream_k,
                      opts && (opts->no_cta_pair || opts->inject_lost_load), opts ? opts->i8_engine : 0,
                      opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0, opts ? opts->pair_k_split : 0,
-                     opts && opts->one_tile_per_cta);
+                     opts && opts->one_tile_per_cta, opts ? opts->raster_gm : 0);
   if (rc != GP_OK) { record(rc, 0); return rc; }
   t_last.stats.plan = plan;
   if (M == 0 || N == 0) { record(GP_OK, 0); return GP_OK; }   // empty output: nothing read or written
@@ -866,7 +911,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
   uint32_t call_id = 0;
   int sms = 0;
   if (e == cudaSuccess) e = device_info(dev, &sms, &call_id, &status);
-  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_DEVICE); return GP_ERR_CUDA; }
   t_last.device = dev;
   t_last.status_slot = status;
   t_last.call_id = call_id;
@@ -879,7 +924,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
       if (t_last.ev[0]) { cudaEventDestroy(t_last.ev[0]); cudaEventDestroy(t_last.ev[1]); }
       t_last.ev[0] = t_last.ev[1] = nullptr;
       if ((e = cudaEventCreate(&t_last.ev[0])) != cudaSuccess || (e = cudaEventCreate(&t_last.ev[1])) != cudaSuccess) {
-        record(GP_ERR_CUDA, e);
+        record(GP_ERR_CUDA, e, GP_SITE_EVENT);
         return GP_ERR_CUDA;
       }
       t_last.ev_device = dev;
@@ -893,13 +938,13 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     const bool no_pair = opts && (opts->no_cta_pair || opts->inject_lost_load);
     rc = plan_impl(M, N, K, dtype, layout, stages, variant, bn_req, sms, &plan, opts && opts->no_stream_k, no_pair,
                    opts ? opts->i8_engine : 0, opts ? opts->ffma_tm : 0, opts ? opts->ffma_tn : 0,
-                   opts ? opts->pair_k_split : 0, opts && opts->one_tile_per_cta);
+                   opts ? opts->pair_k_split : 0, opts && opts->one_tile_per_cta, opts ? opts->raster_gm : 0);
     if (rc != GP_OK) { record(rc, 0); return rc; }
     if (plan.cta_pair == 3) {
       int clusters = 0;
       e = umma_kx_capacity(dtype, plan.smem_bytes, &clusters);
       if (e == cudaSuccess && clusters < 1) e = cudaErrorLaunchOutOfResources;
-      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_CAPACITY); return GP_ERR_CUDA; }
       if (4 * clusters < plan.grid) plan.grid = 4 * clusters;
     }
     void* conv = nullptr;
@@ -914,7 +959,7 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
       int pairs = 0;
       e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs, i8_overlap);
       if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
-      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_CAPACITY); return GP_ERR_CUDA; }
       if (pairs < sms / 2 && !i8_overlap && (!i8_tc || plan.tiles < pairs)) {
         apply_stream_k(&plan, pairs, 2, !(opts && opts->no_stream_k));
         plan.workspace_bytes += conv_bytes;
@@ -923,27 +968,27 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
       if (i8_tc) {
         e = get_conv_workspace(dev, st, static_cast<size_t>(conv_bytes), &conv,
                                !i8_overlap && opts && opts->inputs_ready);
-        if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+        if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_WORKSPACE); return GP_ERR_CUDA; }
       }
       if (i8_overlap) {
         e = get_overlap_ctrs(dev, st, plan.k_tiles, &conv_ctrs, &conv_kcap, &conv_parity);
-        if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+        if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_WORKSPACE); return GP_ERR_CUDA; }
       }
     }
-    SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, 0};
+    SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, 0, plan.raster_gm};
     if (plan.sk_tiles > 0) {
       const size_t counter_words =
           static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair ? 2 : 1) * 2;
       e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes - conv_bytes), counter_words, &sk.workspace,
                         &sk.flags, &sk.epoch);
-      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_WORKSPACE); return GP_ERR_CUDA; }
     }
     FfmaSplit ks{plan.k_splits, nullptr, nullptr, 0};
     if (plan.k_splits > 1) {
       uint32_t* counters = nullptr;
       e = get_workspace(dev, st, static_cast<size_t>(plan.workspace_bytes), static_cast<size_t>(plan.tiles) * 2,
                         &ks.workspace, &counters, &ks.epoch);
-      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_WORKSPACE); return GP_ERR_CUDA; }
       ks.counters = reinterpret_cast<unsigned long long*>(counters);
     }
     LaunchArgs a;
@@ -987,7 +1032,10 @@ int gemm_pipelined_ex(const void* A, const void* B, void* C, int64_t M, int64_t 
     t_last.stats.plan = a.plan;
     t_last.kernel = kernel;
   }
-  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  if (e != cudaSuccess) {
+    record(GP_ERR_CUDA, e, t_fail_site ? t_fail_site : GP_SITE_LAUNCH);
+    return GP_ERR_CUDA;
+  }
   if (timed) {
     cudaEventRecord(t_last.ev[1], st);
     t_last.timed = true;
@@ -1047,6 +1095,7 @@ int gemm_stats(gp_stats* out, int sync) {
     if (e != cudaSuccess) {
       s.status = GP_ERR_CUDA;
       s.cuda_error = e;
+      s.cuda_error_site = GP_SITE_SYNC;
     } else if (t_last.timed) {
       float ms = -1.f;
       if (cudaEventElapsedTime(&ms, t_last.ev[0], t_last.ev[1]) == cudaSuccess) s.last_ms = ms;
@@ -1074,6 +1123,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
   std::memset(&t_last.stats, 0, sizeof(t_last.stats));
   t_last.status_slot = nullptr;
   t_last.call_id = 0;
+  t_fail_site = 0;
   t_last.stats.last_ms = -1.f;
   t_last.kernel = nullptr;
   t_last.timed = false;
@@ -1100,7 +1150,7 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
   unsigned char* scratch = nullptr;
   uint32_t epoch = 0;
   if (e == cudaSuccess) e = noalloc_setup(dev, &scratch, &epoch);
-  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_DEVICE); return GP_ERR_CUDA; }
   t_last.device = dev;
   t_last.status_slot = status;
   t_last.call_id = call_id;
@@ -1116,11 +1166,11 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
       int pairs = 0;
       e = umma_pair_capacity(dtype, plan.smem_bytes, &pairs);
       if (e == cudaSuccess && pairs < 1) e = cudaErrorLaunchOutOfResources;
-      if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+      if (e != cudaSuccess) { record(GP_ERR_CUDA, e, GP_SITE_CAPACITY); return GP_ERR_CUDA; }
       if (pairs < sms / 2) apply_stream_k(&plan, pairs, 2, true);
     }
     t_last.stats.plan = plan;
-    SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, epoch};
+    SkParams sk{plan.dp_tiles, plan.sk_tiles, nullptr, nullptr, epoch, plan.raster_gm};
     if (plan.sk_tiles > 0) {
       const size_t counter_bytes = static_cast<size_t>(plan.sk_tiles) * (plan.cta_pair ? 2 : 1) * 8;
       if (static_cast<size_t>(plan.workspace_bytes) > kNoAllocPartialBytes || counter_bytes > kNoAllocCounterBytes) {
@@ -1163,7 +1213,10 @@ int gemm_pipelined_noalloc(const void* A, const void* B, void* C, int64_t M, int
     t_last.stats.plan = a.plan;
     t_last.kernel = kernel;
   }
-  if (e != cudaSuccess) { record(GP_ERR_CUDA, e); return GP_ERR_CUDA; }
+  if (e != cudaSuccess) {
+    record(GP_ERR_CUDA, e, t_fail_site ? t_fail_site : GP_SITE_LAUNCH);
+    return GP_ERR_CUDA;
+  }
   record(GP_OK, 0);
   return GP_OK;
 }

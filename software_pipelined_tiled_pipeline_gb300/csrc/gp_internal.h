@@ -61,6 +61,7 @@ struct SkParams {
   float* workspace;         // 2 * grid partial tiles, 128 x BN FP32 each
   uint32_t* flags;          // sk_tiles * CTAs-per-worker 64-bit counters (as 32-bit word pairs)
   uint32_t epoch;           // tag of this launch's counts
+  int32_t raster_gm;        // M blocks per group of the tile raster (gp_plan.raster_gm)
 };
 
 // FP32 FFMA path, K-loop split over k_splits CTAs per tile (plan.k_splits):

@@ -62,9 +62,11 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // Grouped raster: GM consecutive M-blocks share each N-block sweep, so the
-// CTAs resident at one time reuse A and B tiles through L2.
-__device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int& mb, int& nb) {
-  constexpr int GM = 8;
+// CTAs resident at one time reuse A and B tiles through L2 (GM = 8 for the
+// one-tile-per-CTA kernels; the persistent rings take it from the plan).
+constexpr int kRasterGM = 8;
+__device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int& mb, int& nb,
+                                            int GM = kRasterGM) {
   const int per_group = GM * n_blocks;
   const int group = tile / per_group;
   const int first_m = group * GM;
@@ -434,9 +436,10 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
+      const uint64_t keep_a = l2_policy_keep();
       while (!cta->abort && next_item(tile, k0, k1)) {
         int mb, nb;
-        tile_coords(tile, m_blocks, n_blocks, mb, nb);
+        tile_coords(tile, m_blocks, n_blocks, mb, nb, sk.raster_gm);
         const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
         const int n_row = nb * BN + rank * Sh::B_ROWS;
         for (int kb = k0; kb < k1; ++kb) {
@@ -445,12 +448,12 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
           if (PAIR) {
             if (leader) mbar_arrive_expect_tx(&bar->full[s], 2 * STAGE);
             const uint32_t full_leader = mapa_shared(smem_u32(&bar->full[s]), lead_rank);
-            tma_load_2d_pair(smem_u32(slot), &tmA, full_leader, kb * BK, m_row);
+            tma_load_2d_pair_keep(smem_u32(slot), &tmA, full_leader, kb * BK, m_row, keep_a);
             tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
             ++issued;
           } else if (!(ctl.inject_lost_load && tile == tiles - 1 && kb == kt - 1)) {
             mbar_arrive_expect_tx(&bar->full[s], STAGE);
-            tma_load_2d(smem_u32(slot), &tmA, &bar->full[s], kb * BK, m_row);
+            tma_load_2d_keep(smem_u32(slot), &tmA, &bar->full[s], kb * BK, m_row, keep_a);
             tma_load_2d(smem_u32(slot + Sh::A_BYTES), &tmB, &bar->full[s], kb * BK, n_row);
             ++issued;
           }
@@ -512,7 +515,7 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
     int sb = 0;
     for (int t = 0; next_item(tile, k0, k1); ++t) {
       int mb, nb;
-      tile_coords(tile, m_blocks, n_blocks, mb, nb);
+      tile_coords(tile, m_blocks, n_blocks, mb, nb, sk.raster_gm);
       const int a = t & 1;
       // A split tile (stream-K): every segment stores its FP32 partial; the
       // segment that completes last sums all of them in K order and writes C.
@@ -895,7 +898,7 @@ __device__ __forceinline__ bool i8_epi_bar_and(bool pred) {   // the 8 epilogue 
 struct I8Item {
   int mb, n0;     // 256-row block; first column
   bool half;      // 128 columns instead of 256
-  __device__ __forceinline__ void decode(int item, int half_from, int m_blocks, int n_blocks) {
+  __device__ __forceinline__ void decode(int item, int half_from, int m_blocks, int n_blocks, int gm) {
     int tile = item, hs = 0;
     half = item >= half_from;
     if (half) {
@@ -903,7 +906,7 @@ struct I8Item {
       hs = (item - half_from) & 1;
     }
     int nb;
-    tile_coords(tile, m_blocks, n_blocks, mb, nb);
+    tile_coords(tile, m_blocks, n_blocks, mb, nb, gm);
     n0 = nb * 256 + hs * 128;
   }
 };
@@ -986,7 +989,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       uint32_t ph = 0;
       while (!cta->abort && it.next(tile, k0, k1)) {
         I8Item w;
-        w.decode(tile, half_from, m_blocks, n_blocks);
+        w.decode(tile, half_from, m_blocks, n_blocks, sk.raster_gm);
         const int m_row = w.mb * Sh::TILE_M + rank * Sh::A_ROWS;
         // a half item: each CTA of the pair loads 64 of its 128 B rows
         const int n_row = w.n0 + rank * (w.half ? Sh::B_ROWS / 2 : Sh::B_ROWS);
@@ -1065,7 +1068,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     bool ok = true;
     while (ok && it.next(tile, k0, k1)) {
       I8Item wi;
-      wi.decode(tile, half_from, m_blocks, n_blocks);
+      wi.decode(tile, half_from, m_blocks, n_blocks, sk.raster_gm);
       const int mb = wi.mb;
       const int cols = wi.half ? HALF / 2 : HALF;   // accumulator columns of this thread
       // A split tile (stream-K): each segment's int32 partial is exact, so the

@@ -19,6 +19,10 @@ Distributions (the value ranges of the synthetic square GEMM workloads):
 * ``normal``    -- Box-Muller on draws 2i and 2i+1: u1 = ((d >> 11) + 1) * 2^-53,
   u2 = (d >> 11) * 2^-53, z = sqrt(-2 ln u1) cos(2 pi u2), scaled by 1/sqrt(K),
   rounded to float32 and then to bfloat16 (both round-to-nearest-even).
+* ``ternary``   -- sparse integers: +1 if the top 4 bits of the draw are 0, -1
+  if they are 1, else 0 (P(+1) = P(-1) = 1/16); exact in every float type.
+  A product of two such operands has integer entries far below 2^8 at the
+  sizes used here, so its rounded value is the exact sum.
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -114,6 +118,16 @@ def bf16_normal(seed: int, tensor_id: int, shape, K: int) -> np.ndarray:
     return _fill(n, chunk, np.uint16, seed, tensor_id).reshape(shape)
 
 
+def _ternary_chunk(seed, tid, s, c):
+    top = draws(seed, tid, s, c) >> np.uint64(60)
+    return np.where(top == 0, 1, np.where(top == 1, -1, 0)).astype(np.int8)
+
+
+def ternary(seed: int, tensor_id: int, shape) -> np.ndarray:
+    """Sparse {-1, 0, +1} as int8."""
+    return _fill(int(np.prod(shape)), _ternary_chunk, np.int8, seed, tensor_id).reshape(shape)
+
+
 def operands(dtype: str, layout: str, M: int, N: int, K: int, seed: int, dist: str = None):
     """(A, B) numpy arrays in storage layout.
 
@@ -131,6 +145,10 @@ def operands(dtype: str, layout: str, M: int, N: int, K: int, seed: int, dist: s
         ("f16", "uniform"): lambda t, sh: f16_uniform(seed, t, sh),
         ("bf16", "normal"): lambda t, sh: bf16_normal(seed, t, sh, K),
         ("bf16", "uniform"): lambda t, sh: _f32_to_bf16_bits(f32_uniform(seed, t, sh)),
+        ("f16", "ternary"): lambda t, sh: ternary(seed, t, sh).astype(np.float16),
+        ("bf16", "ternary"): lambda t, sh: _f32_to_bf16_bits(ternary(seed, t, sh).astype(np.float32)),
+        ("f32", "ternary"): lambda t, sh: ternary(seed, t, sh).astype(np.float32),
+        ("i8", "ternary"): lambda t, sh: ternary(seed, t, sh),
     }
     fn = gens.get((dtype, dist))
     if fn is None:

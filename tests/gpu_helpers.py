@@ -34,8 +34,9 @@ def run(dtype, layout, A, B, M, N, K, variant="pipelined", stages=0, bn=0, **kw)
     C = buf[GUARD:GUARD + M * N]
     gp.gemm_pipelined(tA, tB, C, M, N, K, dtype, layout, stages, variant, torch.cuda.current_stream(), bn=bn, **kw)
     st = gp.gemm_stats(sync=True)
-    assert st["status"] == 0, "status %d (%s), device word %#x" % (st["status"], gp.strerror(st["status"]),
-                                                                     st["device_status"])
+    assert st["status"] == 0, "status %d (%s), device word %#x, CUDA error %d at %s" % (
+        st["status"], gp.strerror(st["status"]), st["device_status"], st["cuda_error"],
+        gp._binding.SITES.get(st["cuda_error_site"], st["cuda_error_site"]))
     head, tail = buf[:GUARD].cpu(), buf[GUARD + M * N:].cpu()
     if dtype == "i8":
         assert bool((head == -0x54545455).all()) and bool((tail == -0x54545455).all()), "write outside C"
@@ -96,5 +97,5 @@ def check_sampled(dtype, layout, A, B, C, K, rows=None, npts=0, seed=0):
             assert err <= tol, "max err %g > tol %g on sampled points" % (err, tol)
 
 
-def operands(dtype, layout, M, N, K, seed):
-    return synth.operands(dtype, layout, M, N, K, seed)
+def operands(dtype, layout, M, N, K, seed, dist=None):
+    return synth.operands(dtype, layout, M, N, K, seed, dist=dist)

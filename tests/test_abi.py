@@ -44,7 +44,7 @@ def test_library_exports_every_declared_function(gp):
 
 
 def test_version_and_strerror(gp):
-    assert gp.abi_version() == 10600
+    assert gp.abi_version() == 10700
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert gp.strerror(code) and "unknown" not in gp.strerror(code)
     assert "unknown" in gp.strerror(-99)
@@ -351,6 +351,20 @@ def test_one_tile_per_cta_plan(gp):
     assert i["tiles"] == ip["tiles"] == ip["grid"]
     f = gp.gemm_plan(1024, 1024, 1024, "f32", "row_row", 3, "pipelined", plan_sms=152, one_tile_per_cta=True)
     assert (f["k_splits"], f["grid"]) == (1, 64)
+
+
+def test_raster_group_plan(gp):
+    # one raster group over all row blocks while their A panels fit the L2 budget, else groups of 8
+    kw = dict(plan_sms=152)
+    assert gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", **kw)["raster_gm"] == 16
+    assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined", **kw)["raster_gm"] == 16
+    assert gp.gemm_plan(8192, 8192, 4096, "bf16", "row_col", 0, "pipelined", **kw)["raster_gm"] == 8
+    assert gp.gemm_plan(4096, 4096, 16384, "f16", "row_col", 0, "pipelined", **kw)["raster_gm"] == 8
+    assert gp.gemm_plan(1000, 1800, 1040, "bf16", "row_col", 0, "pipelined", **kw)["raster_gm"] == 4
+    assert gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", raster_gm=3, **kw)["raster_gm"] == 3
+    with pytest.raises(gp.GemmError) as ex:
+        gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", raster_gm=-1)
+    assert ex.value.code == gp.GP_ERR_ARG
 
 
 def test_pair_k_split_plan(gp):

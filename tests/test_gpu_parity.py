@@ -160,6 +160,23 @@ def test_all_variants_and_depths_bitwise_identical(dtype):
                            ref.view(torch.int16) if ref.dtype in (torch.float16, torch.bfloat16) else ref)
 
 
+@pytest.mark.parametrize("dtype,M,N,K", [("f16", 2304, 2560, 1032), ("bf16", 1000, 1800, 2056), ("i8", 2048, 3072, 1040)])
+def test_raster_group_does_not_change_results(dtype, M, N, K):
+    # the tile order is scheduling only: every raster group gives the same output (identical bits with
+    # whole tiles; stream-K splits may meet partial sums in another order, within the float bound)
+    lay = LAYOUT[dtype]
+    A, B = operands(dtype, lay, M, N, K, seed=M + N)
+    ref, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", no_stream_k=True)
+    check_full(dtype, lay, A, B, ref, K)
+    for g in (1, 3, 8, 64):
+        C, st = run(dtype, lay, A, B, M, N, K, variant="pipelined", no_stream_k=True, raster_gm=g)
+        assert st["plan"]["raster_gm"] == g
+        assert torch.equal(C.view(torch.int16) if C.dtype != torch.int32 else C,
+                           ref.view(torch.int16) if ref.dtype != torch.int32 else ref)
+        C, _ = run(dtype, lay, A, B, M, N, K, variant="pipelined", raster_gm=g)
+        check_full(dtype, lay, A, B, C, K)
+
+
 def test_repeat_calls_reuse_cached_descriptors():
     A, B = operands("f16", "row_col", 512, 512, 512, seed=2)
     c1, _ = run("f16", "row_col", A, B, 512, 512, 512)

@@ -38,7 +38,10 @@ def test_timeout_is_reported_to_its_own_thread_only():
             t2_read.wait(60)
             res["t1"] = gp.gemm_stats(sync=True)
         except Exception as e:  # surfaced by the assertions below
-            res["t1_err"] = "%r cuda_error %d" % (e, gp.gemm_stats(sync=False)["cuda_error"])
+            st = gp.gemm_stats(sync=False)
+            res["t1_err"] = "%r cuda_error %d at %s, plan %s" % (e, st["cuda_error"],
+                                                            gp._binding.SITES.get(st["cuda_error_site"]),
+                                                            {k: st["plan"][k] for k in ("kernel", "smem_bytes", "grid")})
             k1_done.set()
 
     def t2():
@@ -47,7 +50,8 @@ def test_timeout_is_reported_to_its_own_thread_only():
             k1_done.wait(60)
             res["t2"] = gp.gemm_stats(sync=True)
         except Exception as e:
-            res["t2_err"] = "%r cuda_error %d" % (e, gp.gemm_stats(sync=False)["cuda_error"])
+            st = gp.gemm_stats(sync=False)
+            res["t2_err"] = "%r cuda_error %d at %s" % (e, st["cuda_error"], gp._binding.SITES.get(st["cuda_error_site"]))
         finally:
             t2_read.set()
 

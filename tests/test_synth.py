@@ -51,3 +51,22 @@ def test_chunked_fill_matches_single_draw():
     finally:
         synth._CHUNK = old
     assert np.array_equal(a, synth.int8_uniform(5, 0, (3, 11)))
+
+
+def test_ternary_values_frequencies_and_encodings():
+    A, B = synth.operands("f16", "row_col", 512, 256, 1024, seed=4, dist="ternary")
+    v = A.astype(np.float64)
+    assert set(np.unique(v)) <= {-1.0, 0.0, 1.0}
+    n = v.size
+    for val in (1.0, -1.0):   # P = 1/16 each: within 5 standard deviations
+        assert abs((v == val).sum() - n / 16) < 5 * np.sqrt(n / 16)
+    # every float type holds the same integers exactly; int8 gives the pattern itself
+    Ab, _ = synth.operands("bf16", "row_col", 512, 256, 1024, seed=4, dist="ternary")
+    assert np.array_equal((Ab.astype(np.uint32) << 16).view(np.float32).astype(np.float64), v)
+    Af, _ = synth.operands("f32", "row_col", 512, 256, 1024, seed=4, dist="ternary")
+    Ai, _ = synth.operands("i8", "row_col", 512, 256, 1024, seed=4, dist="ternary")
+    assert np.array_equal(Af.astype(np.float64), v) and np.array_equal(Ai.astype(np.float64), v)
+    # same draws as the int8 stream of the same seed: the top 4 bits decide
+    d = synth.draws(4, 0, 0, 64) >> np.uint64(60)
+    expect = np.where(d == 0, 1, np.where(d == 1, -1, 0))
+    assert np.array_equal(Ai.reshape(-1)[:64], expect)

@@ -67,3 +67,20 @@ def test_noalloc_rejects_other_types_and_handles_empty():
     assert gp.gemm_pipelined_noalloc(dummy, dummy, dummy, 8, 8, 16, "i8", check=False) == gp.GP_ERR_UNSUPPORTED
     assert gp.gemm_pipelined_noalloc(dummy, dummy, dummy, 8, 8, 16, "f32", check=False) == gp.GP_ERR_UNSUPPORTED
     assert gp.gemm_pipelined_noalloc(None, None, None, 0, 8, 16, "f16", check=False) == gp.GP_OK
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_noalloc_exact_integer_products(dtype):
+    # integer-valued operands (sparse -1/0/+1): the exact sums are small integers, so the output
+    # must equal the oracle's exact sum rounded to the output type, bit for bit, on the split path
+    M, N, K = 4096, 4096, 4096
+    A, B = operands(dtype, "row_col", M, N, K, seed=5, dist="ternary")
+    tA, tB = to_dev(A, dtype), to_dev(B, dtype)
+    C = torch.full((M, N), float("nan"), dtype=OUT[dtype], device="cuda")
+    gp.gemm_pipelined_noalloc(tA, tB, C, M, N, K, dtype, 0, torch.cuda.current_stream())
+    st = gp.gemm_stats(sync=True)
+    assert st["status"] == 0 and st["plan"]["sk_tiles"] > 0
+    ref = oracle.gemm_ref(A, B, dtype, "row_col")
+    want = oracle.round_f16(ref) if dtype == "f16" else oracle.round_bf16(ref)
+    got = C.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
