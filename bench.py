@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--workload", default="f16_4096")
     ap.add_argument("--stages", type=int, default=0, help="ring depth (0 = the library's default)")
     ap.add_argument("--variant", default="pipelined")
+    ap.add_argument("--one-tile-per-cta", action="store_true",
+                    help="run the ring on the register-staged kernels' launch shape (one CTA per tile)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep-bf16", action="store_true", default=True,
                     help="include the BF16 stage/ratio sweep (default on)")
@@ -554,9 +556,11 @@ def main():
         if pg is not None:
             pg.barrier()
 
+    launch_opts = {"one_tile_per_cta": True} if args.one_tile_per_cta else {}
+
     def gemm(i):
         a, b, c = bufs[i % len(bufs)]
-        gp.gemm_pipelined(a, b, c, w.M, w.N, w.K, w.dtype, w.layout, args.stages, args.variant, stream)
+        gp.gemm_pipelined(a, b, c, w.M, w.N, w.K, w.dtype, w.layout, args.stages, args.variant, stream, **launch_opts)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -654,7 +658,8 @@ def main():
             stream.wait_event(ev_in[s_])
             if i >= 2:
                 stream.wait_event(ev_out[s_])            # C of set s from two steps back is out
-            gp.gemm_pipelined(dA, dB, dC, w.M, w.N, w.K, w.dtype, w.layout, args.stages, args.variant, stream)
+            gp.gemm_pipelined(dA, dB, dC, w.M, w.N, w.K, w.dtype, w.layout, args.stages, args.variant, stream,
+                              **launch_opts)
             ev_done[s_].record(stream)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(ev_done[s_])
@@ -724,7 +729,8 @@ def main():
                    "l2": "inputs and output rotated over %d buffer sets (%.0f MiB > 129 MB L2)" % (
                        ROTATE, ROTATE * (A.nbytes + B.nbytes + w.M * w.N * (4 if w.dtype in ("i8", "f32") else 2))
                        / 2 ** 20),
-                   "parallelism": "replicas" if world > 1 else "single"},
+                   "parallelism": "replicas" if world > 1 else "single",
+                   **({"one_tile_per_cta": True} if args.one_tile_per_cta else {})},
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
                 "d2h_bytes_per_step": int(hC[0].numel() * hC[0].element_size())},
