@@ -12,7 +12,7 @@ the clocks, and a few scalars of the other configurations (INT8 4096^3 per
 call at the library's default, FP32 1024^3, the like-for-like pipelining
 gain).  The full sweeps (stage depth per configuration, the BF16
 compute/load-ratio sweep, the FFMA register-tile sweep) go to a JSON file
-(--sweep-out, default gpurun_out/bench_sweep.json) and, one short line per
+(--sweep-out, default bench_sweep.json at the repository root) and, one short line per
 configuration, to stdout before the final line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sustained-s", type=float, default=3.0,
                     help="seconds of back-to-back steps for the sustained figure (0 = skip)")
-    ap.add_argument("--sweep-out", default=os.path.join(ROOT, "gpurun_out", "bench_sweep.json"),
+    ap.add_argument("--sweep-out", default=os.path.join(ROOT, "bench_sweep.json"),
                     help="file the full sweep results are written to")
     return ap.parse_args()
 

@@ -143,7 +143,7 @@ def test_final_line_fits_the_driver_tail():
             "fp32_1024": {"TFLOPS": 41.8, "frac_alu": 0.5193, "s2_over_pingpong": 1.79, "pingpong_TFLOPS": 23.3},
             "cpu_baseline": {"value": 0.044698, "unit": "TFLOPS", "cores": 16, "kind": "oracle",
                              "sample": "first 512 of 4096 rows of C in 10.1 s"},
-            "sweep_file": "gpurun_out/bench_sweep.json"}
+            "sweep_file": "bench_sweep.json"}
     out = bench.compact_line(dict(line))
     assert len(json.dumps(out)) < 2000
     for k in ("metric", "value", "unit", "roofline", "e2e", "cpu_baseline", "clocks", "config", "gpu_launches"):
