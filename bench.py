@@ -438,10 +438,11 @@ def _code_only(text):
 
 
 def source_sha(name):
-    """Hash of the code of a kernel source file and the device headers it includes."""
+    """Hash of the code of a kernel source file, the device headers it includes and the planner
+    (which sets the schedule, and so the traffic, of every launch)."""
     csrc = os.path.join(ROOT, "software_pipelined_tiled_pipeline_gb300", "csrc")
     h = hashlib.sha256()
-    for p in (name, "gp_device.cuh", "gp_internal.h"):
+    for p in (name, "gp_device.cuh", "gp_internal.h", "api.cu"):
         with open(os.path.join(csrc, p)) as f:
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
