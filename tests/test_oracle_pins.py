@@ -15,6 +15,7 @@ import torch
 
 import oracle
 from software_pipelined_tiled_pipeline_gb300 import synth
+from software_pipelined_tiled_pipeline_gb300.workloads import BASE_SEED, WORKLOADS
 
 LAYOUTS = ["row_col", "row_row"]
 
@@ -319,6 +320,30 @@ def test_f32_loop_exact_on_dyadic_inputs():
     B = (rng.integers(-32, 33, (K, N)) / 4.0).astype(np.float32)
     assert np.array_equal(oracle.gemm_f32_loop(A, B, "row_row").astype(np.float64),
                           oracle.gemm_ref(A, B, "f32", "row_row"))
+
+
+@pytest.mark.parametrize("wname,rows", [("f32_1024", 16), ("f16_4096", 4), ("bf16_8192_k16384", 2)])
+def test_float_loop_error_is_far_inside_the_tolerance(wname, rows):
+    # Information line: the plain loop with a float accumulator ("Part 4 -- Pipelining and
+    # Occupancy", section 4.3) is what an FP32-accumulating kernel computes in one summation
+    # order.  On rows of the workloads' own inputs its error against the exact sum stays far
+    # inside the parity tolerance, so the tolerance admits every correct FP32 accumulation
+    # order while still being a fraction of max|C|.
+    w = WORKLOADS[wname]
+    A, B = synth.operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
+    r = list(range(rows))
+    ref = oracle.gemm_ref(A, B, w.dtype, w.layout, rows=r)
+    # (FP16 operands are numpy half floats, BF16 ones raw bit patterns)
+    dec = {"f32": lambda x: x, "f16": lambda x: x.astype(np.float32), "bf16": oracle.decode_bf16}[w.dtype]
+    Af = np.asarray(dec(A[:rows]), dtype=np.float32)
+    Bf = np.asarray(dec(B), dtype=np.float32)
+    loop = oracle.gemm_f32_loop(Af, Bf, w.layout).astype(np.float64)
+    err = float(np.max(np.abs(loop - ref)))
+    tol = oracle.tolerance(w.K, ref, "f32")
+    print("%s: FP32 loop max|err| = %.3g, tolerance %.3g (%.2g of it), max|C| %.3g"
+          % (wname, err, tol, err / tol, float(np.max(np.abs(ref)))))
+    assert 0 < err < tol / 100
+    assert tol < 0.1 * float(np.max(np.abs(ref)))
 
 
 def test_rounded_output_is_nearest_of_exact():
