@@ -190,6 +190,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+// Bring the box at (x, y) into L2 without writing anything (a hint: no
+// completion to wait for, and the L2 stays coherent with later writes).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+
 // Load the box at (x = inner coordinate, y = outer coordinate) into shared
 // memory at dst; completion is signalled as transaction bytes on bar.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
