@@ -614,24 +614,25 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->dp_tiles = static_cast<int32_t>(p->tiles);
   p->sk_tiles = 0;
   p->workspace_bytes = 0;
-  if (fam == 0 && sm_count > 0 && p->tiles < sm_count && !no_stream_k && !one_tile) {
-    // FFMA: fewer tiles than SMs -- the tiles' K-loops, laid end to end, are
-    // dealt out as equal ranges to k_splits CTAs per tile (at most
-    // kFfmaMaxSplits, ranges of at least kFfmaMinSplitSteps K steps).  A whole
-    // number of CTAs per tile keeps one segment per CTA: measured at FP32
-    // 1024^3, 2 per tile (128 CTAs) ran 34.6 TFLOP/s, one range per SM (152
-    // CTAs, up to 4 per tile, two segments for most CTAs) 28.3.
-    constexpr int64_t kFfmaMaxSplits = 4, kFfmaMinSplitSteps = 256 / kFfmaSplitK;
-    // (counted in units of kFfmaSplitK K steps for every variant: all cut the K-loop at the same
-    // places; kFfmaMinSplitSteps units are 256 K steps)
-    const int64_t split_steps = ceil_div(K, kFfmaSplitK);
-    int64_t splits = sm_count / p->tiles;
-    if (splits > kFfmaMaxSplits) splits = kFfmaMaxSplits;
-    if (splits > split_steps / kFfmaMinSplitSteps) splits = split_steps / kFfmaMinSplitSteps;
-    if (splits >= 2) {
-      p->k_splits = static_cast<int32_t>(splits);
-      p->grid = static_cast<int32_t>(p->tiles * splits);
-      p->workspace_bytes = 2 * p->tiles * splits * p->bm * p->bn * 4;   // two FP32 partial slots per CTA
+  if (fam == 0 && sm_count > 0 && 2 * p->tiles <= sm_count && !no_stream_k && !one_tile) {
+    // FFMA: at most half as many tiles as SMs -- the tiles' K-loops, laid end to end in
+    // units of kFfmaSplitK K steps, are dealt out as equal contiguous ranges
+    // to one CTA per SM (fewer CTAs when that would leave a range shorter than
+    // kFfmaMinSplitSteps units).  A range meets at most two tiles; the CTA that
+    // completes a shared tile adds its partial sums in K order, so the result
+    // does not depend on timing, and every variant takes the same ranges.
+    // Measured with 32 K steps per slot, interleaved against two CTAs per
+    // tile: FP32 1024^3 51.04 -> 50.66 us; 512 x 512 x 4096 (16 tiles)
+    // 96.1 -> 53.4 us; 1000 x 776 x 2056 96.6 -> 78.4 us.  (With 8 K steps per
+    // slot, one range per SM had measured slower than whole CTAs per tile.)
+    constexpr int64_t kFfmaMinSplitSteps = 256 / kFfmaSplitK;   // units of kFfmaSplitK K steps: 256 K steps
+    const int64_t units = ceil_div(K, kFfmaSplitK) * p->tiles;
+    int64_t grid = units / kFfmaMinSplitSteps;
+    if (grid > sm_count) grid = sm_count;
+    if (grid > p->tiles) {
+      p->grid = static_cast<int32_t>(grid);
+      p->k_splits = static_cast<int32_t>(ceil_div(grid, p->tiles));
+      p->workspace_bytes = 2 * grid * p->bm * p->bn * 4;   // two FP32 partial slots per CTA
     }
   }
   if (fam == 2 && ring && sm_count > 0 && !one_tile) {

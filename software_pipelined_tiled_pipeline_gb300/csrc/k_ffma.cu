@@ -10,8 +10,9 @@
 // register-tile sweep of "Part 4", section 4.3 (larger tiles reuse more from
 // registers until the register file runs out and the compiler spills).
 //
-// When the tiles alone would leave SMs idle, each tile's K-loop is split over
-// plan.k_splits CTAs (see FfmaSplit); every data path splits it the same way.
+// When the tiles alone would leave SMs idle, the tiles' K-loops are dealt out
+// as equal ranges to plan.grid CTAs (see FfmaWork); every data path takes the
+// same ranges.
 //
 // Three data paths for the K-loop, sharing the shared-memory layout (A tile
 // [128][8], B tile [8][128], as a TMA box copy lays them out) and the compute:

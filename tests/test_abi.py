@@ -423,9 +423,16 @@ def test_planner_for_a_152_sm_gb300(gp):
     # 368 tiles leave 64 (more than half a wave): whole tiles only
     assert (wide["tiles"], wide["half_tiles"], wide["sk_tiles"]) == (368, 0, 0)
     f32 = gp.gemm_plan(1024, 1024, 1024, "f32", "row_row", 0, "pipelined", **kw)
-    # 64 tiles: each K-loop shared by two CTAs (128 CTAs), two partial slots per CTA
-    assert (f32["tiles"], f32["k_splits"], f32["grid"]) == (64, 2, 128)
-    assert f32["workspace_bytes"] == 2 * 128 * 128 * 128 * 4
+    # 64 tiles: their K-loops dealt out as equal ranges to one CTA per SM (about 2.4 CTAs per
+    # tile), two partial slots per CTA
+    assert (f32["tiles"], f32["k_splits"], f32["grid"]) == (64, 3, 152)
+    assert f32["workspace_bytes"] == 2 * 152 * 128 * 128 * 4
+    # short K-loops: no range under 256 K steps (4 tiles x 1024 K = 16 ranges)
+    small = gp.gemm_plan(256, 256, 1024, "f32", "row_row", 0, "pipelined", **kw)
+    assert (small["tiles"], small["grid"], small["k_splits"]) == (4, 16, 4)
+    # more than half as many tiles as SMs: whole K-loops
+    half = gp.gemm_plan(1280, 1024, 2048, "f32", "row_row", 0, "pipelined", **kw)
+    assert (half["tiles"], half["grid"], half["k_splits"]) == (80, 80, 1)
     f32_big = gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 0, "pipelined", **kw)
     assert (f32_big["k_splits"], f32_big["grid"], f32_big["workspace_bytes"]) == (1, 1024, 0)
     k256 = gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 0, "pipelined", **kw)

@@ -454,12 +454,14 @@ def test_int8_overlap_back_to_back_and_shape_changes():
 
 @pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (500, 372, 1000), (256, 128, 4104), (130, 260, 2052)])
 def test_ffma_split_k_every_variant(M, N, K):
-    # fewer 128 x 128 tiles than SMs: each tile's K-loop is shared by k_splits
-    # CTAs whose partials are added in split order, the same in every variant
+    # at most half as many 128 x 128 tiles as SMs: the tiles' K-loops are dealt out as equal
+    # ranges (one per SM, or fewer for short K-loops); a shared tile's partials are added in K
+    # order, the same in every variant
     A, B = operands("f32", "row_row", M, N, K, seed=M + 3 * N + K)
     C, st = run("f32", "row_row", A, B, M, N, K, variant="pipelined", stages=3)
     p = st["plan"]
-    assert p["k_splits"] >= 2 and p["grid"] == p["tiles"] * p["k_splits"]
+    units = -(-K // 32) * p["tiles"]
+    assert p["k_splits"] >= 2 and p["grid"] == min(st["sm_count"], units // 8) > p["tiles"]
     check_full("f32", "row_row", A, B, C, K)
     for variant, S in (("pipelined", 2), ("pipelined", 8), ("pingpong", 0), ("nopipe", 0)):
         C2, st2 = run("f32", "row_row", A, B, M, N, K, variant=variant, stages=S)
