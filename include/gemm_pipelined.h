@@ -147,12 +147,13 @@ typedef struct gp_plan {
                                     BM/2 rows of A and BN/2 rows of B; stage_bytes and smem_bytes are per CTA.
                                     3 (gp_options.pair_k_split): a cluster of four CTAs (two such pairs)
                                     shares each 256 x 128 tile, splitting its K-loop in two halves */
-    int32_t k_splits;            /* FP32 FFMA path, at most half as many tiles as SMs: the tiles' K-loops are
-                                    dealt out as equal ranges to `grid` CTAs (one per SM, fewer when a range
-                                    would be under 256 K steps), and k_splits = ceil(grid / tiles) CTAs share
-                                    a tile on average (each writes a partial tile; the CTA that completes a
-                                    tile adds them in K order, so results do not depend on timing);
-                                    1 = whole K-loops */
+    int32_t k_splits;            /* FP32 FFMA path, tiles that would leave SMs idle (at most 3/4 of them busy,
+                                    or a part-empty last wave): the tiles' K-loops are dealt out as equal
+                                    ranges to `grid` CTAs (one per SM, fewer when a range would be under 256 K
+                                    steps); k_splits = the CTAs sharing a tile: ceil(grid / tiles) when ranges
+                                    are shorter than a K-loop, 2 when longer (each writes a partial tile; the
+                                    CTA that completes a tile adds them in K order, so results do not depend
+                                    on timing); 1 = whole K-loops */
     int32_t half_tiles;          /* INT8 on tcgen05: the last tiles (after dp_tiles whole ones), each run as two
                                     BM x BN/2 halves by two workers, when the whole tiles would leave a last
                                     wave at most half full; 0 = none */

@@ -614,24 +614,32 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
   p->dp_tiles = static_cast<int32_t>(p->tiles);
   p->sk_tiles = 0;
   p->workspace_bytes = 0;
-  if (fam == 0 && sm_count > 0 && 2 * p->tiles <= sm_count && !no_stream_k && !one_tile) {
-    // FFMA: at most half as many tiles as SMs -- the tiles' K-loops, laid end to end in
-    // units of kFfmaSplitK K steps, are dealt out as equal contiguous ranges
-    // to one CTA per SM (fewer CTAs when that would leave a range shorter than
-    // kFfmaMinSplitSteps units).  A range meets at most two tiles; the CTA that
-    // completes a shared tile adds its partial sums in K order, so the result
-    // does not depend on timing, and every variant takes the same ranges.
-    // Measured with 32 K steps per slot, interleaved against two CTAs per
-    // tile: FP32 1024^3 51.04 -> 50.66 us; 512 x 512 x 4096 (16 tiles)
-    // 96.1 -> 53.4 us; 1000 x 776 x 2056 96.6 -> 78.4 us.  (With 8 K steps per
-    // slot, one range per SM had measured slower than whole CTAs per tile.)
+  if (fam == 0 && sm_count > 0 && p->tiles % sm_count != 0 && !no_stream_k && !one_tile) {
+    // FFMA: the tiles do not fill whole waves of one CTA per SM.  Where the
+    // whole tiles would leave SMs idle (at most 3/4 of the SMs busy in one
+    // wave, or a part-empty last wave), the tiles' K-loops, laid end to end
+    // in units of kFfmaSplitK K steps, are dealt out as equal contiguous
+    // ranges to one CTA per SM (fewer CTAs when a range would be shorter than
+    // kFfmaMinSplitSteps units).  A range meets a tile at most at its two
+    // ends; the CTA that completes a shared tile adds its partial sums in K
+    // order, so the result does not depend on timing, and every variant takes
+    // the same ranges.  Measured (32 K steps per slot, interleaved, against
+    // whole tiles or two CTAs per tile): 1024^3 51.04 -> 50.66 us; 512 x 512 x
+    // 4096 96.1 -> 53.4 us; 1280^2 x 2048 (100 tiles) 173.8 -> 128.4 us;
+    // 2048^3 344.9 -> 304.0 us; 4096^3 2392.5 -> 2332.4 us.  At 144 tiles on
+    // 152 SMs whole tiles were 1.4 % faster.  (With 8 K steps per slot, one
+    // range per SM had measured slower than whole CTAs per tile.)
     constexpr int64_t kFfmaMinSplitSteps = 256 / kFfmaSplitK;   // units of kFfmaSplitK K steps: 256 K steps
     const int64_t units = ceil_div(K, kFfmaSplitK) * p->tiles;
     int64_t grid = units / kFfmaMinSplitSteps;
     if (grid > sm_count) grid = sm_count;
-    if (grid > p->tiles) {
+    const bool few = 4 * p->tiles <= 3 * sm_count && grid > p->tiles;
+    const bool waves = p->tiles > sm_count && grid == sm_count;
+    if (few || waves) {
       p->grid = static_cast<int32_t>(grid);
-      p->k_splits = static_cast<int32_t>(ceil_div(grid, p->tiles));
+      // CTAs sharing a tile: about grid / tiles of them when ranges are shorter than a
+      // K-loop, at most two when they are longer
+      p->k_splits = static_cast<int32_t>(few ? ceil_div(grid, p->tiles) : 2);
       p->workspace_bytes = 2 * grid * p->bm * p->bn * 4;   // two FP32 partial slots per CTA
     }
   }

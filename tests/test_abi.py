@@ -430,11 +430,17 @@ def test_planner_for_a_152_sm_gb300(gp):
     # short K-loops: no range under 256 K steps (4 tiles x 1024 K = 16 ranges)
     small = gp.gemm_plan(256, 256, 1024, "f32", "row_row", 0, "pipelined", **kw)
     assert (small["tiles"], small["grid"], small["k_splits"]) == (4, 16, 4)
-    # more than half as many tiles as SMs: whole K-loops
+    # 80 tiles would keep 72 SMs idle: ranges as well (a tile shared by about two CTAs)
     half = gp.gemm_plan(1280, 1024, 2048, "f32", "row_row", 0, "pipelined", **kw)
-    assert (half["tiles"], half["grid"], half["k_splits"]) == (80, 80, 1)
+    assert (half["tiles"], half["grid"], half["k_splits"]) == (80, 152, 2)
     f32_big = gp.gemm_plan(4096, 4096, 4096, "f32", "row_row", 0, "pipelined", **kw)
-    assert (f32_big["k_splits"], f32_big["grid"], f32_big["workspace_bytes"]) == (1, 1024, 0)
+    # 1024 tiles leave the seventh wave part-empty: one range of the K-loops per SM (about 6.7
+    # tiles each; a tile is shared by at most two CTAs)
+    assert (f32_big["k_splits"], f32_big["grid"], f32_big["workspace_bytes"]) == (2, 152, 2 * 152 * 128 * 128 * 4)
+    # whole waves, short K-loops, or nearly full single waves keep whole tiles
+    for shape, tiles in (((4096, 4864, 1024), 1216), ((2048, 2048, 64), 256), ((1536, 1536, 2048), 144)):
+        q = gp.gemm_plan(*shape, "f32", "row_row", 0, "pipelined", **kw)
+        assert (q["tiles"], q["grid"], q["k_splits"], q["workspace_bytes"]) == (tiles, tiles, 1, 0), shape
     k256 = gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 0, "pipelined", **kw)
     # K <= 256: one CTA per 128 x 256 tile, persistent over the 152 SMs, whole tiles
     assert (k256["kernel"], k256["cta_pair"], k256["bn"], k256["stages"]) == ("umma_ring", 0, 256, 4)

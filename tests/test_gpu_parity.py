@@ -482,6 +482,27 @@ def test_ffma_thread_tiles_match_the_8x8_bits(tile):
     assert torch.equal(C, ref)
 
 
+def test_ffma_ranges_over_part_empty_waves():
+    # 272 tiles (ragged edges) on one CTA per SM: each CTA takes an equal range of the tiles'
+    # K-loops, longer than one K-loop, so a tile is shared by at most two CTAs
+    M, N, K = 2000, 2100, 520
+    A, B = operands("f32", "row_row", M, N, K, seed=41)
+    C, st = run("f32", "row_row", A, B, M, N, K, variant="pipelined", stages=3)
+    p = st["plan"]
+    assert p["tiles"] > st["sm_count"] and p["grid"] == st["sm_count"] and p["k_splits"] == 2
+    check_full("f32", "row_row", A, B, C, K)
+    for variant, S in (("pipelined", 8), ("pingpong", 0), ("nopipe", 0)):
+        C2, _ = run("f32", "row_row", A, B, M, N, K, variant=variant, stages=S)
+        assert torch.equal(C2, C), (variant, S)
+    # integer-valued operands: every summation order is exact, so the ranges must reproduce
+    # the whole-tile result bit for bit (a K unit lost or added twice would not)
+    A, B = operands("f32", "row_row", M, N, K, seed=42, dist="ternary")
+    C, _ = run("f32", "row_row", A, B, M, N, K, variant="pipelined", stages=3)
+    ref, st = run("f32", "row_row", A, B, M, N, K, variant="pipelined", stages=3, one_tile_per_cta=True)
+    assert st["plan"]["grid"] == st["plan"]["tiles"]
+    assert torch.equal(C, ref)
+
+
 def test_ffma_short_k_is_not_split():
     A, B = operands("f32", "row_row", 128, 128, 40, seed=5)
     C, st = run("f32", "row_row", A, B, 128, 128, 40, variant="pipelined", stages=3)
