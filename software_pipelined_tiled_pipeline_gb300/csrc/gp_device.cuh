@@ -1,9 +1,9 @@
 // gp_device.cuh -- device-side building blocks for the pipelined GEMM kernels
 // (sm_103a): mbarrier phases with bounded waits, TMA tile copies, tcgen05
-// (UMMA + TMEM), ldmatrix / mma.sync and the status word.
+// (UMMA + TMEM), ldmatrix / mma.sync and the per-call status record.
 //
 // Every spin-wait here is bounded: after a time limit it records an error in
-// the caller's status word, raises the CTA's abort flag and returns false, so
+// the call's status record, raises the CTA's abort flag and returns false, so
 // that a lost arrival turns into an error code on the host instead of a hung
 // GPU.  Nothing here traps.
 #pragma once

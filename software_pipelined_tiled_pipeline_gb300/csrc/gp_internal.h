@@ -23,7 +23,7 @@ namespace gp {
 constexpr uint32_t kDevErrTimeout = 1;  // a bounded wait gave up
 constexpr int kStatusSlots = 4096;
 
-// wait-site codes (bits 8.. of the status word) -- which wait gave up
+// wait-site codes (bits 8.. of a status record) -- which wait gave up
 enum WaitSite : uint32_t {
   kSiteProducerEmpty = 1,
   kSiteConsumerFull = 2,
