@@ -341,8 +341,6 @@ int auto_raster_gm(int64_t M, int64_t K, int bm, int in_bytes) {
 
 // FP16/BF16 GEMMs with K up to this many elements run one CTA per tile, not CTA pairs.
 constexpr int64_t kShortK = 256;
-// FP16/BF16 GEMMs with K at least this long default to 5 ring stages (6 below).
-constexpr int64_t kLongK = 4096;
 
 int default_stages(int family) { return family == 0 ? 3 : (family == 1 ? 4 : 6); }
 
@@ -413,10 +411,11 @@ int plan_impl(int64_t M, int64_t N, int64_t K, int dtype, int layout, int stages
     // tile beats the CTA pair (measured at 8192 x 8192 x 256, where C's write
     // dominates); its widest tile fits 4 stages.
     if (stages == 0 && family_of(dtype) == 2 && K <= kShortK && N > 128) S = 4;
-    // Long K-loops run best at 5 stages, short ones at 6 (measured on the
-    // 8192^2 BF16 sweep: 0.99 vs 0.93 of the tensor roof at K = 4096, 0.85 vs
-    // 0.87 at K = 1024; equal at 4096^3).
-    if (stages == 0 && family_of(dtype) == 2 && K >= kLongK) S = 5;
+    // (The 256 x 256 pair tile keeps the default 6 stages at every K: measured
+    // back to back with a pause between interleaved samples, 6 against 5
+    // stages took FP16 4096^3 79.5 against 80.0 us, 4096^2 x 8192 160.9
+    // against 162.8 us, BF16 8192^2 x 4096 285.1 against 287.0 us, 8192^2 x
+    // 8192 572.0 against 575.6 us, and 8192^2 x 16384 1155 against 1152 us.)
     // 64 < N <= 128 (the 256 x 128 pair tile, 24 KB per stage): the operand
     // stream bounds these GEMMs, so keep as many bytes in flight as fit.
     if (stages == 0 && family_of(dtype) == 2 && N > 64 && N <= 128 && M > 128 && K > kShortK) S = kMaxStages;

@@ -129,8 +129,8 @@ def test_umma_pairs_up_to_six_stages(gp, S):
 
 
 def test_default_depth_follows_k(gp):
-    # FP16/BF16 ring: 4 stages at K <= 256 (one CTA per tile), 6 below K = 4096, 5 from there on
-    for K, S in ((256, 4), (1024, 6), (2048, 6), (4096, 5), (16384, 5)):
+    # FP16/BF16 ring: 4 stages at K <= 256 (one CTA per tile), 6 on the 256 x 256 pair tile at every longer K
+    for K, S in ((256, 4), (1024, 6), (2048, 6), (4096, 6), (16384, 6)):
         assert gp.gemm_plan(8192, 8192, K, "bf16", "row_col", 0, "pipelined")["stages"] == S, K
     assert gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined")["stages"] == 6
     # 64 < N <= 128 on the 256 x 128 pair tile: the deepest ring (with the K split: 5, see below)
@@ -399,7 +399,7 @@ def test_planner_for_a_152_sm_gb300(gp):
     kw = dict(plan_sms=152)
     f16 = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", **kw)
     # 256 tiles on 76 pairs: two whole waves, the last 104 tiles' K-loops split evenly (stream-K)
-    assert (f16["kernel"], f16["stages"], f16["bn"], f16["grid"]) == ("umma_pair_ring", 5, 256, 152)
+    assert (f16["kernel"], f16["stages"], f16["bn"], f16["grid"]) == ("umma_pair_ring", 6, 256, 152)
     assert (f16["tiles"], f16["dp_tiles"], f16["sk_tiles"]) == (256, 152, 104)
     assert f16["workspace_bytes"] == 152 * 2 * 128 * 256 * 4
     i8 = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined", **kw)
