@@ -372,31 +372,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 // evict_last policy (ask L2 to keep those lines; measured at FP16 4096^3 with
 // one raster group: 124 against 132 MB of DRAM traffic per launch, 1 % less
 // time); B and C are left to L2's default policy (B with evict_first made the
-// other pairs of a column miss: 188 MB).  GP_L2_KEEP_A=0 builds plain loads.
-#ifndef GP_L2_KEEP_A
-#define GP_L2_KEEP_A 1
-#endif
+// other pairs of a column miss: 188 MB).
 __device__ __forceinline__ uint64_t l2_policy_keep() {
-  uint64_t p = 0;
-#if GP_L2_KEEP_A
+  uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-#endif
   return p;
 }
 
-// tma_load_2d, with the L2 policy of l2_policy_keep() when GP_L2_KEEP_A is set.
+// tma_load_2d with an L2 cache-policy hint (from l2_policy_keep()).
 __device__ __forceinline__ void tma_load_2d_keep(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
                                                  int32_t y, uint64_t policy) {
-#if GP_L2_KEEP_A
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
       "%4}], [%2], %5;" ::"r"(dst),
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
       : "memory");
-#else
-  (void)policy;
-  tma_load_2d(dst, map, bar, x, y);
-#endif
 }
 
 // Store 16 bytes into another CTA's shared memory (cluster-window address).
@@ -406,19 +396,14 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t cluster_addr, float4 v) {
                : "memory");
 }
 
-// tma_load_2d_pair, with the L2 policy of l2_policy_keep() when GP_L2_KEEP_A is set.
+// tma_load_2d_pair with an L2 cache-policy hint (from l2_policy_keep()).
 __device__ __forceinline__ void tma_load_2d_pair_keep(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
                                                       int32_t x, int32_t y, uint64_t policy) {
-#if GP_L2_KEEP_A
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
       "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y), "l"(policy)
       : "memory");
-#else
-  (void)policy;
-  tma_load_2d_pair(dst, map, bar_cluster_addr, x, y);
-#endif
 }
 
 // TMEM management for a CTA pair: one warp of EACH CTA executes these together.
