@@ -289,34 +289,21 @@ def roofline_row(w, kernel, ms, peaks, imma_peak):
 
 def rw_roof_us(w, rw):
     """Least time to move A + B in and C out given the measured copy, pure-read and pure-write
-    bandwidths (GB/s): a stream of writes alone runs well below the copy rate on HBM."""
+    bandwidths (GB/s): the slowest of the three bounds."""
     return max(w.algorithmic_bytes / rw["copy_gbs"], w.read_bytes / rw["read_gbs"],
                w.write_bytes / rw["write_gbs"]) / 1e3
 
 
-def hbm_probe(torch, dev, nbytes=1 << 30, reps=10):
-    """Pure-write (fill), pure-read (sum) and copy bandwidth of this GPU, best of reps, CUDA events."""
-    x = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    y = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    x.fill_(1)
-    xf = x.view(torch.float32)
-
-    def best(fn):
-        ts = []
-        for _ in range(reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return min(ts)
-    out = {"write_gbs": round(nbytes / best(lambda: x.fill_(3)) / 1e6, 1),
-           "read_gbs": round(nbytes / best(lambda: xf.sum()) / 1e6, 1),
-           "copy_gbs": round(2 * nbytes / best(lambda: y.copy_(x)) / 1e6, 1),
-           "how": "torch fill_ / sum / copy_ over 1 GiB, best of %d" % reps}
-    del x, y, xf
+def hbm_probe(torch, gp, dev, stream, nbytes=2 << 30):
+    """Pure-write, pure-read and copy bandwidth of this GPU (GB/s) from the library's own probe
+    kernels (16-byte accesses, grid-stride, best over launch shapes; see gemm_probe.h)."""
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    torch.cuda.synchronize()
+    out = {k + "_gbs": round(gp.probe_hbm(k, buf, stream) / 1e9, 1) for k in ("write", "read", "copy")}
+    out["how"] = "gemm_probe_hbm over %d GiB (copy: half onto half), best of 2/4/8 blocks x 512 threads per SM" % (
+        nbytes >> 30)
+    del buf
     torch.cuda.empty_cache()
     return out
 
@@ -721,7 +708,7 @@ def main():
     if bound == "hbm":
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         gbs = w.algorithmic_bytes / (kavg * 1e-3) / 1e9
-        rw = hbm_probe(torch, dev)
+        rw = hbm_probe(torch, gp, dev, stream)
         roofline.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "algorithmic_bytes": w.algorithmic_bytes,
                          "peak_source": peaks["_source"] + ": copy",
@@ -776,7 +763,7 @@ def main():
         del bufs
         torch.cuda.empty_cache()
         imma_peak = gp.probe_peak("imma_s8", stream) / 1e12
-        rw = hbm_probe(torch, dev) if args.sweep_bf16 else None
+        rw = hbm_probe(torch, gp, dev, stream) if args.sweep_bf16 else None
         sw = sweep(torch, gp, dev, stream, names, extra_steps, peaks, imma_peak, rw)
         full["hbm_probe"] = rw
         full["sweep"] = sw

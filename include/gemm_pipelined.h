@@ -159,6 +159,10 @@ typedef struct gp_plan {
                                     wave at most half full; 0 = none */
     int32_t raster_gm;           /* tile order: groups of raster_gm consecutive BM-row blocks, each group swept
                                     over all N blocks (N block major inside a group), groups in turn */
+    int32_t b_resident;          /* FP16/BF16 one-CTA ring whose K-loop fills the ring exactly (stages ==
+                                    k_tiles, whole tiles only): each CTA takes a contiguous range of tiles in
+                                    M-block-fastest order (raster_gm = all M blocks) and keeps the B tile in
+                                    the ring while the N block repeats, so only A is loaded; 0 = off */
 } gp_plan;
 
 /* Record of the last gemm_pipelined call made by the calling host thread. */

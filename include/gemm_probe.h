@@ -13,6 +13,8 @@
 #ifndef GEMM_PROBE_H
 #define GEMM_PROBE_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -29,6 +31,31 @@ extern "C" {
  * Allocates nothing.
  */
 int gemm_probe_peak(int kind, double* ops_per_s, void* stream);
+
+/*
+ * HBM bandwidth ceilings for the kernels whose roof is memory: the GEMMs with
+ * few K steps write C far more than they read (store-bound), the skinny ones
+ * read A once (load-bound).  Each is measured with 16-byte accesses by a
+ * grid-stride kernel over a caller-supplied device buffer, so that the
+ * denominators come from this GPU rather than from a nominal figure.
+ */
+#define GP_PROBE_HBM_WRITE 2 /* stores only: bytes written per second over the whole buffer */
+#define GP_PROBE_HBM_READ 3  /* loads only: bytes read per second over the whole buffer */
+#define GP_PROBE_HBM_COPY 4  /* first half copied to the second: bytes read + bytes written per second */
+
+/*
+ * gemm_probe_hbm -- time the access pattern `kind` over the device buffer
+ * `buf` of `bytes` bytes (owned by the caller, 16-byte aligned, at least
+ * 1 MiB and a multiple of 32 bytes; its contents are overwritten by the
+ * write and copy probes) on `stream` (cudaStream_t as void*, NULL = default
+ * stream), five timed launches (each after an untimed one) for each of 2, 4
+ * and 8 blocks of 512 threads per SM, and store the best rate in *bytes_per_s.  Use a
+ * buffer far larger than the L2 (hundreds of MB or more) so that the rate is
+ * that of HBM.  Synchronous.  Returns 0, GP_ERR_ARG (-1) for a bad kind, a
+ * NULL pointer, a misaligned or too small buffer, or GP_ERR_CUDA (-4).
+ * Allocates nothing.
+ */
+int gemm_probe_hbm(int kind, void* buf, size_t bytes, double* bytes_per_s, void* stream);
 
 #ifdef __cplusplus
 }

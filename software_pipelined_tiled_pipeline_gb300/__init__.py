@@ -10,7 +10,7 @@ synthetic operands.
 from ._binding import (  # noqa: F401
     DTYPES, LAYOUTS, VARIANTS, GP_OK, GP_ERR_ARG, GP_ERR_UNSUPPORTED, GP_ERR_SMEM, GP_ERR_CUDA, GP_ERR_TIMEOUT,
     GP_ERR_SIZE, GP_ERR_SCRATCH, GemmError, abi_version, gemm_pipelined, gemm_pipelined_noalloc, gemm_plan,
-    gemm_plan_rc, gemm_stats, probe_peak, release, strerror, lib,
+    gemm_plan_rc, gemm_stats, probe_hbm, probe_peak, release, strerror, lib,
 )
 
 _OUT_DTYPE = {"i8": "int32", "f16": "float16", "bf16": "bfloat16", "f32": "float32"}

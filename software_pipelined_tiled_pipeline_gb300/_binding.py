@@ -41,7 +41,8 @@ VARIANTS = {"pingpong": GP_PINGPONG, "pipelined": GP_PIPELINED, "nopipe": GP_NOP
 
 # exported symbols, in header order
 SYMBOLS = ["gemm_pipelined", "gemm_pipelined_ex", "gemm_plan", "gemm_plan_ex", "gemm_stats", "gemm_strerror",
-           "gemm_abi_version", "gemm_release", "gemm_pipelined_noalloc", "gemm_probe_peak"]
+           "gemm_abi_version", "gemm_release", "gemm_pipelined_noalloc", "gemm_probe_peak",
+           "gemm_probe_hbm"]
 
 
 class GpPlan(ctypes.Structure):
@@ -54,7 +55,7 @@ class GpPlan(ctypes.Structure):
         ("compute_load_ratio", ctypes.c_double), ("kernel", ctypes.c_char_p),
         ("dp_tiles", ctypes.c_int32), ("sk_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
         ("cta_pair", ctypes.c_int32), ("k_splits", ctypes.c_int32), ("half_tiles", ctypes.c_int32),
-        ("raster_gm", ctypes.c_int32),
+        ("raster_gm", ctypes.c_int32), ("b_resident", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -125,6 +126,8 @@ def lib():
     L.gemm_pipelined_noalloc.restype = ci
     L.gemm_probe_peak.argtypes = [ci, ctypes.POINTER(ctypes.c_double), vp]
     L.gemm_probe_peak.restype = ci
+    L.gemm_probe_hbm.argtypes = [ci, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_double), vp]
+    L.gemm_probe_hbm.restype = ci
     _lib = L
     return L
 
@@ -256,4 +259,19 @@ def probe_peak(kind, stream=0) -> float:
     rc = lib().gemm_probe_peak(_enum(kind, PROBES, "probe"), ctypes.byref(out), s or None)
     if rc != GP_OK:
         raise GemmError(rc, "gemm_probe_peak")
+    return out.value
+
+
+HBM_PROBES = {"write": 2, "read": 3, "copy": 4}
+
+
+def probe_hbm(kind, buf, stream=0) -> float:
+    """Measured HBM bytes/s of 16-byte stores, loads or a copy over the device tensor `buf`
+    (see include/gemm_probe.h; the write and copy probes overwrite it)."""
+    out = ctypes.c_double(0.0)
+    s = getattr(stream, "cuda_stream", stream)
+    rc = lib().gemm_probe_hbm(_enum(kind, HBM_PROBES, "HBM probe"), _ptr(buf), buf.numel() * buf.element_size(),
+                              ctypes.byref(out), s or None)
+    if rc != GP_OK:
+        raise GemmError(rc, "gemm_probe_hbm")
     return out.value

@@ -62,6 +62,7 @@ struct SkParams {
   uint32_t* flags;          // sk_tiles * CTAs-per-worker 64-bit counters (as 32-bit word pairs)
   uint32_t epoch;           // tag of this launch's counts
   int32_t raster_gm;        // M blocks per group of the tile raster (gp_plan.raster_gm)
+  int32_t b_resident;       // contiguous tile ranges per worker, B kept in the ring (gp_plan.b_resident)
 };
 
 // FP32 FFMA path, K-loop split over k_splits CTAs per tile (plan.k_splits):

@@ -162,7 +162,9 @@ __device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint32_t a_addr, ui
 // the fix-up of a split tile takes 6-8 us after its last MMA); one whole tile
 // goes first because all workers then start on neighbouring tiles at K step
 // 0, whose operands they share in L2 (measured +2 % at 4096^3).  An item is
-// (tile, first K step, one past the last K step).
+// (tile, first K step, one past the last K step).  With B kept in the ring
+// (SkParams.b_resident) a worker instead walks one contiguous run of whole
+// tiles, so that consecutive tiles share their N block.
 struct WorkIter {
   int dp_tiles, kt, next_dp, step;
   int64_t u, u_end;
@@ -172,11 +174,19 @@ struct WorkIter {
     return static_cast<int64_t>(w) * units / workers;
   }
   __device__ __forceinline__ void init(const SkParams& sk, int kt_, int worker, int workers) {
-    dp_tiles = sk.dp_tiles;
     kt = kt_;
+    first_done = false;
+    if (sk.b_resident) {
+      // whole tiles only: worker w takes the contiguous run [w T / W, (w + 1) T / W)
+      next_dp = static_cast<int>(range_start(worker, sk.dp_tiles, workers));
+      dp_tiles = static_cast<int>(range_start(worker + 1, sk.dp_tiles, workers));
+      step = 1;
+      u = u_end = 0;
+      return;
+    }
+    dp_tiles = sk.dp_tiles;
     next_dp = worker;
     step = workers;
-    first_done = false;
     const int64_t units = static_cast<int64_t>(sk.sk_tiles) * kt;
     u = range_start(worker, units, workers);
     u_end = range_start(worker + 1, units, workers);
@@ -467,11 +477,18 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       const uint64_t keep_a = l2_policy_keep();
+      int held_nb = -1;   // N block whose B tile fills the ring's B halves, slot kb holding K step kb
       while (!cta->abort && next_item(tile, k0, k1)) {
         int mb, nb;
         tile_coords(tile, m_blocks, n_blocks, mb, nb, sk.raster_gm);
         const int m_row = mb * Sh::TILE_M + rank * Sh::A_ROWS;
         const int n_row = nb * BN + rank * Sh::B_ROWS;
+        // A whole K-loop in a ring of exactly kt slots puts K step kb in slot kb
+        // for every tile, so a repeated N block finds its B tile still there: no
+        // write ever reaches a slot's B half while that is so.
+        const bool whole_ring = !PAIR && sk.b_resident && k0 == 0 && k1 == kt && kt == stages && s == 0;
+        const bool keep_b = whole_ring && nb == held_nb;
+        held_nb = whole_ring ? nb : -1;
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&bar->empty[s], ph ^ 1u, ctl, cta, kSiteProducerEmpty)) goto producer_done;
           uint8_t* slot = ring + s * STAGE;
@@ -482,9 +499,9 @@ __global__ void __launch_bounds__(RingShape<BN, PAIR>::THREADS, 1)
             tma_load_2d_pair(smem_u32(slot + Sh::A_BYTES), &tmB, full_leader, kb * BK, n_row);
             ++issued;
           } else if (!(ctl.inject_lost_load && tile == tiles - 1 && kb == kt - 1)) {
-            mbar_arrive_expect_tx(&bar->full[s], STAGE);
+            mbar_arrive_expect_tx(&bar->full[s], keep_b ? Sh::A_BYTES : STAGE);
             tma_load_2d_keep(smem_u32(slot), &tmA, &bar->full[s], kb * BK, m_row, keep_a);
-            tma_load_2d(smem_u32(slot + Sh::A_BYTES), &tmB, &bar->full[s], kb * BK, n_row);
+            if (!keep_b) tma_load_2d(smem_u32(slot + Sh::A_BYTES), &tmB, &bar->full[s], kb * BK, n_row);
             ++issued;
           }
           if (++s == stages) { s = 0; ph ^= 1u; }

@@ -114,6 +114,22 @@ def test_call_argument_errors_need_no_device(gp):
     assert st["status"] == 0
 
 
+def test_hbm_probe_argument_errors_need_no_device(gp):
+    import ctypes
+    f = gp.lib().gemm_probe_hbm
+    out = ctypes.c_double(0.0)
+    ok_ptr, mib = 0x10000, 1 << 20
+    assert f(2, None, mib, ctypes.byref(out), None) == gp.GP_ERR_ARG          # no buffer
+    assert f(2, ok_ptr, mib, None, None) == gp.GP_ERR_ARG                     # no output
+    assert f(5, ok_ptr, mib, ctypes.byref(out), None) == gp.GP_ERR_ARG        # not an HBM probe
+    assert f(0, ok_ptr, mib, ctypes.byref(out), None) == gp.GP_ERR_ARG        # (the IMMA probe kind)
+    assert f(3, ok_ptr + 8, mib, ctypes.byref(out), None) == gp.GP_ERR_ARG    # misaligned
+    assert f(3, ok_ptr, mib - 32, ctypes.byref(out), None) == gp.GP_ERR_ARG   # under 1 MiB
+    assert f(4, ok_ptr, mib + 16, ctypes.byref(out), None) == gp.GP_ERR_ARG   # not whole 32-byte pairs
+    with pytest.raises(ValueError):
+        gp.probe_hbm("sum", None)
+
+
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 5, 6])
 def test_umma_pairs_up_to_six_stages(gp, S):
     # CTA pair: 256 x 256 tile per pair, each CTA 128 rows of A and 128 of B = 32 KB per K step
@@ -167,10 +183,35 @@ def test_short_k_runs_one_cta_per_tile(gp):
     for K in (64, 200, 256):
         p = gp.gemm_plan(8192, 8192, K, "bf16", "row_col", 0, "pipelined")
         assert (p["cta_pair"], p["bn"], p["stages"]) == (0, 256, 4), K
+        # (with SMs queried, K = 200 and 256 keep B in the ring at one slot per K step: still 4)
     p = gp.gemm_plan(8192, 8192, 320, "bf16", "row_col", 0, "pipelined")
     assert (p["cta_pair"], p["stages"]) == (1, 6)
     assert gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 6, "pipelined")["cta_pair"] == 0
     assert gp.gemm_plan(8192, 128, 256, "bf16", "row_col", 0, "pipelined")["stages"] == 6   # N <= 128: BN 128
+
+
+def test_b_resident_plan(gp):
+    # a K-loop of 2-4 steps that fills the ring, whole tiles, more tiles than SMs: one slot per K step,
+    # contiguous tile runs in M-block-fastest order, B kept in the ring while the N block repeats
+    kw = dict(plan_sms=152)
+    for K, kt in ((128, 2), (192, 3), (200, 4), (256, 4)):
+        p = gp.gemm_plan(8192, 8192, K, "bf16", "row_col", 0, "pipelined", **kw)
+        assert (p["b_resident"], p["stages"], p["k_tiles"], p["raster_gm"], p["bn"], p["cta_pair"]) == \
+            (1, kt, kt, 64, 256, 0), K
+        assert p["ring_bytes"] == kt * (128 + 256) * 64 * 2
+        assert p["smem_bytes"] == max(1024 + p["ring_bytes"] + 32768 + 256, 232448 // 2 + 1024)
+    assert gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 4, "pipelined", **kw)["b_resident"] == 1
+    assert gp.gemm_plan(2000, 5000, 192, "f16", "row_col", 0, "pipelined", **kw)["b_resident"] == 1
+    # streamed: one K step, a depth other than the K-loop, a raster chosen by the caller, one tile per
+    # CTA, fewer tiles than SMs, and K beyond the ring (the CTA pair)
+    assert gp.gemm_plan(8192, 8192, 64, "bf16", "row_col", 0, "pipelined", **kw)["b_resident"] == 0
+    assert gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 3, "pipelined", **kw)["b_resident"] == 0
+    assert gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 0, "pipelined", raster_gm=8, **kw)["b_resident"] == 0
+    assert gp.gemm_plan(8192, 8192, 256, "bf16", "row_col", 0, "pipelined", one_tile_per_cta=True,
+                        **kw)["b_resident"] == 0
+    assert gp.gemm_plan(1024, 1024, 256, "bf16", "row_col", 0, "pipelined", **kw)["b_resident"] == 0
+    assert gp.gemm_plan(8192, 8192, 512, "bf16", "row_col", 0, "pipelined", **kw)["b_resident"] == 0
+    assert gp.gemm_plan(4096, 4096, 256, "i8", "row_col", 0, "pipelined", **kw)["b_resident"] == 0
 
 
 @pytest.mark.parametrize("S", range(1, 9))

@@ -177,6 +177,26 @@ def test_raster_group_does_not_change_results(dtype, M, N, K):
         check_full(dtype, lay, A, B, C, K)
 
 
+@pytest.mark.parametrize("dtype,M,N,K", [("bf16", 2000, 5000, 192), ("f16", 2048, 4096, 256), ("bf16", 4100, 2000, 128),
+                                         ("f16", 1300, 9000, 200)])
+def test_b_resident_short_k(dtype, M, N, K):
+    # a K-loop that fills the ring: each CTA walks a contiguous run of tiles and keeps the B tile in
+    # the ring while the N block repeats (ragged M, N and K edges included); every tile runs the same
+    # MMAs in the same order as on the streamed ring, so the bits are the same
+    lay = "row_col"
+    A, B = operands(dtype, lay, M, N, K, seed=M + K)
+    C, st = run(dtype, lay, A, B, M, N, K)
+    p = st["plan"]
+    assert p["b_resident"] == 1 and p["stages"] == p["k_tiles"] and p["raster_gm"] == -(-M // 128)
+    check_full(dtype, lay, A, B, C, K)
+    C2, st2 = run(dtype, lay, A, B, M, N, K, raster_gm=8)
+    assert st2["plan"]["b_resident"] == 0
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+    # back to back on one stream
+    C3, _ = run(dtype, lay, A, B, M, N, K)
+    assert torch.equal(C.view(torch.int16), C3.view(torch.int16))
+
+
 def test_repeat_calls_reuse_cached_descriptors():
     A, B = operands("f16", "row_col", 512, 512, 512, seed=2)
     c1, _ = run("f16", "row_col", A, B, 512, 512, 512)
