@@ -157,6 +157,8 @@ __device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint32_t a_addr, ui
 // whole tile (w), then its contiguous range of the stream-K units (one unit =
 // one K step of one of the sk_tiles tiles after the whole ones), cut at tile
 // boundaries, then its other whole tiles (w+W, w+2W, ... below dp_tiles).
+// (The split tiles are those left after the full waves, or after all but the
+// last full wave with a shallow ring: the planner decides.)
 // The split tiles come before the last whole tiles so that their partial-tile
 // traffic and fix-ups overlap MMAs instead of trailing the kernel (measured:
 // the fix-up of a split tile takes 6-8 us after its last MMA); one whole tile

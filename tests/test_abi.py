@@ -439,10 +439,19 @@ def test_planner_for_a_152_sm_gb300(gp):
     # the launch-time decisions, planned for a GB300's 152 SMs (76 CTA pairs) without a device
     kw = dict(plan_sms=152)
     f16 = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", **kw)
-    # 256 tiles on 76 pairs: two whole waves, the last 104 tiles' K-loops split evenly (stream-K)
+    # 256 tiles on 76 pairs: three whole waves, the 28 tiles left over split evenly (stream-K)
     assert (f16["kernel"], f16["stages"], f16["bn"], f16["grid"]) == ("umma_pair_ring", 6, 256, 152)
-    assert (f16["tiles"], f16["dp_tiles"], f16["sk_tiles"]) == (256, 152, 104)
+    assert (f16["tiles"], f16["dp_tiles"], f16["sk_tiles"]) == (256, 228, 28)
     assert f16["workspace_bytes"] == 152 * 2 * 128 * 256 * 4
+    # a ring of at most 4 slots splits the last full wave too: two whole waves, 104 split tiles
+    for S in (2, 3, 4):
+        q = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", S, "pipelined", **kw)
+        assert (q["dp_tiles"], q["sk_tiles"], q["grid"]) == (152, 104, 152), S
+    q = gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 5, "pipelined", **kw)
+    assert (q["dp_tiles"], q["sk_tiles"]) == (228, 28)
+    # 8192^2 x 16384 on the 6-slot ring: 1024 tiles, 13 whole waves, 36 split tiles
+    big = gp.gemm_plan(8192, 8192, 16384, "bf16", "row_col", 0, "pipelined", **kw)
+    assert (big["tiles"], big["dp_tiles"], big["sk_tiles"]) == (1024, 988, 36)
     i8 = gp.gemm_plan(4096, 4096, 4096, "i8", "row_col", 0, "pipelined", **kw)
     # three whole waves, then the 28 tiles left over as 56 half tiles on 56 pairs
     assert (i8["kernel"], i8["stages"], i8["grid"], i8["sk_tiles"]) == ("umma_i8_pair_ring", 6, 152, 0)

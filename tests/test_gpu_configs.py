@@ -53,13 +53,21 @@ def test_f16_4096_sampled_and_stage_invariant():
     w = WORKLOADS["f16_4096"]
     A, B = operands(w.dtype, w.layout, w.M, w.N, w.K, BASE_SEED)
     rows = list(range(0, 4096, 67)) + [4095]
-    # the benchmark's launch: TMA ring on CTA pairs, 4 stages
+    # TMA ring on CTA pairs at 4 stages: two whole waves, the K-loops of the last 104 tiles split
     C, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4)
-    assert st["plan"]["cta_pair"] == 1
+    assert st["plan"]["cta_pair"] == 1 and (st["plan"]["dp_tiles"], st["plan"]["sk_tiles"]) == (152, 104)
     check_sampled(w.dtype, w.layout, A, B, C, w.K, rows=rows, npts=4000, seed=1)
-    for S in (2, 3, 6):
-        C2, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
+    for S in (2, 3):
+        C2, st2 = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=S)
+        assert st2["plan"]["sk_tiles"] == 104
         assert torch.equal(_bits(C2), _bits(C))
+    # 5 and 6 stages (the default) split only the 28 tiles left after three whole waves: the same
+    # split at both depths, so the same bits; other tiles' partial sums meet in another order
+    C6, st6 = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=6)
+    assert (st6["plan"]["dp_tiles"], st6["plan"]["sk_tiles"]) == (228, 28)
+    check_sampled(w.dtype, w.layout, A, B, C6, w.K, rows=rows, npts=4000, seed=4)
+    C5, _ = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=5)
+    assert torch.equal(_bits(C5), _bits(C6))
     # one CTA per tile, whole tiles: every variant and depth runs the same MMA sequence
     ref, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4, no_stream_k=True,
                   no_cta_pair=True)
@@ -76,7 +84,7 @@ def test_f16_4096_sampled_and_stage_invariant():
     C3, st = run(w.dtype, w.layout, A, B, w.M, w.N, w.K, variant="pipelined", stages=4, no_cta_pair=True)
     assert st["plan"]["sk_tiles"] > 0
     check_sampled(w.dtype, w.layout, A, B, C3, w.K, rows=rows, npts=4000, seed=3)
-    for other in (C, C3):
+    for other in (C, C3, C6):
         diff = (other.float() - ref.float()).abs().max().item()
         assert diff <= 2.0 ** -6 * ref.float().abs().max().item()
 

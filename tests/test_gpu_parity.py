@@ -243,6 +243,29 @@ def test_stream_k_split_tiles(dtype, M, N, K, S):
     assert diff <= 2.0 ** -6 * C2.float().abs().max().item()
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_stream_k_split_follows_the_ring_depth(dtype):
+    # 99 pair tiles (ragged M, N, K): a ring of 5 or more slots keeps the full wave whole and splits
+    # the tiles left over; a ring of at most 4 splits the full wave too.  Both match the oracle, and
+    # depths with the same split give the same bits
+    lay = "row_col"
+    M, N, K = 2800, 2296, 2056
+    A, B = operands(dtype, lay, M, N, K, seed=99)
+    C6, st6 = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=6)
+    p6 = st6["plan"]
+    G, T = st6["sm_count"] // 2, p6["tiles"]
+    assert p6["cta_pair"] == 1 and T == 99 and T > G
+    assert (p6["dp_tiles"], p6["sk_tiles"]) == ((T // G) * G, T - (T // G) * G)
+    check_full(dtype, lay, A, B, C6, K)
+    C5, _ = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=5)
+    assert torch.equal(C5.view(torch.int16), C6.view(torch.int16))
+    C4, st4 = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=4)
+    assert (st4["plan"]["dp_tiles"], st4["plan"]["sk_tiles"]) == ((T // G - 1) * G, T - (T // G - 1) * G)
+    check_full(dtype, lay, A, B, C4, K)
+    C3, _ = run(dtype, lay, A, B, M, N, K, variant="pipelined", stages=3)
+    assert torch.equal(C3.view(torch.int16), C4.view(torch.int16))
+
+
 def test_stream_k_repeated_launches_reuse_workspace():
     # flags carry a per-launch epoch: back-to-back launches on one stream stay correct
     A, B = operands("f16", "row_col", 1024, 1024, 4096, seed=9)
