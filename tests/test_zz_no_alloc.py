@@ -84,3 +84,26 @@ def test_noalloc_exact_integer_products(dtype):
     want = oracle.round_f16(ref) if dtype == "f16" else oracle.round_bf16(ref)
     got = C.cpu().view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_noalloc_short_k_keeps_b_in_the_ring(dtype):
+    # K = 192 (3 K steps): one CTA per 128 x 256 tile with B kept in the ring; no workspace at all,
+    # and the same bits as the allocating entry point
+    M, N, K = 2048, 4096, 192
+    A, B = operands(dtype, "row_col", M, N, K, seed=11)
+    tA, tB = to_dev(A, dtype), to_dev(B, dtype)
+    stream = torch.cuda.current_stream()
+    ref = torch.empty((M, N), dtype=OUT[dtype], device="cuda")
+    gp.gemm_pipelined(tA, tB, ref, M, N, K, dtype, "row_col", 0, "pipelined", stream)
+    assert gp.gemm_stats(sync=True)["status"] == 0
+    C = torch.full((M, N), float("nan"), dtype=OUT[dtype], device="cuda")
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    gp.gemm_pipelined_noalloc(tA, tB, C, M, N, K, dtype, 0, stream)
+    st = gp.gemm_stats(sync=True)
+    assert st["status"] == 0
+    assert st["plan"]["b_resident"] == 1 and st["plan"]["sk_tiles"] == 0 and st["plan"]["stages"] == 3
+    assert torch.cuda.mem_get_info()[0] >= free_before - (8 << 20)
+    assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    check_sampled(dtype, "row_col", A, B, C.cpu(), K, npts=500, seed=4)
