@@ -379,6 +379,14 @@ __device__ __forceinline__ uint64_t l2_policy_keep() {
   return p;
 }
 
+// 16-byte global store with an L2 cache-policy hint (from l2_policy_keep()).
+__device__ __forceinline__ void st_global_v4_hint(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                  uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(a), "r"(b), "r"(c),
+               "r"(d), "l"(policy)
+               : "memory");
+}
+
 // tma_load_2d with an L2 cache-policy hint (from l2_policy_keep()).
 __device__ __forceinline__ void tma_load_2d_keep(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
                                                  int32_t y, uint64_t policy) {
