@@ -498,3 +498,54 @@ def test_planner_for_a_152_sm_gb300(gp):
     assert gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined")["grid"] == 0   # no device queried
     with pytest.raises(gp.GemmError):
         gp.gemm_plan(4096, 4096, 4096, "f16", "row_col", 0, "pipelined", plan_sms=-1)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "i8", "f32"])
+def test_plan_invariants_over_many_shapes(gp, dtype):
+    # planned for a 152-SM GB300 without a device: whatever the shape and depth, the work split is
+    # a partition of the tiles, the launch fits the SMs and shared memory, and each schedule's own
+    # rules hold
+    import itertools
+    lay = "row_row" if dtype == "f32" else "row_col"
+    sizes = (64, 128, 200, 520, 1000, 2048, 4104, 8192)
+    ks = (16, 64, 128, 192, 256, 320, 1032, 4096, 16384)
+    seen = set()
+    for M, N, K in itertools.product(sizes, sizes, ks):
+        if dtype == "f32" and K % 4:
+            continue
+        for S in (0, 2, 4, 6):
+            rc = gp.gemm_plan_rc(M, N, K, dtype, lay, S, "pipelined")
+            if rc != 0:
+                continue
+            p = gp.gemm_plan(M, N, K, dtype, lay, S, "pipelined", plan_sms=152)
+            tiles, grid, dp, sk = p["tiles"], p["grid"], p["dp_tiles"], p["sk_tiles"]
+            seen.update(k for k in ("b_resident", "half_tiles") if p[k])
+            seen.update(["split after whole waves"] if sk and dp else ["split only"] if sk else [])
+            seen.update(["k-split cluster"] if p["cta_pair"] == 3 else [])
+            seen.update(["ffma ranges"] if p["k_splits"] > 1 else [])
+            assert tiles == -(-M // p["bm"]) * -(-N // p["bn"]), (M, N, K, S)
+            assert p["k_tiles"] == -(-K // p["bk"])
+            assert 0 < grid <= 152 or (not p["persistent"] and grid == tiles)
+            assert p["smem_bytes"] <= 232448 and 1 <= p["stages"] <= 8
+            if dtype in ("f16", "bf16"):
+                # whole tiles then split ones: the split tiles are the last, whole waves before them
+                assert dp + sk == tiles and 0 <= sk
+                workers = grid // (2 if p["cta_pair"] else 1)
+                if sk:
+                    assert p["cta_pair"] != 3 and p["workspace_bytes"] > 0
+                    assert dp % workers == 0 and sk <= (2 if p["stages"] <= 4 else 1) * workers
+                if p["b_resident"]:
+                    assert (p["cta_pair"], sk) == (0, 0) and p["stages"] == p["k_tiles"] >= 2
+                    assert tiles > grid and p["raster_gm"] == -(-M // p["bm"])
+                if p["cta_pair"] == 3:
+                    assert grid % 4 == 0 and tiles <= grid // 4
+            elif dtype == "i8" and p["cta_pair"]:
+                assert dp + sk + p["half_tiles"] == tiles or dp + sk == tiles
+                assert not (sk and p["half_tiles"])
+            elif dtype == "f32":
+                assert p["k_splits"] >= 1 and (p["k_splits"] == 1) == (p["workspace_bytes"] == 0)
+    # the sizes reach every schedule of the type
+    want = {"f16": {"b_resident", "split after whole waves", "split only", "k-split cluster"},
+            "bf16": {"b_resident", "split after whole waves", "split only", "k-split cluster"},
+            "i8": {"half_tiles", "split only"}, "f32": {"ffma ranges"}}[dtype]
+    assert want <= seen, want - seen
