@@ -5,13 +5,14 @@ One step = one GEMM over the workload (all steps of the K-loop hot path:
 tile decomposition, prologue, steady-state ring, drain, output epilogue).
 Default workload: FP16 GEMM M=N=K=4096, A row-major, B column-major, FP32
 accumulate, FP16 out, TMA-ring tcgen05 kernel on CTA pairs at the library's
-default depth (5 stages at this shape).  The last line on stdout (rank 0)
+default depth (6 stages at this shape).  The last line on stdout (rank 0)
 is one compact JSON object (under 2 KB): the headline, its roofline, the
 end-to-end rate through the C ABI with host buffers, the CPU oracle baseline,
 the clocks, and a few scalars of the other configurations (INT8 4096^3 per
 call at the library's default, FP32 1024^3, the like-for-like pipelining
 gain).  The full sweeps (stage depth per configuration, the BF16
-compute/load-ratio sweep, the FFMA register-tile sweep) go to a JSON file
+compute/load-ratio sweep with the HBM rows' read/write roof from the
+library's own bandwidth probe, the FFMA register-tile sweep) go to a JSON file
 (--sweep-out, default bench_sweep.json at the repository root) and, one short line per
 configuration, to stdout before the final line.
 
